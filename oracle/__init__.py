@@ -1,0 +1,179 @@
+"""Plain CPU oracle for the BitNet b1.58 BitLinear forward.
+
+TEST INFRASTRUCTURE ONLY.  Only the test-suite, ``__graft_entry__.smoke()`` and
+the ``cpu_baseline`` / reference leg of ``bench.py`` may import this package.
+The CUDA library never calls it, and it never calls the CUDA library: the two
+share no code.
+
+The arithmetic lives in ``bitlinear_oracle.c`` (plain C loops, one IEEE fp32
+operation per step, exact integer sums); this module compiles it with gcc on
+first use and exposes numpy-level wrappers.  Every function states the reading
+of the method it follows; see the C file's header for the list (R1..R6).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "bitlinear_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+# The activation clamp of reading R4 and the eps of the configurations.
+ACT_CLAMP_EPS = np.float32(1e-5)
+WEIGHT_EPS = np.float32(1e-5)
+
+_CFLAGS = ["-O2", "-std=gnu11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math", "-fno-builtin-rintf"]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle shared library (idempotent).  Returns its path."""
+    with _lock:
+        stale = (not os.path.exists(_LIB_PATH)) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)
+        if force or stale:
+            os.makedirs(_BUILD_DIR, exist_ok=True)
+            tmp = _LIB_PATH + f".tmp{os.getpid()}"
+            subprocess.run(["gcc", *_CFLAGS, _SRC, "-o", tmp, "-lm"], check=True)
+            os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        u64, i64 = ctypes.c_uint64, ctypes.c_int64
+        lib.oracle_absmean.argtypes = [P, u64]
+        lib.oracle_absmean.restype = ctypes.c_float
+        lib.oracle_ternarize.argtypes = [P, u64, ctypes.c_float, ctypes.c_float, P]
+        lib.oracle_pack.argtypes = [P, u64, P]
+        lib.oracle_unpack.argtypes = [P, u64, P]
+        lib.oracle_unpack.restype = u64
+        lib.oracle_bf16_to_f32.argtypes = [P, u64, P]
+        lib.oracle_quant_act.argtypes = [P, i64, i64, ctypes.c_float, P, P]
+        lib.oracle_matmul_int.argtypes = [P, P, i64, i64, i64, P]
+        lib.oracle_dequant.argtypes = [P, ctypes.c_float, P, i64, i64, P]
+        lib.oracle_forward.argtypes = [P, ctypes.c_float, P, P, i64, i64, i64, P, P]
+        lib.oracle_forward.restype = i64
+        _lib = lib
+    return _lib
+
+
+def _c(a: np.ndarray, dtype) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _p(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def absmean(W: np.ndarray) -> np.float32:
+    """gamma = mean|W| (reading R1: exact mean, one RNE rounding to fp32)."""
+    W = _c(W, np.float32).reshape(-1)
+    if W.size == 0 or W.size > 2**32:
+        raise ValueError("absmean needs 1..2^32 values")
+    return np.float32(_load().oracle_absmean(_p(W), W.size))
+
+
+def ternarize(W: np.ndarray, gamma, eps=WEIGHT_EPS) -> np.ndarray:
+    """W_q = clip(rint(W / fp32(gamma + eps)), -1, 1) (reading R2)."""
+    W = _c(W, np.float32)
+    q = np.empty(W.shape, dtype=np.int8)
+    _load().oracle_ternarize(_p(W), W.size, float(np.float32(gamma)), float(np.float32(eps)), _p(q))
+    return q
+
+
+def pack(q: np.ndarray) -> np.ndarray:
+    """Four ternary codes per byte, least significant first (reading R3).
+    q is [N, K] with K % 4 == 0; returns uint8 [N, K/4]."""
+    q = _c(q, np.int8)
+    if q.shape[-1] % 4:
+        raise ValueError("K must be a multiple of 4")
+    out = np.empty(q.shape[:-1] + (q.shape[-1] // 4,), dtype=np.uint8)
+    _load().oracle_pack(_p(q), q.size, _p(out))
+    return out
+
+
+def unpack(packed: np.ndarray, K: int) -> tuple[np.ndarray, int]:
+    """Inverse of :func:`pack`; also returns the count of (invalid) code-3 fields."""
+    packed = _c(packed, np.uint8)
+    n = packed.size * 4
+    q = np.empty(packed.shape[:-1] + (K,), dtype=np.int8)
+    if q.size != n:
+        raise ValueError("packed size does not match K")
+    bad = _load().oracle_unpack(_p(packed), n, _p(q))
+    return q, int(bad)
+
+
+def pack_weights(W: np.ndarray, eps=WEIGHT_EPS) -> tuple[np.ndarray, np.float32]:
+    """The whole weight path: gamma, ternarise, pack.  Returns (W_packed, gamma)."""
+    g = absmean(W)
+    return pack(ternarize(W, g, eps)), g
+
+
+def bf16_bits_to_f32(x_bits: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 (given as its uint16 bit patterns) to fp32."""
+    x_bits = _c(x_bits, np.uint16)
+    out = np.empty(x_bits.shape, dtype=np.float32)
+    _load().oracle_bf16_to_f32(_p(x_bits), x_bits.size, _p(out))
+    return out
+
+
+def quant_act(X: np.ndarray, clamp_eps=ACT_CLAMP_EPS) -> tuple[np.ndarray, np.ndarray]:
+    """Per-token absmax int8 quantisation (readings R4, R5).  X is fp32 [M, K]."""
+    X = _c(X, np.float32)
+    M, K = X.shape
+    xq = np.empty((M, K), dtype=np.int8)
+    s = np.empty((M,), dtype=np.float32)
+    _load().oracle_quant_act(_p(X), M, K, float(np.float32(clamp_eps)), _p(xq), _p(s))
+    return xq, s
+
+
+def matmul_int(q: np.ndarray, x_q: np.ndarray) -> np.ndarray:
+    """acc[m, n] = sum_k q[n, k] * x_q[m, k] in exact integer arithmetic."""
+    q = _c(q, np.int8)
+    x_q = _c(x_q, np.int8)
+    N, K = q.shape
+    M, K2 = x_q.shape
+    if K != K2:
+        raise ValueError("K mismatch")
+    acc = np.empty((M, N), dtype=np.int32)
+    _load().oracle_matmul_int(_p(q), _p(x_q), M, N, K, _p(acc))
+    return acc
+
+
+def dequant(acc: np.ndarray, gamma, s: np.ndarray) -> np.ndarray:
+    """y = fp32(fp32(acc) * fp32(gamma / s[m])) (reading R6)."""
+    acc = _c(acc, np.int32)
+    s = _c(s, np.float32)
+    M, N = acc.shape
+    y = np.empty((M, N), dtype=np.float32)
+    _load().oracle_dequant(_p(acc), float(np.float32(gamma)), _p(s), M, N, _p(y))
+    return y
+
+
+def forward(W_packed: np.ndarray, gamma, x_q: np.ndarray, s: np.ndarray, K: int) -> tuple[np.ndarray, np.ndarray]:
+    """Forward pass from packed weights.  Returns (y fp32 [M,N], acc int32 [M,N])."""
+    W_packed = _c(W_packed, np.uint8)
+    x_q = _c(x_q, np.int8)
+    s = _c(s, np.float32)
+    N = W_packed.size * 4 // K
+    M = x_q.shape[0]
+    if W_packed.size * 4 != N * K or x_q.shape[1] != K or s.shape[0] != M:
+        raise ValueError("shape mismatch")
+    y = np.empty((M, N), dtype=np.float32)
+    acc = np.empty((M, N), dtype=np.int32)
+    rc = _load().oracle_forward(_p(W_packed), float(np.float32(gamma)), _p(x_q), _p(s), M, N, K, _p(y), _p(acc))
+    if rc < 0:
+        raise MemoryError("oracle_forward allocation failed")
+    if rc > 0:
+        raise ValueError(f"packed weights hold {rc} invalid code-3 fields")
+    return y, acc
