@@ -1,0 +1,161 @@
+/*
+ * bitlinear.h -- C ABI of libbitlinear.so, the BitNet b1.58 BitLinear forward
+ * pass on NVIDIA B300 (sm_103a).
+ *
+ * The operation (BitLinear in place of a dense linear layer: weights
+ * constrained to {-1, 0, +1} by an absmean quantiser, activations at 8 bits;
+ * anthology note-168 on arXiv 2402.17764, section "What it does"; the
+ * yousumm.com transcript of the BitNet b1.58 2B4T video, paragraph on the
+ * "ABS mean quantizer" and the "eight-bit numbers"):
+ *
+ *   gamma  = mean(|W|)                                 one fp32 per matrix
+ *   W_q    = clip(round(W / (gamma + eps)), -1, +1)
+ *   s[m]   = 127 / max_k |X[m,k]|                      one fp32 per token
+ *   x_q    = clip(round(X * s[m]), -128, 127)          int8
+ *   acc    = W_q . x_q   (int32; the product only adds and subtracts
+ *            activations: anthology note-168, "The part that is a bet rather
+ *            than a measurement")
+ *   y[m,n] = acc[m,n] * gamma / s[m]                   fp32
+ *
+ * Numerical contract (every result below is reproduced bit for bit by the
+ * library; the test-suite checks it against an independent CPU oracle):
+ *   - gamma is the exact real mean of |W| rounded once to fp32 (ties to
+ *     even), independent of summation order;
+ *   - round() is round-half-to-even; gamma + eps, W / (gamma + eps),
+ *     127 / max|x| and X * s are single IEEE fp32 operations;
+ *   - max|X[m,:]| is clamped from below at BITLINEAR_ACT_CLAMP_EPS, so an
+ *     all-zero token gives x_q = 0 and y = 0;
+ *   - y[m,n] = fp32( fp32(acc[m,n]) * fp32(gamma / s[m]) ).
+ *
+ * Packed weight layout ("bundles four chips into a single byte", yousumm.com
+ * transcript, paragraph on running the model on graphics cards): row-major
+ * [N, K/4] bytes; weight (n, k) is the 2-bit code W_q + 1 in {0, 1, 2} at
+ * bits 2*(k % 4) of byte n*K/4 + k/4.  Code 3 is never written.
+ *
+ * Conventions for every entry point:
+ *   - every array pointer is a DEVICE pointer owned by the caller (e.g. a
+ *     torch tensor); the library allocates no device memory in these calls
+ *     and keeps no per-call state;
+ *   - every call is asynchronous on `stream` (0 = legacy default stream);
+ *     arguments are validated on the host before anything is launched, and
+ *     on a validation error nothing is launched and no output is touched;
+ *   - arrays are dense and row-major; the required alignments are stated per
+ *     call (BL_ERR_MISALIGNED otherwise);
+ *   - kernels that wait on an on-chip barrier give up after a bounded number
+ *     of polls instead of hanging; they then record an error word that
+ *     bitlinear_check_device_error() reports as BL_ERR_TIMEOUT.
+ */
+#ifndef BITLINEAR_H
+#define BITLINEAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  BL_OK = 0,
+  BL_ERR_INVALID_ARG = 1,       /* null pointer, size <= 0, bad eps or dtype */
+  BL_ERR_UNSUPPORTED_SHAPE = 2, /* a size outside the limits stated per call */
+  BL_ERR_MISALIGNED = 3,        /* a pointer without the stated alignment */
+  BL_ERR_WORKSPACE = 4,         /* workspace smaller than required */
+  BL_ERR_CUDA = 5,              /* a CUDA runtime call or launch failed */
+  BL_ERR_TIMEOUT = 6            /* a kernel's bounded wait expired (see above) */
+} bl_status;
+
+typedef enum { BL_F32 = 0, BL_BF16 = 1 } bl_dtype;
+
+/* Lower clamp of max|X[m,:]| before s = 127 / max|X[m,:]|. */
+#define BITLINEAR_ACT_CLAMP_EPS 1e-5f
+
+/* Largest K accepted by bitlinear_forward: 127 * K stays below 2^24, so every
+ * partial sum of the product is an integer that fp32 holds exactly. */
+#define BITLINEAR_MAX_K 131072
+
+/*
+ * bitlinear_pack_workspace_bytes -- bytes of device workspace that
+ * bitlinear_pack_weights needs for an [N, K] matrix (a small constant).
+ */
+size_t bitlinear_pack_workspace_bytes(int64_t N, int64_t K);
+
+/*
+ * bitlinear_pack_weights -- absmean ternarisation and 2-bit packing of one
+ * latent weight matrix (anthology note-168, "What it does": weights
+ * constrained to {-1, 0, +1} by an absmean quantisation; yousumm.com
+ * transcript: four weights per byte).
+ *
+ *   W          in   fp32 [N, K] row-major, 16-byte aligned, finite values
+ *   N, K       in   N >= 1, K >= 4, K % 4 == 0, N*K <= 2^32
+ *   eps        in   finite, > 0 (the eps of gamma + eps; 1e-5 is usual)
+ *   W_packed   out  uint8 [N, K/4], 16-byte aligned (layout above)
+ *   gamma      out  one fp32 (device), 4-byte aligned: mean |W|
+ *   workspace  tmp  >= bitlinear_pack_workspace_bytes(N, K) bytes, 16-byte
+ *                   aligned; clobbered; may be reused once the call's work on
+ *                   `stream` is done
+ *
+ * If W holds an inf or NaN, gamma is NaN and W_packed is unspecified.
+ * Launches four kernels on `stream`; touches W twice (read 4*N*K bytes each
+ * time) and writes N*K/4 bytes.
+ */
+bl_status bitlinear_pack_weights(const float* W, int64_t N, int64_t K, float eps, uint8_t* W_packed, float* gamma,
+                                 void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * bitlinear_quant_act -- per-token absmax quantisation of activations to int8
+ * (anthology note-168, "What it does": activations at 8 bits; yousumm.com
+ * transcript: messages squeezed into "eight-bit numbers").
+ *
+ *   X      in   [M, K] row-major, dtype BL_BF16 or BL_F32, 16-byte aligned
+ *   M, K   in   M >= 1, 1 <= K <= 2^24
+ *   x_q    out  int8 [M, K] row-major, 16-byte aligned
+ *   s      out  fp32 [M]: s[m] = 127 / max(max_k |X[m,k]|, 1e-5), 4-byte aligned
+ *
+ * x_q always lies in [-127, 127].  Non-finite X gives unspecified x_q and s.
+ */
+bl_status bitlinear_quant_act(const void* X, bl_dtype dtype, int64_t M, int64_t K, int8_t* x_q, float* s,
+                              cudaStream_t stream);
+
+/*
+ * bitlinear_forward -- y = (W_q . x_q) * gamma / s: the ternary-times-int8
+ * product accumulated exactly in int32, rescaled per token by gamma/s[m] in
+ * a fused epilogue (anthology note-168, "The part that is a bet rather than a
+ * measurement": the product only involves integer addition; yousumm.com
+ * transcript: packed weights are unpacked next to the math engine and
+ * multiplied with the 8-bit activations).
+ *
+ *   W_packed  in   uint8 [N, K/4] from bitlinear_pack_weights, 16-byte aligned
+ *   gamma     in   one fp32 (device)
+ *   x_q, s    in   int8 [M, K] (16-byte aligned) and fp32 [M] from
+ *                  bitlinear_quant_act
+ *   M, N, K   in   M >= 1, N >= 1, K % 64 == 0, 64 <= K <= BITLINEAR_MAX_K,
+ *                  M, N < 2^31
+ *   y         out  fp32 [M, N], 16-byte aligned
+ *   acc       out  optional (may be NULL): int32 [M, N], 16-byte aligned,
+ *                  the exact integer products before the rescale
+ *
+ * Picks a kernel by M: a streaming GEMV for few tokens and a tensor-core GEMM
+ * for many.  Either way the result is the same bit for bit.
+ */
+bl_status bitlinear_forward(const uint8_t* W_packed, const float* gamma, const int8_t* x_q, const float* s,
+                            int64_t M, int64_t N, int64_t K, float* y, int32_t* acc, cudaStream_t stream);
+
+/*
+ * bitlinear_check_device_error -- waits for `stream`, then reports and clears
+ * the library's device error word: BL_ERR_TIMEOUT if a kernel gave up on a
+ * bounded wait since the last check, BL_ERR_CUDA if the stream itself failed,
+ * BL_OK otherwise.
+ */
+bl_status bitlinear_check_device_error(cudaStream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* bitlinear_status_string(bl_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BITLINEAR_H */

@@ -1,0 +1,174 @@
+"""BitNet b1.58 BitLinear forward on B300 (sm_103a): Python binding.
+
+A thin ctypes layer over ``libbitlinear.so`` (C ABI in ``include/bitlinear.h``).
+Every step of the computation runs in the library's CUDA kernels; this module
+only checks tensor metadata, allocates outputs with torch and passes raw
+device pointers and the current torch stream.  If the library is not built
+(see ``ternary_weight_06_b300.build``) importing this module raises: there is
+no fallback.
+
+Functions carry the C names:
+
+* :func:`bitlinear_pack_weights` -- latent fp32 W [N, K] -> (packed uint8 [N, K/4], gamma fp32 [1])
+* :func:`bitlinear_quant_act`    -- X bf16/fp32 [M, K]   -> (x_q int8 [M, K], s fp32 [M])
+* :func:`bitlinear_forward`      -- packed W, gamma, x_q, s -> y fp32 [M, N] (and int32 acc)
+* :func:`bitlinear_check_device_error`, :func:`bitlinear_status_string`
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "BitLinearError",
+    "LIB_PATH",
+    "lib",
+    "bitlinear_pack_weights",
+    "bitlinear_pack_workspace_bytes",
+    "bitlinear_quant_act",
+    "bitlinear_forward",
+    "bitlinear_check_device_error",
+    "bitlinear_status_string",
+    "EXPORTED_SYMBOLS",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libbitlinear.so")
+
+BL_OK, BL_ERR_INVALID_ARG, BL_ERR_UNSUPPORTED_SHAPE, BL_ERR_MISALIGNED, BL_ERR_WORKSPACE, BL_ERR_CUDA, \
+    BL_ERR_TIMEOUT = range(7)
+BL_F32, BL_BF16 = 0, 1
+
+EXPORTED_SYMBOLS = (
+    "bitlinear_pack_workspace_bytes",
+    "bitlinear_pack_weights",
+    "bitlinear_quant_act",
+    "bitlinear_forward",
+    "bitlinear_check_device_error",
+    "bitlinear_status_string",
+)
+
+
+class BitLinearError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {bitlinear_status_string(status)} (status {status})")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python -m ternary_weight_06_b300.build` "
+                          "(the BitLinear kernels have no non-CUDA fallback)")
+    L = ctypes.CDLL(LIB_PATH)
+    P, i64, sz, f32, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float, ctypes.c_int
+    L.bitlinear_pack_workspace_bytes.argtypes = [i64, i64]
+    L.bitlinear_pack_workspace_bytes.restype = sz
+    L.bitlinear_pack_weights.argtypes = [P, i64, i64, f32, P, P, P, sz, P]
+    L.bitlinear_pack_weights.restype = i32
+    L.bitlinear_quant_act.argtypes = [P, i32, i64, i64, P, P, P]
+    L.bitlinear_quant_act.restype = i32
+    L.bitlinear_forward.argtypes = [P, P, P, P, i64, i64, i64, P, P, P]
+    L.bitlinear_forward.restype = i32
+    L.bitlinear_check_device_error.argtypes = [P]
+    L.bitlinear_check_device_error.restype = i32
+    L.bitlinear_status_string.argtypes = [i32]
+    L.bitlinear_status_string.restype = ctypes.c_char_p
+    return L
+
+
+lib = _load()
+
+
+def bitlinear_status_string(status: int) -> str:
+    return lib.bitlinear_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != BL_OK:
+        raise BitLinearError(status, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None) -> int:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def bitlinear_pack_workspace_bytes(N: int, K: int) -> int:
+    return int(lib.bitlinear_pack_workspace_bytes(int(N), int(K)))
+
+
+def bitlinear_pack_weights(W: torch.Tensor, eps: float = 1e-5, W_packed: torch.Tensor | None = None,
+                           gamma: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None):
+    """Absmean-ternarise and pack latent weights W (fp32 [N, K], K % 4 == 0).
+    Returns (W_packed uint8 [N, K/4], gamma fp32 [1]), both on W's device."""
+    N, K = W.shape
+    if W_packed is None:
+        W_packed = torch.empty((N, K // 4), dtype=torch.uint8, device=W.device)
+    if gamma is None:
+        gamma = torch.empty((1,), dtype=torch.float32, device=W.device)
+    ws_bytes = bitlinear_pack_workspace_bytes(N, K)
+    if workspace is None:
+        workspace = torch.empty((ws_bytes,), dtype=torch.uint8, device=W.device)
+    _check(lib.bitlinear_pack_weights(_dev(W, "W", torch.float32), N, K, float(eps),
+                                      _dev(W_packed, "W_packed", torch.uint8), _dev(gamma, "gamma", torch.float32),
+                                      _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+                                      _stream(stream)), "bitlinear_pack_weights")
+    return W_packed, gamma
+
+
+def bitlinear_quant_act(X: torch.Tensor, x_q: torch.Tensor | None = None, s: torch.Tensor | None = None,
+                        stream=None):
+    """Per-token absmax int8 quantisation of X (bf16 or fp32 [M, K]).
+    Returns (x_q int8 [M, K], s fp32 [M])."""
+    M, K = X.shape
+    if X.dtype == torch.bfloat16:
+        dt = BL_BF16
+    elif X.dtype == torch.float32:
+        dt = BL_F32
+    else:
+        raise ValueError(f"X must be bf16 or fp32, got {X.dtype}")
+    if x_q is None:
+        x_q = torch.empty((M, K), dtype=torch.int8, device=X.device)
+    if s is None:
+        s = torch.empty((M,), dtype=torch.float32, device=X.device)
+    _check(lib.bitlinear_quant_act(_dev(X, "X"), dt, M, K, _dev(x_q, "x_q", torch.int8),
+                                   _dev(s, "s", torch.float32), _stream(stream)), "bitlinear_quant_act")
+    return x_q, s
+
+
+def bitlinear_forward(W_packed: torch.Tensor, gamma: torch.Tensor, x_q: torch.Tensor, s: torch.Tensor,
+                      y: torch.Tensor | None = None, acc: torch.Tensor | bool | None = None, stream=None):
+    """y = (W_q . x_q) * gamma / s.  W_packed uint8 [N, K/4], x_q int8 [M, K].
+    Returns y (fp32 [M, N]); with ``acc=True`` (or an int32 [M, N] tensor)
+    returns (y, acc) where acc holds the exact int32 products."""
+    N, K4 = W_packed.shape
+    M, K = x_q.shape
+    if K4 * 4 != K:
+        raise ValueError(f"W_packed has K/4 = {K4} but x_q has K = {K}")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x_q.device)
+    want_acc = acc is not None and acc is not False
+    if acc is True:
+        acc = torch.empty((M, N), dtype=torch.int32, device=x_q.device)
+    acc_ptr = _dev(acc, "acc", torch.int32) if want_acc else None
+    _check(lib.bitlinear_forward(_dev(W_packed, "W_packed", torch.uint8), _dev(gamma, "gamma", torch.float32),
+                                 _dev(x_q, "x_q", torch.int8), _dev(s, "s", torch.float32), M, N, K,
+                                 _dev(y, "y", torch.float32), acc_ptr, _stream(stream)), "bitlinear_forward")
+    return (y, acc) if want_acc else y
+
+
+def bitlinear_check_device_error(stream=None) -> None:
+    """Raise BitLinearError if a kernel gave up on a bounded wait (or the stream failed)."""
+    _check(lib.bitlinear_check_device_error(_stream(stream)), "bitlinear_check_device_error")

@@ -1,0 +1,134 @@
+// bitlinear_api.cu -- the extern "C" entry points of libbitlinear.so: argument
+// validation on the host, kernel selection, and the device error word.
+// Contracts are documented in include/bitlinear.h.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "bitlinear.h"
+#include "internal.h"
+
+// The library's only state: one error word per device, set by kernels whose
+// bounded waits expire (see bitlinear_check_device_error).
+static __device__ uint32_t g_bl_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kGemvMaxTokens = 4;
+
+struct DeviceInfo {
+  bool ready = false;
+  int num_sms = 0;
+  uint32_t* err = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+// Per-device facts, filled on first use with that device current.
+bl_status device_info(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BL_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return BL_ERR_CUDA;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_bl_error_word) != cudaSuccess) return BL_ERR_CUDA;
+    d.err = static_cast<uint32_t*>(p);
+    d.ready = true;
+  }
+  *out = d;
+  return BL_OK;
+}
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline bl_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BL_OK : BL_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+size_t bitlinear_pack_workspace_bytes(int64_t N, int64_t K) {
+  (void)N;
+  (void)K;
+  return bl::kPackWorkspaceBytes;
+}
+
+bl_status bitlinear_pack_weights(const float* W, int64_t N, int64_t K, float eps, uint8_t* W_packed, float* gamma,
+                                 void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!W || !W_packed || !gamma || !workspace) return BL_ERR_INVALID_ARG;
+  if (N < 1 || K < 1) return BL_ERR_INVALID_ARG;
+  if (!std::isfinite(eps) || !(eps > 0.0f)) return BL_ERR_INVALID_ARG;
+  if (K % 4 != 0 || K < 4) return BL_ERR_UNSUPPORTED_SHAPE;
+  if (N > (int64_t)(1ull << 32) / K) return BL_ERR_UNSUPPORTED_SHAPE;  // N*K <= 2^32
+  if (!aligned(W, 16) || !aligned(W_packed, 16) || !aligned(gamma, 4) || !aligned(workspace, 16))
+    return BL_ERR_MISALIGNED;
+  if (workspace_bytes < bl::kPackWorkspaceBytes) return BL_ERR_WORKSPACE;
+  DeviceInfo d;
+  if (bl_status st = device_info(&d)) return st;
+  return from_cuda(bl::launch_pack(W, (uint64_t)N * (uint64_t)K, eps, W_packed, gamma,
+                                   static_cast<bl::PackWorkspace*>(workspace), d.num_sms, stream));
+}
+
+bl_status bitlinear_quant_act(const void* X, bl_dtype dtype, int64_t M, int64_t K, int8_t* x_q, float* s,
+                              cudaStream_t stream) {
+  if (!X || !x_q || !s) return BL_ERR_INVALID_ARG;
+  if (M < 1 || K < 1) return BL_ERR_INVALID_ARG;
+  if (dtype != BL_F32 && dtype != BL_BF16) return BL_ERR_INVALID_ARG;
+  if (M > INT32_MAX || K > (int64_t)1 << 24) return BL_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(X, 16) || !aligned(x_q, 16) || !aligned(s, 4)) return BL_ERR_MISALIGNED;
+  return from_cuda(bl::launch_quant_act(X, dtype == BL_BF16, M, K, x_q, s, stream));
+}
+
+bl_status bitlinear_forward(const uint8_t* W_packed, const float* gamma, const int8_t* x_q, const float* s,
+                            int64_t M, int64_t N, int64_t K, float* y, int32_t* acc, cudaStream_t stream) {
+  if (!W_packed || !gamma || !x_q || !s || !y) return BL_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1) return BL_ERR_INVALID_ARG;
+  if (K % 64 != 0 || K > BITLINEAR_MAX_K || M > INT32_MAX || N > INT32_MAX) return BL_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(W_packed, 16) || !aligned(x_q, 16) || !aligned(y, 16) || !aligned(gamma, 4) || !aligned(s, 4) ||
+      (acc && !aligned(acc, 16)))
+    return BL_ERR_MISALIGNED;
+  DeviceInfo d;
+  if (bl_status st = device_info(&d)) return st;
+  bl::ForwardArgs a{W_packed, gamma, x_q, s, M, N, K, y, acc, d.err};
+  if (M > kGemvMaxTokens) {
+    const cudaError_t e = bl::launch_gemm_tc(a, d.num_sms, stream);
+    if (e != cudaErrorNotSupported) return from_cuda(e);
+  }
+  return from_cuda(bl::launch_gemv(a, d.num_sms, stream));
+}
+
+bl_status bitlinear_check_device_error(cudaStream_t stream) {
+  DeviceInfo d;
+  if (bl_status st = device_info(&d)) return st;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return BL_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpyFromSymbolAsync(&word, g_bl_error_word, sizeof(word), 0, cudaMemcpyDeviceToHost, stream) !=
+      cudaSuccess)
+    return BL_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return BL_ERR_CUDA;
+  if (word) {
+    if (cudaMemsetAsync(d.err, 0, sizeof(uint32_t), stream) != cudaSuccess) return BL_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return BL_ERR_CUDA;
+    return BL_ERR_TIMEOUT;
+  }
+  return BL_OK;
+}
+
+const char* bitlinear_status_string(bl_status status) {
+  switch (status) {
+    case BL_OK: return "BL_OK";
+    case BL_ERR_INVALID_ARG: return "BL_ERR_INVALID_ARG: null pointer, non-positive size, bad eps or dtype";
+    case BL_ERR_UNSUPPORTED_SHAPE: return "BL_ERR_UNSUPPORTED_SHAPE: a size outside the documented limits";
+    case BL_ERR_MISALIGNED: return "BL_ERR_MISALIGNED: a pointer lacks the documented alignment";
+    case BL_ERR_WORKSPACE: return "BL_ERR_WORKSPACE: workspace smaller than bitlinear_pack_workspace_bytes()";
+    case BL_ERR_CUDA: return "BL_ERR_CUDA: a CUDA runtime call or kernel launch failed";
+    case BL_ERR_TIMEOUT: return "BL_ERR_TIMEOUT: a kernel gave up on a bounded wait";
+  }
+  return "unknown bl_status";
+}
+
+}  // extern "C"

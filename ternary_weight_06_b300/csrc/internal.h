@@ -1,0 +1,45 @@
+// internal.h -- host-side declarations shared between the C-ABI layer and the
+// kernel translation units of libbitlinear.so.  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace bl {
+
+// Device workspace of bitlinear_pack_weights.
+struct PackWorkspace {
+  unsigned long long bucket[32];  // exact per-exponent-group sums of |w| (see pack.cu)
+  uint32_t nonfinite;             // set if any weight is inf or NaN
+  uint32_t thresh_bits;           // fp32 bits of the zero-band threshold T
+  float gamma;                    // copy of gamma for later kernels
+  uint32_t pad;
+};
+static_assert(sizeof(PackWorkspace) == 272, "workspace layout");
+constexpr size_t kPackWorkspaceBytes = 512;
+
+cudaError_t launch_pack(const float* W, uint64_t n, float eps, uint8_t* Wp, float* gamma, PackWorkspace* ws,
+                        int num_sms, cudaStream_t stream);
+
+cudaError_t launch_quant_act(const void* X, bool bf16, int64_t M, int64_t K, int8_t* xq, float* s,
+                             cudaStream_t stream);
+
+struct ForwardArgs {
+  const uint8_t* Wp;
+  const float* gamma;
+  const int8_t* xq;
+  const float* s;
+  int64_t M, N, K;
+  float* y;
+  int32_t* acc;
+  uint32_t* err;  // device error word
+};
+
+// Streaming GEMV for a few tokens (any M: tokens are taken in groups of <= 4).
+cudaError_t launch_gemv(const ForwardArgs& a, int num_sms, cudaStream_t stream);
+
+// Tensor-core GEMM (tcgen05) for many tokens.  Returns cudaErrorNotSupported
+// when the shape is outside what the kernel handles.
+cudaError_t launch_gemm_tc(const ForwardArgs& a, int num_sms, cudaStream_t stream);
+
+}  // namespace bl

@@ -1,0 +1,121 @@
+// quant.cu -- per-token absmax int8 quantisation of activations ("activations
+// at 8 bits": anthology note-168 on arXiv 2402.17764, "What it does").
+//
+//   a    = max(max_k |x[m,k]|, 1e-5)         (clamp: an all-zero token stays finite)
+//   s[m] = fp32(127 / a)                     (one IEEE division)
+//   x_q  = clip(rint(fp32(x * s[m])), -128, 127)   (rint = round half to even)
+//
+// One CTA per token row.  Pass 1 reduces max|x| over the row with 128-bit
+// loads (as fp32 bit patterns: for non-negative floats the unsigned order is
+// the numeric order, so the reduction is exact and order-free); pass 2 reads
+// the row again (from L1/L2) and writes x_q.
+#include <cstdint>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace bl {
+namespace {
+
+constexpr float kActClampEps = 1e-5f;
+
+__device__ __forceinline__ uint32_t abs_bits_bf16x2(uint32_t w) {
+  return max((w << 16) & 0x7fff0000u, w & 0x7fff0000u);
+}
+
+__device__ __forceinline__ uint32_t q8(float x, float s) {
+  int q = __float2int_rn(__fmul_rn(x, s));
+  q = min(max(q, -128), 127);
+  return (uint32_t)q & 0xffu;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+template <bool BF16>
+__global__ void __launch_bounds__(1024) quant_act_kernel(const void* __restrict__ X, int64_t K, bool vec,
+                                                         int8_t* __restrict__ xq, float* __restrict__ s) {
+  constexpr int kEsize = BF16 ? 2 : 4;
+  const int64_t m = blockIdx.x;
+  const char* row = static_cast<const char*>(X) + m * K * kEsize;
+  int8_t* out = xq + m * K;
+  const int tid = threadIdx.x, nt = blockDim.x;
+
+  uint32_t amax = 0;
+  if (vec) {
+    const uint4* r4 = reinterpret_cast<const uint4*>(row);
+    const int64_t nch = K * kEsize / 16;
+    for (int64_t c = tid; c < nch; c += nt) {
+      const uint4 v = __ldg(r4 + c);
+      if (BF16) {
+        amax = max(amax, max(max(abs_bits_bf16x2(v.x), abs_bits_bf16x2(v.y)),
+                             max(abs_bits_bf16x2(v.z), abs_bits_bf16x2(v.w))));
+      } else {
+        amax = max(amax, max(max(v.x & 0x7fffffffu, v.y & 0x7fffffffu), max(v.z & 0x7fffffffu, v.w & 0x7fffffffu)));
+      }
+    }
+  } else {
+    for (int64_t k = tid; k < K; k += nt) {
+      uint32_t b = BF16 ? ((uint32_t)reinterpret_cast<const uint16_t*>(row)[k] << 16)
+                        : reinterpret_cast<const uint32_t*>(row)[k];
+      amax = max(amax, b & 0x7fffffffu);
+    }
+  }
+  __shared__ uint32_t red[32];
+  amax = __reduce_max_sync(0xffffffffu, amax);
+  if ((tid & 31) == 0) red[tid >> 5] = amax;
+  __syncthreads();
+  if (tid < 32) {
+    uint32_t v = tid < (nt >> 5) ? red[tid] : 0u;
+    v = __reduce_max_sync(0xffffffffu, v);
+    if (tid == 0) red[0] = v;
+  }
+  __syncthreads();
+  float a = __uint_as_float(red[0]);
+  if (a < kActClampEps) a = kActClampEps;
+  const float sm = __fdiv_rn(127.0f, a);
+  if (tid == 0) s[m] = sm;
+
+  if (vec) {
+    const uint4* r4 = reinterpret_cast<const uint4*>(row);
+    const int64_t nch = K * kEsize / 16;
+    for (int64_t c = tid; c < nch; c += nt) {
+      const uint4 v = __ldg(r4 + c);
+      if (BF16) {
+        uint2 o;
+        o.x = q8(bf16_lo(v.x), sm) | (q8(bf16_hi(v.x), sm) << 8) | (q8(bf16_lo(v.y), sm) << 16) |
+              (q8(bf16_hi(v.y), sm) << 24);
+        o.y = q8(bf16_lo(v.z), sm) | (q8(bf16_hi(v.z), sm) << 8) | (q8(bf16_lo(v.w), sm) << 16) |
+              (q8(bf16_hi(v.w), sm) << 24);
+        reinterpret_cast<uint2*>(out)[c] = o;
+      } else {
+        const uint32_t o = q8(__uint_as_float(v.x), sm) | (q8(__uint_as_float(v.y), sm) << 8) |
+                           (q8(__uint_as_float(v.z), sm) << 16) | (q8(__uint_as_float(v.w), sm) << 24);
+        reinterpret_cast<uint32_t*>(out)[c] = o;
+      }
+    }
+  } else {
+    for (int64_t k = tid; k < K; k += nt) {
+      const float x = BF16 ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(row)[k] << 16)
+                           : reinterpret_cast<const float*>(row)[k];
+      out[k] = (int8_t)q8(x, sm);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quant_act(const void* X, bool bf16, int64_t M, int64_t K, int8_t* xq, float* s,
+                             cudaStream_t stream) {
+  const int esize = bf16 ? 2 : 4;
+  const bool vec = (K * esize) % 16 == 0;
+  const int64_t work = vec ? K * esize / 16 : K;
+  int threads = (int)((work + 31) / 32 * 32);
+  if (threads > 1024) threads = 1024;
+  if (threads < 32) threads = 32;
+  if (bf16) quant_act_kernel<true><<<(unsigned)M, threads, 0, stream>>>(X, K, vec, xq, s);
+  else quant_act_kernel<false><<<(unsigned)M, threads, 0, stream>>>(X, K, vec, xq, s);
+  return cudaGetLastError();
+}
+
+}  // namespace bl

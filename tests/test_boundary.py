@@ -1,0 +1,135 @@
+"""The C-ABI boundary on the CPU: the library builds, loads, exports every
+entry point include/bitlinear.h declares, and rejects bad arguments on the
+host before anything is launched.  No call here reaches a CUDA API: every
+case fails validation first (the pointers are fake and never dereferenced)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bitlinear.h")
+
+
+@pytest.fixture(scope="module")
+def bl():
+    from ternary_weight_06_b300 import build
+
+    build.build()
+    import ternary_weight_06_b300 as mod
+
+    return mod
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(bitlinear_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("bitlinear_pack_weights", "bitlinear_quant_act", "bitlinear_forward",
+                     "bitlinear_check_device_error", "bitlinear_status_string", "bitlinear_pack_workspace_bytes"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(bl):
+    lib = ctypes.CDLL(bl.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in bitlinear.h but not exported"
+    assert set(bl.EXPORTED_SYMBOLS) <= set(declared_functions())
+
+
+def test_status_strings(bl):
+    for code in range(7):
+        s = bl.bitlinear_status_string(code)
+        assert s.startswith("BL_")
+    assert "unknown" in bl.bitlinear_status_string(99)
+
+
+def test_workspace_size_is_small_constant(bl):
+    assert 272 <= bl.bitlinear_pack_workspace_bytes(8192, 28672) <= 4096
+    assert bl.bitlinear_pack_workspace_bytes(1, 4) == bl.bitlinear_pack_workspace_bytes(8192, 28672)
+
+
+GOOD = 0x10000  # a fake, 64 KiB-aligned address: never dereferenced by these cases
+
+
+def pack(bl, W=GOOD, N=8, K=64, eps=1e-5, Wp=GOOD, g=GOOD, ws=GOOD, ws_bytes=4096):
+    return bl.lib.bitlinear_pack_weights(W, N, K, eps, Wp, g, ws, ws_bytes, None)
+
+
+def test_pack_validation(bl):
+    assert pack(bl, W=None) == bl.BL_ERR_INVALID_ARG
+    assert pack(bl, Wp=None) == bl.BL_ERR_INVALID_ARG
+    assert pack(bl, g=None) == bl.BL_ERR_INVALID_ARG
+    assert pack(bl, ws=None) == bl.BL_ERR_INVALID_ARG
+    assert pack(bl, N=0) == bl.BL_ERR_INVALID_ARG
+    assert pack(bl, K=-4) == bl.BL_ERR_INVALID_ARG
+    assert pack(bl, eps=0.0) == bl.BL_ERR_INVALID_ARG
+    assert pack(bl, eps=float("nan")) == bl.BL_ERR_INVALID_ARG
+    assert pack(bl, eps=float("inf")) == bl.BL_ERR_INVALID_ARG
+    assert pack(bl, K=6) == bl.BL_ERR_UNSUPPORTED_SHAPE
+    assert pack(bl, N=2**20, K=2**13) == bl.BL_ERR_UNSUPPORTED_SHAPE  # N*K = 2^33 > 2^32
+    assert pack(bl, W=GOOD + 4) == bl.BL_ERR_MISALIGNED
+    assert pack(bl, Wp=GOOD + 8) == bl.BL_ERR_MISALIGNED
+    assert pack(bl, g=GOOD + 2) == bl.BL_ERR_MISALIGNED
+    assert pack(bl, ws=GOOD + 8) == bl.BL_ERR_MISALIGNED
+    assert pack(bl, ws_bytes=16) == bl.BL_ERR_WORKSPACE
+
+
+def quant(bl, X=GOOD, dt=1, M=4, K=64, xq=GOOD, s=GOOD):
+    return bl.lib.bitlinear_quant_act(X, dt, M, K, xq, s, None)
+
+
+def test_quant_validation(bl):
+    assert quant(bl, X=None) == bl.BL_ERR_INVALID_ARG
+    assert quant(bl, xq=None) == bl.BL_ERR_INVALID_ARG
+    assert quant(bl, s=None) == bl.BL_ERR_INVALID_ARG
+    assert quant(bl, M=0) == bl.BL_ERR_INVALID_ARG
+    assert quant(bl, K=0) == bl.BL_ERR_INVALID_ARG
+    assert quant(bl, dt=7) == bl.BL_ERR_INVALID_ARG
+    assert quant(bl, M=2**31) == bl.BL_ERR_UNSUPPORTED_SHAPE
+    assert quant(bl, K=2**24 + 1) == bl.BL_ERR_UNSUPPORTED_SHAPE
+    assert quant(bl, X=GOOD + 2) == bl.BL_ERR_MISALIGNED
+    assert quant(bl, xq=GOOD + 1) == bl.BL_ERR_MISALIGNED
+    assert quant(bl, s=GOOD + 2) == bl.BL_ERR_MISALIGNED
+
+
+def fwd(bl, Wp=GOOD, g=GOOD, xq=GOOD, s=GOOD, M=1, N=16, K=64, y=GOOD, acc=None):
+    return bl.lib.bitlinear_forward(Wp, g, xq, s, M, N, K, y, acc, None)
+
+
+def test_forward_validation(bl):
+    assert fwd(bl, Wp=None) == bl.BL_ERR_INVALID_ARG
+    assert fwd(bl, g=None) == bl.BL_ERR_INVALID_ARG
+    assert fwd(bl, xq=None) == bl.BL_ERR_INVALID_ARG
+    assert fwd(bl, s=None) == bl.BL_ERR_INVALID_ARG
+    assert fwd(bl, y=None) == bl.BL_ERR_INVALID_ARG
+    assert fwd(bl, M=0) == bl.BL_ERR_INVALID_ARG
+    assert fwd(bl, N=-1) == bl.BL_ERR_INVALID_ARG
+    assert fwd(bl, K=0) == bl.BL_ERR_INVALID_ARG
+    assert fwd(bl, K=96) == bl.BL_ERR_UNSUPPORTED_SHAPE  # K % 64 != 0
+    assert fwd(bl, K=32) == bl.BL_ERR_UNSUPPORTED_SHAPE
+    assert fwd(bl, K=131072 + 64) == bl.BL_ERR_UNSUPPORTED_SHAPE
+    assert fwd(bl, M=2**31) == bl.BL_ERR_UNSUPPORTED_SHAPE
+    assert fwd(bl, N=2**31) == bl.BL_ERR_UNSUPPORTED_SHAPE
+    assert fwd(bl, Wp=GOOD + 4) == bl.BL_ERR_MISALIGNED
+    assert fwd(bl, xq=GOOD + 8) == bl.BL_ERR_MISALIGNED
+    assert fwd(bl, y=GOOD + 4) == bl.BL_ERR_MISALIGNED
+    assert fwd(bl, g=GOOD + 1) == bl.BL_ERR_MISALIGNED
+    assert fwd(bl, s=GOOD + 2) == bl.BL_ERR_MISALIGNED
+    assert fwd(bl, acc=GOOD + 4) == bl.BL_ERR_MISALIGNED
+
+
+def test_python_binding_rejects_cpu_tensors(bl):
+    import torch
+
+    with pytest.raises(ValueError):
+        bl.bitlinear_quant_act(torch.zeros((2, 64), dtype=torch.bfloat16))
+    with pytest.raises(ValueError):
+        bl.bitlinear_pack_weights(torch.zeros((2, 64), dtype=torch.float32))

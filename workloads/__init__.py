@@ -101,13 +101,35 @@ def activations(M: int, K: int, dtype: str, seed: int, outlier_frac: float = 0.0
     raise ValueError(dtype)
 
 
+def weight_seed(wl: Workload, index: int) -> int:
+    """Layers of a workload that differ only in M are one weight matrix seen at
+    several batch sizes: the weight seed depends on the (K, N) shape only."""
+    shapes = []
+    for L in wl.layers:
+        if (L.K, L.N) not in shapes:
+            shapes.append((L.K, L.N))
+    L = wl.layers[index]
+    return 1000 * wl.seed + shapes.index((L.K, L.N))
+
+
+def activation_seed(wl: Workload, index: int) -> int:
+    return 1000 * wl.seed + 500 + index
+
+
+def layer_weights(wl: Workload, index: int) -> torch.Tensor:
+    L = wl.layers[index]
+    return latent_weights(L.N, L.K, L.w_sigma, seed=weight_seed(wl, index))
+
+
+def layer_activations(wl: Workload, index: int) -> torch.Tensor:
+    L = wl.layers[index]
+    return activations(L.M, L.K, L.x_dtype, seed=activation_seed(wl, index), outlier_frac=L.outlier_frac,
+                       outlier_scale=L.outlier_scale)
+
+
 def layer_inputs(wl: Workload, index: int) -> tuple[torch.Tensor, torch.Tensor]:
     """(W fp32 [N,K], X [M,K]) for layer ``index`` of workload ``wl``."""
-    L = wl.layers[index]
-    W = latent_weights(L.N, L.K, L.w_sigma, seed=1000 * wl.seed + 2 * index)
-    X = activations(L.M, L.K, L.x_dtype, seed=1000 * wl.seed + 2 * index + 1,
-                    outlier_frac=L.outlier_frac, outlier_scale=L.outlier_scale)
-    return W, X
+    return layer_weights(wl, index), layer_activations(wl, index)
 
 
 def x_as_f32_numpy(X: torch.Tensor) -> np.ndarray:
