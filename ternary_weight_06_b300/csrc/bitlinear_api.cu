@@ -94,10 +94,7 @@ bl_status bitlinear_forward(const uint8_t* W_packed, const float* gamma, const i
   DeviceInfo d;
   if (bl_status st = device_info(&d)) return st;
   bl::ForwardArgs a{W_packed, gamma, x_q, s, M, N, K, y, acc, d.err};
-  if (M > kGemvMaxTokens) {
-    const cudaError_t e = bl::launch_gemm_tc(a, d.num_sms, stream);
-    if (e != cudaErrorNotSupported) return from_cuda(e);
-  }
+  if (M > kGemvMaxTokens) return from_cuda(bl::launch_gemm_tc(a, d.num_sms, stream));
   return from_cuda(bl::launch_gemv(a, d.num_sms, stream));
 }
 

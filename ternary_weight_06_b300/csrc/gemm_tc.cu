@@ -1,13 +1,412 @@
-// gemm_tc.cu -- tensor-core (tcgen05) BitLinear GEMM for many tokens.
+// gemm_tc.cu -- tensor-core BitLinear GEMM for many tokens (tcgen05, sm_103a).
+//
+// "unpacks it right next to the math engine, and multiplies it with those
+// little 8-bit bricks" (yousumm.com BitNet b1.58 2B4T transcript): packed
+// ternary tiles and int8 activation tiles are staged in shared memory by TMA,
+// expanded next to the tensor core into an exact MMA operand format, and
+// multiplied by tcgen05.mma with the accumulator in tensor memory.
+//
+// Exactness.  sm_103a has no integer tcgen05 MMA, so the product runs as
+// kind::f16 with fp32 accumulation.  Every ternary weight and every int8
+// activation is exact in fp16, every product is an integer of magnitude
+// <= 128, and every partial sum is an integer of magnitude <= 128*K < 2^24
+// (K <= 131072), so every intermediate is exactly representable in fp32 and
+// the accumulator equals the int32 sum bit for bit.  The test-suite checks
+// this on adversarial inputs that drive |acc| to 128*K.
+//
+// Tile: 128 output features (MMA M, operand A = W) x BN tokens (MMA N <= 256,
+// operand B = x) x 64 k per stage.  Warp roles:
+//   warp 0      TMA producer: packed W box [128 rows x 16 B] and int8 x box
+//               [BN rows x 64 B] into a ring of raw stages;
+//   warp 1      allocates tensor memory; one thread issues the MMAs;
+//   warps 2..9  convert raw stages into fp16 operands (128-byte swizzled,
+//               K-major), then run the epilogue (tensor memory -> y).
+//
+// Within every group of 16 consecutive k both operands use the order
+// p = 4i + j <-> k = 4j + i.  In that order the packed word P of 16 codes
+// unpacks with (P >> 2i) & 0x03030303 (codes of k = 4j + i as bytes j), and
+// a sum over k does not depend on the order, so the product is unchanged.
+#include <cuda.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
 #include "internal.h"
 
 namespace bl {
+namespace {
+
+constexpr int kBM = 128;         // features per tile (MMA M)
+constexpr int kBK = 64;          // k per stage
+constexpr int kRawStages = 4;
+constexpr int kOpStages = 2;
+constexpr int kConvWarps = 8;
+constexpr int kThreads = 32 * (2 + kConvWarps);
+constexpr int kWRawBytes = kBM * kBK / 4;     // 2048
+constexpr int kARowBytes = kBK * 2;           // 128: one fp16 row of a stage
+constexpr int kAOpBytes = kBM * kARowBytes;   // 16384
+
+struct GemmCfg {
+  const float* gamma;
+  const float* s;
+  float* y;
+  int32_t* acc;
+  uint32_t* err;
+  int M, N, K, BN;
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row atoms of
+// 1024 bytes stacked contiguously (stride-dimension offset 1024).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3fffu);
+  d |= (uint64_t)(16u >> 4) << 16;    // leading-dimension offset (unused with this swizzle)
+  d |= (uint64_t)(1024u >> 4) << 32;  // stride-dimension offset
+  d |= (uint64_t)1 << 46;             // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;             // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp16 A and B, fp32 D, both K-major.
+__host__ __device__ constexpr uint32_t f16_idesc(int m, int n) {
+  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ bool wait_flag(uint64_t* bar, uint32_t parity, uint32_t* err, volatile uint32_t* abort_flag) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(a, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(err, kErrGemmWait);
+      *abort_flag = 1u;
+      return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- operand expansion
+
+// Two fp16 of 1024 + byte, from bytes b0, b1 of w (selector 0x4140) or b2, b3 (0x4342).
+__device__ __forceinline__ uint32_t bytes_to_h2(uint32_t w, uint32_t sel) { return __byte_perm(w, 0x64646464u, sel); }
+
+__device__ __forceinline__ uint32_t h2_sub(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// 16 codes (one 32-bit packed word) -> 16 fp16 in order p = 4i + j (k = 4j + i), values c - 1.
+__device__ __forceinline__ void unpack_word_f16(uint32_t P, uint32_t* h /* 8 words */) {
+  const uint32_t k1025 = 0x64016401u;  // fp16 (1025, 1025)
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t S = (P >> (2 * i)) & 0x03030303u;
+    h[2 * i] = h2_sub(bytes_to_h2(S, 0x4140), k1025);
+    h[2 * i + 1] = h2_sub(bytes_to_h2(S, 0x4342), k1025);
+  }
+}
+
+// 16 int8 activations (natural order, 4 words) -> 16 fp16 in order p = 4i + j.
+__device__ __forceinline__ void convert_x16_f16(uint4 v, uint32_t* h /* 8 words */) {
+  const uint32_t x0 = v.x ^ 0x80808080u, x1 = v.y ^ 0x80808080u, x2 = v.z ^ 0x80808080u, x3 = v.w ^ 0x80808080u;
+  const uint32_t t0 = __byte_perm(x0, x1, 0x5140), t1 = __byte_perm(x2, x3, 0x5140);
+  const uint32_t t2 = __byte_perm(x0, x1, 0x7362), t3 = __byte_perm(x2, x3, 0x7362);
+  const uint32_t o[4] = {__byte_perm(t0, t1, 0x5410), __byte_perm(t0, t1, 0x7632), __byte_perm(t2, t3, 0x5410),
+                         __byte_perm(t2, t3, 0x7632)};
+  const uint32_t k1152 = 0x64806480u;  // fp16 (1152, 1152): undoes the +128 bias and the 1024 offset
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    h[2 * i] = h2_sub(bytes_to_h2(o[i], 0x4140), k1152);
+    h[2 * i + 1] = h2_sub(bytes_to_h2(o[i], 0x4342), k1152);
+  }
+}
+
+// Store 16-byte unit u (0..7) of row r of a 128-byte-swizzled K-major tile.
+__device__ __forceinline__ void st_sw128(uint8_t* tile, int r, int u, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  uint4* p = reinterpret_cast<uint4*>(tile + r * 128 + ((u ^ (r & 7)) << 4));
+  *p = make_uint4(a, b, c, d);
+}
+
+// ---------------------------------------------------------------- the kernel
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
+                   const GemmCfg c) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int BN = c.BN;
+  const int b_op_bytes = BN * kARowBytes;
+  const int x_raw_bytes = BN * kBK;
+  uint8_t* op_base = smem;                                          // kOpStages x (A 16 KB | B BN*128)
+  uint8_t* raw_base = op_base + kOpStages * (kAOpBytes + b_op_bytes);  // kRawStages x (W 2 KB | x BN*64)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(raw_base + kRawStages * (kWRawBytes + x_raw_bytes));
+  uint64_t* raw_full = bars;
+  uint64_t* raw_empty = raw_full + kRawStages;
+  uint64_t* op_full = raw_empty + kRawStages;
+  uint64_t* op_empty = op_full + kOpStages;
+  uint64_t* acc_full = op_empty + kOpStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+  float* tscale = reinterpret_cast<float*>(tmem_slot + 4);  // [BN]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * kBM;  // first feature of the tile
+  const int m0 = blockIdx.y * BN;   // first token of the tile
+  const int nkb = c.K / kBK;
+  const uint32_t tmem_cols = BN <= 32 ? 32u : BN <= 64 ? 64u : BN <= 128 ? 128u : 256u;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRawStages; ++i) {
+      mbar_init(&raw_full[i], 1);
+      mbar_init(&raw_empty[i], kConvWarps);
+    }
+    for (int i = 0; i < kOpStages; ++i) {
+      mbar_init(&op_full[i], kConvWarps);
+      mbar_init(&op_empty[i], 1);
+    }
+    mbar_init(acc_full, 1);
+    *abort_flag = 0u;
+    fence_mbarrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, tmem_cols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int slot = kb % kRawStages;
+        if (!wait_flag(&raw_empty[slot], ((uint32_t)(kb / kRawStages) & 1u) ^ 1u, c.err, abort_flag)) break;
+        uint8_t* wdst = raw_base + slot * (kWRawBytes + x_raw_bytes);
+        mbar_arrive_expect_tx(&raw_full[slot], (uint32_t)(kWRawBytes + x_raw_bytes));
+        tma_load_2d(wdst, &tmap_w, kb * (kBK / 4), n0, &raw_full[slot]);
+        tma_load_2d(wdst + kWRawBytes, &tmap_x, kb * kBK, m0, &raw_full[slot]);
+        issued = kb + 1;
+      }
+      if (*abort_flag) {
+        for (int kb = (issued > kRawStages ? issued - kRawStages : 0); kb < issued; ++kb) {
+          const uint32_t a = smem_u32(&raw_full[kb % kRawStages]), par = (uint32_t)(kb / kRawStages) & 1u;
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(a, par) && globaltimer_ns() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = f16_idesc(kBM, BN);
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int os = kb % kOpStages;
+        if (!wait_flag(&op_full[os], (uint32_t)(kb / kOpStages) & 1u, c.err, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t a_base = smem_u32(op_base + os * (kAOpBytes + b_op_bytes));
+        const uint32_t b_base = a_base + kAOpBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          mma_f16(tmem, sw128_desc(a_base + kk * 32), sw128_desc(b_base + kk * 32), idesc, (kb | kk) ? 1u : 0u);
+        mma_commit(&op_empty[os]);
+      }
+      mma_commit(acc_full);  // fires once every MMA issued above has completed
+    }
+  } else {
+    // ---------------- converters, then epilogue
+    const int ct = threadIdx.x - 64;  // 0 .. 255
+    pdl_wait();
+    const float gamma = __ldg(c.gamma);
+    for (int j = ct; j < BN; j += 32 * kConvWarps) {
+      const int m = m0 + j;
+      tscale[j] = m < c.M ? __fdiv_rn(gamma, __ldg(c.s + m)) : 0.0f;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kConvWarps) : "memory");  // scales visible to the epilogue warps
+    bool ok = true;
+    for (int kb = 0; kb < nkb && ok; ++kb) {
+      const int slot = kb % kRawStages, os = kb % kOpStages;
+      ok = wait_flag(&op_empty[os], ((uint32_t)(kb / kOpStages) & 1u) ^ 1u, c.err, abort_flag) &&
+           wait_flag(&raw_full[slot], (uint32_t)(kb / kRawStages) & 1u, c.err, abort_flag);
+      if (!ok) break;
+      const uint8_t* wraw = raw_base + slot * (kWRawBytes + x_raw_bytes);
+      const uint8_t* xraw = wraw + kWRawBytes;
+      uint8_t* aop = op_base + os * (kAOpBytes + b_op_bytes);
+      uint8_t* bop = aop + kAOpBytes;
+      // W: thread -> (row r, half h): 8 packed bytes = 32 codes = 4 swizzle units
+      {
+        const int r = ct >> 1, h = ct & 1;
+        const uint2 pw = *reinterpret_cast<const uint2*>(wraw + r * 16 + h * 8);
+        uint32_t f[8];
+        unpack_word_f16(pw.x, f);
+        st_sw128(aop, r, 4 * h + 0, f[0], f[1], f[2], f[3]);
+        st_sw128(aop, r, 4 * h + 1, f[4], f[5], f[6], f[7]);
+        unpack_word_f16(pw.y, f);
+        st_sw128(aop, r, 4 * h + 2, f[0], f[1], f[2], f[3]);
+        st_sw128(aop, r, 4 * h + 3, f[4], f[5], f[6], f[7]);
+      }
+      // x: 16-byte chunk q of token row t -> swizzle units 2q, 2q+1
+      for (int idx = ct; idx < BN * 4; idx += 32 * kConvWarps) {
+        const int t = idx >> 2, q = idx & 3;
+        const uint4 v = *reinterpret_cast<const uint4*>(xraw + t * kBK + q * 16);
+        uint32_t f[8];
+        convert_x16_f16(v, f);
+        st_sw128(bop, t, 2 * q, f[0], f[1], f[2], f[3]);
+        st_sw128(bop, t, 2 * q + 1, f[4], f[5], f[6], f[7]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&raw_empty[slot]);
+        mbar_arrive(&op_full[os]);
+      }
+    }
+    // ---- epilogue: warp w reads tensor-memory lanes 32*(w%4) .. +31 = features
+    if (warp < 6) {  // four warps cover the 128 lanes
+      const bool done = wait_flag(acc_full, 0u, c.err, abort_flag);
+      tc_fence_after();
+      if (done) {
+        const int q = warp & 3;
+        const int f = q * 32 + lane;
+        const int n = n0 + f;
+        for (int j0 = 0; j0 < BN; j0 += 16) {
+          uint32_t r[16];
+          tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)j0, r);
+          if (n < c.N) {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int m = m0 + j0 + jj;
+              if (m < c.M) {
+                const float v = __uint_as_float(r[jj]);
+                const int64_t o = (int64_t)m * c.N + n;
+                c.y[o] = __fmul_rn(v, tscale[j0 + jj]);
+                if (c.acc) c.acc[o] = __float2int_rn(v);
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    // Every MMA issued must have finished before its accumulator is freed; the
+    // issuer always commits acc_full, so this completes (bounded in any case).
+    const uint32_t a = smem_u32(acc_full);
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(a, 0u) && globaltimer_ns() - t0 < kWaitLimitNs) {
+    }
+    tc_fence_after();
+    tmem_dealloc(tmem, tmem_cols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool encode_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                  uint32_t box_outer) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
 
 cudaError_t launch_gemm_tc(const ForwardArgs& a, int num_sms, cudaStream_t stream) {
-  (void)a;
   (void)num_sms;
-  (void)stream;
-  return cudaErrorNotSupported;
+  // token tiles of equal size, rounded up to the MMA's N granularity of 16
+  const int64_t ntiles = (a.M + 255) / 256;
+  int BN = (int)((a.M + ntiles - 1) / ntiles);
+  BN = (BN + 15) / 16 * 16;
+  CUtensorMap tw, tx;
+  if (!encode_u8_2d(&tw, a.Wp, (uint64_t)a.K / 4, (uint64_t)a.N, kBK / 4, kBM)) return cudaErrorInvalidValue;
+  if (!encode_u8_2d(&tx, a.xq, (uint64_t)a.K, (uint64_t)a.M, kBK, (uint32_t)BN)) return cudaErrorInvalidValue;
+  GemmCfg c{a.gamma, a.s, a.y, a.acc, a.err, (int)a.M, (int)a.N, (int)a.K, BN};
+  const size_t smem = 1024 + (size_t)kOpStages * (kAOpBytes + BN * kARowBytes) +
+                      (size_t)kRawStages * (kWRawBytes + BN * kBK) + (2 * kRawStages + 2 * kOpStages + 1) * 8 + 16 +
+                      (size_t)BN * 4;
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)((a.N + kBM - 1) / kBM), (unsigned)ntiles);
+  gemm_tc_kernel<<<grid, kThreads, smem, stream>>>(tw, tx, c);
+  return cudaGetLastError();
 }
 
 }  // namespace bl

@@ -38,8 +38,7 @@ struct ForwardArgs {
 // Streaming GEMV for a few tokens (any M: tokens are taken in groups of <= 4).
 cudaError_t launch_gemv(const ForwardArgs& a, int num_sms, cudaStream_t stream);
 
-// Tensor-core GEMM (tcgen05) for many tokens.  Returns cudaErrorNotSupported
-// when the shape is outside what the kernel handles.
+// Tensor-core GEMM (tcgen05) for more tokens than the GEMV handles well.
 cudaError_t launch_gemm_tc(const ForwardArgs& a, int num_sms, cudaStream_t stream);
 
 }  // namespace bl
