@@ -1,0 +1,542 @@
+#!/usr/bin/env python3
+"""Benchmark of the BitNet b1.58 BitLinear forward on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|...] [--impl ours|reference]
+
+One step is one pass of the per-token hot path over every layer of the
+workload: per-token int8 activation quantisation, then the ternary x int8
+product with the fused gamma/s rescale, through the C ABI of libbitlinear.so.
+Weights are packed once beforehand (the pages' "inference-ready pack"); the
+packing kernels are timed in the same run and reported under "pack".
+
+Timing: W warm-up steps, then exactly K steps replayed from CUDA graphs of the
+public C-ABI calls, bracketed by a barrier and cuda.synchronize() on both
+sides and timed with CUDA events; max over ranks.  L2 (126 MB) is defeated by
+rotating over R copies of the packed weights and activations whose total is
+more than twice L2.  After the timed region the last step is re-run eagerly
+and its outputs must match bit for bit ("verified").  Rank 0 prints one JSON
+line.
+
+Under torchrun (N > 1) every rank runs its own replica of the workload (weak
+scaling; the path has no data-path exchange) and value is the sum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+DEFAULT_STEPS = {"decode": 100000, "tiny": 20000, "skinny": 20000, "prefill": 400, "llama70b": 2000}
+GRAPH_CHUNK = 500  # steps per captured graph
+
+
+# ---------------------------------------------------------------- helpers
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_digest(files):
+    h = hashlib.sha256()
+    for rel in files:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None if absent
+    or if the kernel's source changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        table = json.load(f)
+    for e in table.get("entries", []):
+        if e.get("kernel") == kernel and e.get("workload") == workload:
+            if e.get("source_digest") != kernel_source_digest(e.get("source_files", [])):
+                return None
+            return e.get("dram_bytes_per_launch")
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                        rows.append(parts)
+        except OSError:
+            pass
+        finally:
+            if self.path and os.path.exists(self.path):
+                os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        mx = [float(r[2]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(pw) if pw else None}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group(backend="nccl" if torch.cuda.is_available() else "gloo")
+        return dist, rank, world, local
+    return None, rank, world, local
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, value: float) -> float:
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- accounting
+
+def x_bytes(L) -> int:
+    return 2 if L.x_dtype == "bf16" else 4
+
+
+def layer_bytes(L) -> int:
+    """Algorithmic HBM bytes of one layer step: read X, read the packed
+    weights, write y (the per-token scales and gamma are counted too)."""
+    return L.M * L.K * x_bytes(L) + L.N * L.K // 4 + 4 * L.M * L.N + 4 * L.M + 4
+
+
+def forward_kernel_bytes(L, fused: bool) -> int:
+    """Algorithmic bytes of the timed forward kernel: packed W and y, plus
+    x_q and s read (two-call path) or X read and x_q, s written (fused)."""
+    act = L.M * L.K * (x_bytes(L) + 1) if fused else L.M * L.K
+    return L.N * L.K // 4 + act + 4 * L.M + 4 * L.M * L.N + 4
+
+
+def layer_ops(L) -> int:
+    return 2 * L.M * L.N * L.K
+
+
+def metric_for(wl) -> tuple[str, str]:
+    if max(L.M for L in wl.layers) <= 4:
+        return "BitLinear GEMV GB/s (HBM roofline)", "GB/s"
+    return "BitLinear GEMM int8 TOPS (tensor roofline)", "TOPS"
+
+
+def fused_available(bl) -> bool:
+    return hasattr(bl, "bitlinear_quant_forward")
+
+
+# ---------------------------------------------------------------- CPU oracle (baseline and reference arm)
+
+def run_oracle(wl, budget_s: float, steps: int | None = None, warmup: int = 0):
+    """Time the oracle on a bounded sample of the per-token step: a fraction f
+    of each layer's output rows (all tokens).  Returns (value, f, s/step, steps)."""
+    import oracle
+
+    layers = []
+    for i, L in enumerate(wl.layers):
+        p, g = oracle.pack_weights(workloads.layer_weights(wl, i).numpy())
+        layers.append((L, p, g, workloads.x_as_f32_numpy(workloads.layer_activations(wl, i))))
+    _, unit = metric_for(wl)
+
+    def one(frac):
+        work = 0.0
+        for (L, p, g, X) in layers:
+            rows = max(1, int(round(L.N * frac)))
+            xq, s = oracle.quant_act(X)
+            oracle.forward(p[:rows], g, xq, s, L.K)
+            work += (L.M * L.K * x_bytes(L) + rows * L.K / 4 + 4 * L.M * rows) if unit == "GB/s" \
+                else 2.0 * L.M * rows * L.K
+        return work
+
+    t0 = time.perf_counter()
+    one(0.02)
+    t_small = time.perf_counter() - t0
+    frac = 0.02
+    if steps:
+        n_total = steps
+        frac = max(1.0 / max(L.N for L in wl.layers), min(1.0, budget_s / (steps * t_small / 0.02)))
+    else:
+        n_total = max(1, int(budget_s / max(t_small, 1e-4)))
+    for _ in range(warmup):
+        one(frac)
+    t0 = time.perf_counter()
+    work = 0.0
+    for _ in range(n_total):
+        work += one(frac)
+    dt = time.perf_counter() - t0
+    return work / dt / (1e9 if unit == "GB/s" else 1e12), frac, dt / n_total, n_total
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_gpu(args, dist, rank, world, local):
+    import ternary_weight_06_b300 as bl
+
+    wl = workloads.WORKLOADS[args.workload]
+    metric, unit = metric_for(wl)
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = props.L2_cache_size
+    stream = torch.cuda.Stream(device=dev)  # graphs cannot be captured on the legacy default stream
+    torch.cuda.set_stream(stream)
+    fused = args.path == "fused"
+    if fused and not fused_available(bl):
+        raise SystemExit("--path fused needs bitlinear_quant_forward")
+
+    # ---- resident inputs: pack each layer's weights once (timed as the "pack" figure)
+    packed, gammas, Xs, Xs_host, ys, xqs, ss = [], [], [], [], [], [], []
+    pack_ms, pack_bytes = 0.0, 0
+    for i, L in enumerate(wl.layers):
+        W = workloads.layer_weights(wl, i).to(dev)
+        bl.bitlinear_pack_weights(W)  # warm
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        Wp, g = bl.bitlinear_pack_weights(W)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        pack_ms += e0.elapsed_time(e1)
+        pack_bytes += 2 * 4 * L.N * L.K + L.N * L.K // 4
+        del W
+        packed.append(Wp)
+        gammas.append(g)
+        X = workloads.layer_activations(wl, i)
+        Xs_host.append(X.pin_memory())
+        Xs.append(X.to(dev))
+        ys.append(torch.empty((L.M, L.N), dtype=torch.float32, device=dev))
+        xqs.append(torch.empty((L.M, L.K), dtype=torch.int8, device=dev))
+        ss.append(torch.empty((L.M,), dtype=torch.float32, device=dev))
+    step_input_bytes = sum(p.numel() + x.numel() * x.element_size() for p, x in zip(packed, Xs))
+    R = min(256, max(1, math.ceil(2 * l2 / step_input_bytes) + 1))
+    Wrot = [[p] + [p.clone() for _ in range(R - 1)] for p in packed]
+    Xrot = [[x] + [x.clone() for _ in range(R - 1)] for x in Xs]
+    torch.cuda.synchronize()
+
+    def step(i, events=None, X_override=None):
+        r = i % R
+        for l in range(len(wl.layers)):
+            X = Xrot[l][r] if X_override is None else X_override[l]
+            if fused:
+                if events is not None:
+                    events[l][0].record(stream)
+                bl.bitlinear_quant_forward(Wrot[l][r], gammas[l], X, y=ys[l], x_q=xqs[l], s=ss[l],
+                                           flags=bl.BITLINEAR_WEIGHTS_RESIDENT, stream=stream)
+            else:
+                bl.bitlinear_quant_act(X, x_q=xqs[l], s=ss[l], stream=stream)
+                if events is not None:
+                    events[l][0].record(stream)
+                bl.bitlinear_forward(Wrot[l][r], gammas[l], xqs[l], ss[l], y=ys[l], stream=stream)
+            if events is not None:
+                events[l][1].record(stream)
+
+    K, Wm = args.steps, args.warmup
+    for i in range(Wm):
+        step(i)
+    torch.cuda.synchronize()
+    bl.bitlinear_check_device_error(stream)
+    launches = K * sum(1 if (fused and L.M <= 4) else 2 for L in wl.layers)
+    peaks, peak_src = load_peaks()
+
+    if args.eager:
+        return run_gpu_eager(args, bl, wl, step, K, stream, dist, world, unit, metric, R, launches)
+
+    # ---- capture: chunks of GRAPH_CHUNK steps; the last full chunk carries
+    # external timing events around every forward launch
+    chunk = min(GRAPH_CHUNK, K)
+    nfull, rem = divmod(K, chunk)
+    nlayers = len(wl.layers)
+    ev = [[[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)] for _ in range(nlayers)]
+          for _ in range(chunk)]
+
+    def capture(n, with_events):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(n):
+                step(j, events=ev[j] if with_events else None)
+        return g
+
+    g_plain = capture(chunk, False)
+    g_timed = capture(chunk, True)
+    g_rem = capture(rem, False) if rem else None
+    for _ in range(2):
+        g_plain.replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region
+    t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    with sampler:
+        barrier(dist)
+        torch.cuda.synchronize()
+        t0e.record(stream)
+        for c in range(nfull):
+            (g_timed if c == nfull - 1 else g_plain).replay()
+        if g_rem is not None:
+            g_rem.replay()
+        t1e.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+    clocks = sampler.summary()
+    ms_per_step = max_over_ranks(dist, t0e.elapsed_time(t1e)) / K
+    bl.bitlinear_check_device_error(stream)
+    fwd_ms = [sum(ev[j][l][0].elapsed_time(ev[j][l][1]) for j in range(chunk)) / chunk for l in range(nlayers)]
+
+    # ---- the graph-replayed outputs must equal an eager re-run of the last step
+    last = [y.clone() for y in ys]
+    step(rem - 1 if rem else chunk - 1)  # graphs were captured with chunk-local step indices
+    torch.cuda.synchronize()
+    verified = all(torch.equal(a, b) for a, b in zip(last, ys))
+
+    step_bytes = sum(layer_bytes(L) for L in wl.layers)
+    step_ops = sum(layer_ops(L) for L in wl.layers)
+    value = world * (step_bytes / (ms_per_step * 1e-3) / 1e9 if unit == "GB/s"
+                     else step_ops / (ms_per_step * 1e-3) / 1e12)
+
+    # ---- dominant kernel roofline (the forward kernel: GEMV or tcgen05 GEMM)
+    fwd_total_ms = sum(fwd_ms)
+    kname = "gemv_kernel" if max(L.M for L in wl.layers) <= 4 else "gemm_tc_kernel"
+    if unit == "GB/s":
+        achieved = sum(forward_kernel_bytes(L, fused) for L in wl.layers) / (fwd_total_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "peak_source": f"{peak_src} hbm_gbs (copy)"}
+    else:
+        achieved = step_ops / (fwd_total_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "peak_source": f"{peak_src} bf16_tflops burst (kind::f16 runs at the bf16 rate)"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["traffic"] = ncu_traffic(kname, args.workload)
+    roof["kernel"] = kname
+    roof["kernel_us"] = [round(x * 1e3, 3) for x in fwd_ms]
+    if fused and kname == "gemv_kernel":
+        roof["note"] = "the timed kernel also quantises the activations (fused)"
+
+    e2e = run_e2e(bl, wl, step, Xs_host, ys, R, K, Wm, stream, dist, world, unit, step_bytes, step_ops)
+
+    return {
+        "metric": metric, "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": K, "warmup": Wm,
+        "ms_per_step": round(ms_per_step, 6), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8 x ternary -> int32 (fp32 rescale)", "data": "synthetic",
+        "config": {"workload": args.workload,
+                   "layers": [f"M={L.M} K={L.K} N={L.N} X={L.x_dtype}" for L in wl.layers],
+                   "l2": f"inputs rotate over {R} copies ({R * step_input_bytes / 2**20:.0f} MiB > 2x L2 "
+                         f"{l2 / 2**20:.0f} MiB)",
+                   "launch": f"CUDA graphs of the C-ABI calls, {chunk} steps per graph",
+                   "path": ("bitlinear_quant_forward (quant fused into the GEMV for M <= 4; weights resident, "
+                            "programmatic dependent launch)") if fused else "bitlinear_quant_act + bitlinear_forward",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "verified": verified,
+        "clocks": clocks,
+        "pack": {"ms": round(pack_ms, 4), "GB/s": round(pack_bytes / (pack_ms * 1e-3) / 1e9, 1),
+                 "note": "gamma + ternarise + pack of every layer (one call each), outside the step"},
+    }
+
+
+def run_gpu_eager(args, bl, wl, step, K, stream, dist, world, unit, metric, R, launches):
+    """Timed region with eager launches (for profilers; includes launch gaps)."""
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for i in range(K):
+        step(i)
+    b.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    ms = max_over_ranks(dist, a.elapsed_time(b)) / K
+    step_bytes = sum(layer_bytes(L) for L in wl.layers)
+    step_ops = sum(layer_ops(L) for L in wl.layers)
+    value = world * (step_bytes / (ms * 1e-3) / 1e9 if unit == "GB/s" else step_ops / (ms * 1e-3) / 1e12)
+    return {"metric": metric, "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int8 x ternary -> int32 (fp32 rescale)", "data": "synthetic",
+            "config": {"workload": args.workload, "launch": "eager (profiling mode)", "path": args.path,
+                       "l2": f"inputs rotate over {R} copies"},
+            "gpu_launches": launches}
+
+
+def run_e2e(bl, wl, step, Xs_host, ys, R, K, Wm, stream, dist, world, unit, step_bytes, step_ops):
+    """The same step through the public API with host buffers: each step copies
+    X from pinned host memory, runs the layer calls, and copies y back to
+    pinned host memory; replayed from CUDA graphs like the device-side number."""
+    dev = ys[0].device
+    Xd = [torch.empty(x.shape, dtype=x.dtype, device=dev) for x in Xs_host]
+    yh = [torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for y in ys]
+    h2d = sum(x.numel() * x.element_size() for x in Xs_host)
+    d2h = sum(y.numel() * y.element_size() for y in ys)
+
+    def e2e_step(i):
+        for l in range(len(wl.layers)):
+            Xd[l].copy_(Xs_host[l], non_blocking=True)
+        step(i, X_override=Xd)
+        for l in range(len(wl.layers)):
+            yh[l].copy_(ys[l], non_blocking=True)
+
+    for i in range(Wm):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    chunk = min(GRAPH_CHUNK, K)
+    nfull, rem = divmod(K, chunk)
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(n):
+                e2e_step(j)
+        return g
+
+    g1 = capture(chunk)
+    g2 = capture(rem) if rem else None
+    g1.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(nfull):
+        g1.replay()
+    if g2 is not None:
+        g2.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    ms = max_over_ranks(dist, a.elapsed_time(b)) / K
+    val = world * (step_bytes / (ms * 1e-3) / 1e9 if unit == "GB/s" else step_ops / (ms * 1e-3) / 1e12)
+    return {"value": round(val, 2), "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(ms, 6), "how": "CUDA graphs of pinned H2D copy + C-ABI calls + D2H copy"}
+
+
+# ---------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="decode", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--path", default="separate", choices=["fused", "separate"],
+                    help="fused: bitlinear_quant_forward; separate: bitlinear_quant_act + bitlinear_forward")
+    ap.add_argument("--eager", action="store_true",
+                    help="launch every step eagerly instead of from CUDA graphs (for profilers)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the oracle CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.steps is None:
+        args.steps = DEFAULT_STEPS[args.workload]
+
+    dist, rank, world, local = dist_setup()
+    wl = workloads.WORKLOADS[args.workload]
+    metric, unit = metric_for(wl)
+
+    if args.impl == "reference":
+        # this build's reference arm is the CPU oracle on the host cores; rank 0 only
+        if rank == 0:
+            value, frac, sec_step, n = run_oracle(wl, budget_s=120.0, steps=args.steps, warmup=args.warmup)
+            line = {"impl": "reference", "metric": metric, "value": round(value, 4), "unit": unit,
+                    "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                    "ms_per_step": round(sec_step * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+                    "vs_baseline": None, "dtype": "int8 x ternary -> int64 sums (fp32 rescale)",
+                    "data": "synthetic",
+                    "config": {"workload": args.workload,
+                               "layers": [f"M={L.M} K={L.K} N={L.N} X={L.x_dtype}" for L in wl.layers]},
+                    "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": 1, "kind": "oracle",
+                                     "sample": f"{frac:.4%} of each layer's output rows, all tokens, per step"},
+                    "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0,
+                            "d2h_bytes_per_step": 0}}
+            print(json.dumps(line), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the BitLinear kernels have no CPU path)")
+    line = run_gpu(args, dist, rank, world, local)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        value, frac, sec_step, n = run_oracle(wl, budget_s=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(value, 4), "unit": unit, "cores": 1, "kind": "oracle",
+                                "sample": f"{n} oracle steps on {frac:.2%} of each layer's output rows "
+                                          f"(all tokens), single thread, {n * sec_step:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -3,9 +3,9 @@
 A thin ctypes layer over ``libbitlinear.so`` (C ABI in ``include/bitlinear.h``).
 Every step of the computation runs in the library's CUDA kernels; this module
 only checks tensor metadata, allocates outputs with torch and passes raw
-device pointers and the current torch stream.  If the library is not built
-(see ``ternary_weight_06_b300.build``) importing this module raises: there is
-no fallback.
+device pointers and the current torch stream.  The library is loaded on first
+use; if it is not built (see ``ternary_weight_06_b300.build``) that first call
+raises ImportError: there is no fallback.
 
 Functions carry the C names:
 
@@ -24,7 +24,7 @@ import torch
 __all__ = [
     "BitLinearError",
     "LIB_PATH",
-    "lib",
+    "get_lib",
     "bitlinear_pack_weights",
     "bitlinear_pack_workspace_bytes",
     "bitlinear_quant_act",
@@ -77,11 +77,19 @@ def _load() -> ctypes.CDLL:
     return L
 
 
-lib = _load()
+_lib = None
+
+
+def get_lib() -> ctypes.CDLL:
+    """The loaded libbitlinear.so (raises ImportError if it was never built)."""
+    global _lib
+    if _lib is None:
+        _lib = _load()
+    return _lib
 
 
 def bitlinear_status_string(status: int) -> str:
-    return lib.bitlinear_status_string(int(status)).decode()
+    return get_lib().bitlinear_status_string(int(status)).decode()
 
 
 def _check(status: int, where: str) -> None:
@@ -106,7 +114,7 @@ def _dev(t: torch.Tensor, name: str, dtype=None) -> int:
 
 
 def bitlinear_pack_workspace_bytes(N: int, K: int) -> int:
-    return int(lib.bitlinear_pack_workspace_bytes(int(N), int(K)))
+    return int(get_lib().bitlinear_pack_workspace_bytes(int(N), int(K)))
 
 
 def bitlinear_pack_weights(W: torch.Tensor, eps: float = 1e-5, W_packed: torch.Tensor | None = None,
@@ -121,7 +129,7 @@ def bitlinear_pack_weights(W: torch.Tensor, eps: float = 1e-5, W_packed: torch.T
     ws_bytes = bitlinear_pack_workspace_bytes(N, K)
     if workspace is None:
         workspace = torch.empty((ws_bytes,), dtype=torch.uint8, device=W.device)
-    _check(lib.bitlinear_pack_weights(_dev(W, "W", torch.float32), N, K, float(eps),
+    _check(get_lib().bitlinear_pack_weights(_dev(W, "W", torch.float32), N, K, float(eps),
                                       _dev(W_packed, "W_packed", torch.uint8), _dev(gamma, "gamma", torch.float32),
                                       _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
                                       _stream(stream)), "bitlinear_pack_weights")
@@ -143,7 +151,7 @@ def bitlinear_quant_act(X: torch.Tensor, x_q: torch.Tensor | None = None, s: tor
         x_q = torch.empty((M, K), dtype=torch.int8, device=X.device)
     if s is None:
         s = torch.empty((M,), dtype=torch.float32, device=X.device)
-    _check(lib.bitlinear_quant_act(_dev(X, "X"), dt, M, K, _dev(x_q, "x_q", torch.int8),
+    _check(get_lib().bitlinear_quant_act(_dev(X, "X"), dt, M, K, _dev(x_q, "x_q", torch.int8),
                                    _dev(s, "s", torch.float32), _stream(stream)), "bitlinear_quant_act")
     return x_q, s
 
@@ -163,7 +171,7 @@ def bitlinear_forward(W_packed: torch.Tensor, gamma: torch.Tensor, x_q: torch.Te
     if acc is True:
         acc = torch.empty((M, N), dtype=torch.int32, device=x_q.device)
     acc_ptr = _dev(acc, "acc", torch.int32) if want_acc else None
-    _check(lib.bitlinear_forward(_dev(W_packed, "W_packed", torch.uint8), _dev(gamma, "gamma", torch.float32),
+    _check(get_lib().bitlinear_forward(_dev(W_packed, "W_packed", torch.uint8), _dev(gamma, "gamma", torch.float32),
                                  _dev(x_q, "x_q", torch.int8), _dev(s, "s", torch.float32), M, N, K,
                                  _dev(y, "y", torch.float32), acc_ptr, _stream(stream)), "bitlinear_forward")
     return (y, acc) if want_acc else y
@@ -171,4 +179,4 @@ def bitlinear_forward(W_packed: torch.Tensor, gamma: torch.Tensor, x_q: torch.Te
 
 def bitlinear_check_device_error(stream=None) -> None:
     """Raise BitLinearError if a kernel gave up on a bounded wait (or the stream failed)."""
-    _check(lib.bitlinear_check_device_error(_stream(stream)), "bitlinear_check_device_error")
+    _check(get_lib().bitlinear_check_device_error(_stream(stream)), "bitlinear_check_device_error")

@@ -60,7 +60,7 @@ GOOD = 0x10000  # a fake, 64 KiB-aligned address: never dereferenced by these ca
 
 
 def pack(bl, W=GOOD, N=8, K=64, eps=1e-5, Wp=GOOD, g=GOOD, ws=GOOD, ws_bytes=4096):
-    return bl.lib.bitlinear_pack_weights(W, N, K, eps, Wp, g, ws, ws_bytes, None)
+    return bl.get_lib().bitlinear_pack_weights(W, N, K, eps, Wp, g, ws, ws_bytes, None)
 
 
 def test_pack_validation(bl):
@@ -83,7 +83,7 @@ def test_pack_validation(bl):
 
 
 def quant(bl, X=GOOD, dt=1, M=4, K=64, xq=GOOD, s=GOOD):
-    return bl.lib.bitlinear_quant_act(X, dt, M, K, xq, s, None)
+    return bl.get_lib().bitlinear_quant_act(X, dt, M, K, xq, s, None)
 
 
 def test_quant_validation(bl):
@@ -101,7 +101,7 @@ def test_quant_validation(bl):
 
 
 def fwd(bl, Wp=GOOD, g=GOOD, xq=GOOD, s=GOOD, M=1, N=16, K=64, y=GOOD, acc=None):
-    return bl.lib.bitlinear_forward(Wp, g, xq, s, M, N, K, y, acc, None)
+    return bl.get_lib().bitlinear_forward(Wp, g, xq, s, M, N, K, y, acc, None)
 
 
 def test_forward_validation(bl):
