@@ -105,6 +105,32 @@ bl_status bitlinear_pack_weights(const float* W, int64_t N, int64_t K, float eps
                                  void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * bitlinear_pack_weights_noalloc -- the same packing as bitlinear_pack_weights
+ * (identical W_packed and gamma), for callers that cannot supply device
+ * workspace: applications whose device memory belongs to their own pool
+ * allocator, code running during CUDA stream capture (where cudaMalloc is not
+ * allowed), or plug-in hosts that only pass pointers to memory they own.  The
+ * BitNet b1.58 pages have no counterpart of this call; it only changes where
+ * the workspace lives.
+ *
+ * The workspace is a fixed 512-byte array inside the library's device image
+ * (held by every GPU that loads the library until the process exits), so the
+ * call allocates nothing and needs no workspace argument.  Arguments, limits
+ * and errors are those of bitlinear_pack_weights; a request needing more
+ * workspace than the array holds returns BL_ERR_WORKSPACE (the packing
+ * workspace is a constant 272 bytes, so no valid shape does).
+ *
+ * The first call on a device, made with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress); make that first call before
+ * any stream capture.  Every call on a device shares the one array, whose
+ * contents persist between calls and are cleared on `stream` at the start of
+ * each call: calls that may overlap on the GPU (different streams without
+ * ordering between them) race on it and must be serialised by the caller.
+ */
+bl_status bitlinear_pack_weights_noalloc(const float* W, int64_t N, int64_t K, float eps, uint8_t* W_packed,
+                                         float* gamma, cudaStream_t stream);
+
+/*
  * bitlinear_quant_act -- per-token absmax quantisation of activations to int8
  * (anthology note-168, "What it does": activations at 8 bits; yousumm.com
  * transcript: messages squeezed into "eight-bit numbers").

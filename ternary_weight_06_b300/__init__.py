@@ -43,6 +43,7 @@ BL_F32, BL_BF16 = 0, 1
 EXPORTED_SYMBOLS = (
     "bitlinear_pack_workspace_bytes",
     "bitlinear_pack_weights",
+    "bitlinear_pack_weights_noalloc",
     "bitlinear_quant_act",
     "bitlinear_forward",
     "bitlinear_check_device_error",
@@ -70,6 +71,8 @@ def _load() -> ctypes.CDLL:
     L.bitlinear_quant_act.restype = i32
     L.bitlinear_forward.argtypes = [P, P, P, P, i64, i64, i64, P, P, P]
     L.bitlinear_forward.restype = i32
+    L.bitlinear_pack_weights_noalloc.argtypes = [P, i64, i64, f32, P, P, P]
+    L.bitlinear_pack_weights_noalloc.restype = i32
     L.bitlinear_check_device_error.argtypes = [P]
     L.bitlinear_check_device_error.restype = i32
     L.bitlinear_status_string.argtypes = [i32]
