@@ -169,6 +169,36 @@ bl_status bitlinear_quant_act(const void* X, bl_dtype dtype, int64_t M, int64_t 
 bl_status bitlinear_forward(const uint8_t* W_packed, const float* gamma, const int8_t* x_q, const float* s,
                             int64_t M, int64_t N, int64_t K, float* y, int32_t* acc, cudaStream_t stream);
 
+/* Flag of bitlinear_quant_forward: W_packed and gamma are NOT written by any
+ * work still pending on `stream` (true once the weights are packed and
+ * synchronised, as in serving).  The call may then start streaming weights
+ * before the preceding kernel on `stream` has finished (programmatic
+ * dependent launch); activations are still read only after it completes. */
+#define BITLINEAR_WEIGHTS_RESIDENT 1u
+
+/*
+ * bitlinear_quant_forward -- bitlinear_quant_act followed by
+ * bitlinear_forward, as one call: per-token absmax int8 quantisation of X
+ * (anthology note-168, "What it does": activations at 8 bits) and the
+ * ternary x int8 product with the gamma/s rescale.  For M <= 4 (and K <=
+ * 65536) both run in ONE kernel (each CTA quantises the few token rows it
+ * needs; the first CTA writes x_q and s out), which removes a launch and a
+ * round trip per layer in decode; otherwise it is the two kernels in
+ * sequence.  Results are bit-identical to the two separate calls.
+ *
+ *   W_packed, gamma     in   as for bitlinear_forward
+ *   X, dtype            in   as for bitlinear_quant_act
+ *   M, N, K             in   as for bitlinear_forward
+ *   y                   out  fp32 [M, N], 16-byte aligned
+ *   x_q, s              out  int8 [M, K] (16-byte aligned) and fp32 [M] (4-byte
+ *                            aligned): the quantised activations and scales
+ *   acc                 out  optional int32 [M, N] (may be NULL)
+ *   flags               in   0 or BITLINEAR_WEIGHTS_RESIDENT
+ */
+bl_status bitlinear_quant_forward(const uint8_t* W_packed, const float* gamma, const void* X, bl_dtype dtype,
+                                  int64_t M, int64_t N, int64_t K, float* y, int8_t* x_q, float* s, int32_t* acc,
+                                  unsigned flags, cudaStream_t stream);
+
 /*
  * bitlinear_check_device_error -- waits for `stream`, then reports and clears
  * the library's device error word: BL_ERR_TIMEOUT if a kernel gave up on a

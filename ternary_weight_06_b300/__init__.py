@@ -29,8 +29,10 @@ __all__ = [
     "bitlinear_pack_workspace_bytes",
     "bitlinear_quant_act",
     "bitlinear_forward",
+    "bitlinear_quant_forward",
     "bitlinear_check_device_error",
     "bitlinear_status_string",
+    "BITLINEAR_WEIGHTS_RESIDENT",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -39,6 +41,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libbitlinea
 BL_OK, BL_ERR_INVALID_ARG, BL_ERR_UNSUPPORTED_SHAPE, BL_ERR_MISALIGNED, BL_ERR_WORKSPACE, BL_ERR_CUDA, \
     BL_ERR_TIMEOUT = range(7)
 BL_F32, BL_BF16 = 0, 1
+BITLINEAR_WEIGHTS_RESIDENT = 1
 
 EXPORTED_SYMBOLS = (
     "bitlinear_pack_workspace_bytes",
@@ -46,6 +49,7 @@ EXPORTED_SYMBOLS = (
     "bitlinear_pack_weights_noalloc",
     "bitlinear_quant_act",
     "bitlinear_forward",
+    "bitlinear_quant_forward",
     "bitlinear_check_device_error",
     "bitlinear_status_string",
 )
@@ -73,6 +77,8 @@ def _load() -> ctypes.CDLL:
     L.bitlinear_forward.restype = i32
     L.bitlinear_pack_weights_noalloc.argtypes = [P, i64, i64, f32, P, P, P]
     L.bitlinear_pack_weights_noalloc.restype = i32
+    L.bitlinear_quant_forward.argtypes = [P, P, P, i32, i64, i64, i64, P, P, P, P, ctypes.c_uint, P]
+    L.bitlinear_quant_forward.restype = i32
     L.bitlinear_check_device_error.argtypes = [P]
     L.bitlinear_check_device_error.restype = i32
     L.bitlinear_status_string.argtypes = [i32]
@@ -178,6 +184,44 @@ def bitlinear_forward(W_packed: torch.Tensor, gamma: torch.Tensor, x_q: torch.Te
                                  _dev(x_q, "x_q", torch.int8), _dev(s, "s", torch.float32), M, N, K,
                                  _dev(y, "y", torch.float32), acc_ptr, _stream(stream)), "bitlinear_forward")
     return (y, acc) if want_acc else y
+
+
+def bitlinear_quant_forward(W_packed: torch.Tensor, gamma: torch.Tensor, X: torch.Tensor,
+                            y: torch.Tensor | None = None, x_q: torch.Tensor | None = None,
+                            s: torch.Tensor | None = None, acc: torch.Tensor | bool | None = None, flags: int = 0,
+                            stream=None):
+    """Quantise X (bf16/fp32 [M, K]) and apply the BitLinear product in one call
+    (one kernel for M <= 4).  Returns (y, x_q, s), or (y, x_q, s, acc) with ``acc``.
+    ``flags=BITLINEAR_WEIGHTS_RESIDENT`` lets the kernel stream weights before the
+    preceding kernel on the stream finishes; only valid when no pending work on
+    the stream writes W_packed or gamma."""
+    N, K4 = W_packed.shape
+    M, K = X.shape
+    if K4 * 4 != K:
+        raise ValueError(f"W_packed has K/4 = {K4} but X has K = {K}")
+    if X.dtype == torch.bfloat16:
+        dt = BL_BF16
+    elif X.dtype == torch.float32:
+        dt = BL_F32
+    else:
+        raise ValueError(f"X must be bf16 or fp32, got {X.dtype}")
+    dev = X.device
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    if x_q is None:
+        x_q = torch.empty((M, K), dtype=torch.int8, device=dev)
+    if s is None:
+        s = torch.empty((M,), dtype=torch.float32, device=dev)
+    want_acc = acc is not None and acc is not False
+    if acc is True:
+        acc = torch.empty((M, N), dtype=torch.int32, device=dev)
+    acc_ptr = _dev(acc, "acc", torch.int32) if want_acc else None
+    _check(get_lib().bitlinear_quant_forward(_dev(W_packed, "W_packed", torch.uint8),
+                                             _dev(gamma, "gamma", torch.float32), _dev(X, "X"), dt, M, N, K,
+                                             _dev(y, "y", torch.float32), _dev(x_q, "x_q", torch.int8),
+                                             _dev(s, "s", torch.float32), acc_ptr, int(flags), _stream(stream)),
+           "bitlinear_quant_forward")
+    return (y, x_q, s, acc) if want_acc else (y, x_q, s)
 
 
 def bitlinear_check_device_error(stream=None) -> None:

@@ -1,5 +1,5 @@
 // gemv.cu -- streaming ternary GEMV for a few tokens (decode), with the
-// dequant epilogue fused.
+// dequant epilogue fused, and optionally the activation quantisation too.
 //
 // The work is bounded by reading the packed weights from HBM once ("bundles
 // four chips into a single byte, slides that bundle across the GPU highway,
@@ -8,21 +8,32 @@
 // note-168, "The part that is a bet rather than a measurement").
 //
 // Layout of the work:
-//   * one CTA per SM, each owning a contiguous block of ~N/#SM output rows;
-//     because packed rows are contiguous, that block is one contiguous byte
-//     range, streamed through a ring of shared-memory stages by 1-D bulk
-//     async copies (one elected producer thread, mbarrier completion);
-//   * consumer warps own a fixed slice of K: lane l of k-warp kw handles the
-//     16-code words w = kw*Cw + l + 32 j of every row.  Their activations are
-//     loaded once into registers, so shared memory carries weights only;
+//   * one CTA per SM owns a contiguous block of ~N/#SM output rows; packed rows
+//     are contiguous, so the block is one byte range, streamed into a ring of
+//     shared-memory stages by 1-D bulk async copies issued from one producer
+//     thread (mbarrier completion, bounded waits).  A decode-sized block fits
+//     the ring whole, so all of it is requested at kernel entry;
+//   * the copies are issued BEFORE the kernel waits on its predecessor
+//     (griddepcontrol.wait), and the kernel lets its own successor launch
+//     early (griddepcontrol.launch_dependents).  Under programmatic dependent
+//     launch a chain of layers therefore streams the next layer's weights
+//     while the previous layer finishes; two CTAs fit per SM for that;
+//   * consumer warps own a fixed K slice: lane l of k-warp kw handles the
+//     16-code words w = kw*Cw + l + 32 j (j < J, J fixed at compile time) of
+//     every row, with the matching activations held in registers;
 //   * unpacking a 32-bit word P of 16 codes takes two ops per 4 weights:
-//     S_i = (P >> 2i) & 0x03030303 holds the codes of weights 4j+i (j = 0..3)
-//     as bytes in {0,1,2}.  The matching activation word X'_i holds x[4j+i]
-//     (a 4x4 byte transpose of the natural 16 activations, done once), so
+//     S_i = (P >> 2i) & 0x03030303 holds the codes c of weights 4j+i (j=0..3)
+//     as bytes in {0,1,2}; the activation word X'_i holds x[4j+i] (a 4x4 byte
+//     transpose of the natural 16 activations, done once), so
 //       sum_k (c_k - 1) x_k = sum_i dp4a(S_i, X'_i) - sum_k x_k,
 //     an exact int32 sum ("only involves integer addition");
-//   * y[m,n] = fp32(acc) * fp32(gamma / s[m]) is written straight from the
-//     reduced accumulator (and acc itself when requested).
+//   * a warp handles four rows per iteration (independent dependency chains),
+//     reduces each over its lanes and adds it into a per-CTA shared
+//     accumulator; after the last stage the CTA writes y = fp32(acc) *
+//     fp32(gamma / s[m]) with coalesced stores.
+// The fused variant quantises X itself (per-token absmax; the same IEEE
+// operations as the stand-alone kernel, so x_q and s are bit-identical); the
+// first CTA also writes x_q and s out.
 #include <cstdint>
 
 #include "common.cuh"
@@ -31,23 +42,29 @@
 namespace bl {
 namespace {
 
-constexpr int kStages = 6;
-constexpr int kStageBytesTarget = 16384;
-constexpr int kMaxRowsPerStage = 128;
-constexpr int kMaxConsumerWarps = 16;
+constexpr int kStages = 3;
+constexpr int kStageBytesTarget = 32768;
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = 32 * (kConsumerWarps + 1);
+constexpr int kRowsPerIter = 4;
+constexpr float kActClampEps = 1e-5f;
 
 struct GemvCfg {
   const uint8_t* Wp;
   const float* gamma;
-  const int8_t* xq;
-  const float* s;
+  const int8_t* xq_in;  // two-call path: quantised activations
+  const float* s_in;    // two-call path: per-token scales
+  const void* X;        // fused: raw activations
+  int8_t* xq_out;       // fused: x_q output (first CTA writes it)
+  float* s_out;         // fused: s output
   float* y;
   int32_t* acc;
   uint32_t* err;
   int64_t N, K;
-  int tok0, ntok;  // tokens of this launch
-  int rows_per_cta, rows_per_stage, row_bytes;
-  int kw, rwp, words_per_row, words_per_warp, J;
+  int tok0, ntok;  // tokens of this launch (<= MT)
+  int x_bf16;
+  int rows_per_cta, rows_per_stage, row_bytes, nslots;  // nslots <= kStages ring slots
+  int kw, words_per_row, words_per_warp;
 };
 
 __device__ __forceinline__ void transpose4x4(uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3, uint32_t* o) {
@@ -75,58 +92,84 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, ui
   }
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps) : "memory"); }
+
+__device__ __forceinline__ uint32_t q8(float x, float s) {
+  int q = __float2int_rn(__fmul_rn(x, s));
+  q = min(max(q, -128), 127);
+  return (uint32_t)q & 0xffu;
 }
 
-template <int MT, int JMAX>
-__global__ void __launch_bounds__(32 * (1 + kMaxConsumerWarps)) gemv_kernel(const GemvCfg c) {
+// 16 activations of a token row starting at element k0, quantised, as 4 natural int8 words.
+__device__ __forceinline__ void quant16(const void* xrow, int x_bf16, int64_t k0, float s, uint32_t* out) {
+  if (x_bf16) {
+    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(xrow) + k0);
+    const uint4 a = __ldg(p), b = __ldg(p + 1);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      out[i] = q8(__uint_as_float(w[2 * i] << 16), s) | (q8(__uint_as_float(w[2 * i] & 0xffff0000u), s) << 8) |
+               (q8(__uint_as_float(w[2 * i + 1] << 16), s) << 16) |
+               (q8(__uint_as_float(w[2 * i + 1] & 0xffff0000u), s) << 24);
+  } else {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(xrow) + k0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 v = __ldg(p + i);
+      out[i] = q8(v.x, s) | (q8(v.y, s) << 8) | (q8(v.z, s) << 16) | (q8(v.w, s) << 24);
+    }
+  }
+}
+
+template <int MT, int J, bool FUSED>
+__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvCfg c) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int SR = c.rows_per_stage;
   const int stage_bytes = SR * c.row_bytes;  // multiple of 16
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * stage_bytes);
+  const int NS = c.nslots;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * stage_bytes);
   uint64_t* empty = full + kStages;
-  int32_t* red = reinterpret_cast<int32_t*>(empty + kStages);
-  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(red + kStages * SR * MT);
-  const int n_consumers = c.kw * c.rwp;
+  int32_t* acc_sm = reinterpret_cast<int32_t*>(empty + kStages);                   // [rows_per_cta][MT]
+  uint32_t* amax_sm = reinterpret_cast<uint32_t*>(acc_sm + c.rows_per_cta * MT);  // [kConsumerWarps][MT]
+  float* tsc_sm = reinterpret_cast<float*>(amax_sm + kConsumerWarps * MT);       // [MT]
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(tsc_sm + MT);
 
   const int64_t row0 = (int64_t)blockIdx.x * c.rows_per_cta;
-  const int64_t row_end = min(row0 + (int64_t)c.rows_per_cta, c.N);
-  const int nrows = (int)(row_end - row0);
+  const int nrows = (int)min((int64_t)c.rows_per_cta, c.N - row0);
   const int nstages = (nrows + SR - 1) / SR;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], (uint32_t)n_consumers);
+      mbar_init(&empty[i], kConsumerWarps);
     }
     *abort_flag = 0u;
     fence_mbarrier_init();
   }
-  for (int i = threadIdx.x; i < kStages * SR * MT; i += blockDim.x) red[i] = 0;
+  for (int i = threadIdx.x; i < c.rows_per_cta * MT; i += blockDim.x) acc_sm[i] = 0;
   __syncthreads();
 
-  if (warp == 0) {
-    // ---------------- producer: one elected thread streams the row block.
+  if (warp == kConsumerWarps) {
+    // ---------------- producer: weights only, so it may run ahead of griddepcontrol.wait
     if (lane == 0) {
       int issued = 0;
       for (int st = 0; st < nstages; ++st) {
-        const int slot = st % kStages;
-        if (st >= kStages &&
-            !wait_or_abort(&empty[slot], (uint32_t)((st / kStages) - 1) & 1u, c.err, kErrGemvEmptyWait, abort_flag))
+        const int slot = st % NS;
+        if (st >= NS && !wait_or_abort(&empty[slot], (uint32_t)((st / NS) - 1) & 1u, c.err, kErrGemvEmptyWait,
+                                       abort_flag))
           break;
         const int rows = min(SR, nrows - st * SR);
         const uint32_t bytes = (uint32_t)(rows * c.row_bytes);
         mbar_arrive_expect_tx(&full[slot], bytes);
         bulk_g2s(smem + slot * stage_bytes, c.Wp + (row0 + (int64_t)st * SR) * c.row_bytes, bytes, &full[slot]);
         issued = st + 1;
+        if (st == min(nstages, NS) - 1) pdl_launch_dependents();
       }
       if (*abort_flag) {
         // Let every copy this CTA started land before its shared memory goes away.
-        for (int st = (issued > kStages ? issued - kStages : 0); st < issued; ++st) {
-          uint64_t* bar = &full[st % kStages];
-          const uint32_t a = smem_u32(bar), par = (uint32_t)(st / kStages) & 1u;
+        for (int st = (issued > NS ? issued - NS : 0); st < issued; ++st) {
+          const uint32_t a = smem_u32(&full[st % NS]), par = (uint32_t)(st / NS) & 1u;
           const uint64_t t0 = globaltimer_ns();
           while (!mbar_try_wait(a, par) && globaltimer_ns() - t0 < kWaitLimitNs) {
           }
@@ -137,131 +180,226 @@ __global__ void __launch_bounds__(32 * (1 + kMaxConsumerWarps)) gemv_kernel(cons
   }
 
   // ---------------- consumers
-  const int cw = warp - 1;
-  const int kw = cw % c.kw, rw = cw / c.kw;
-  pdl_wait();  // activations and scales may come from the preceding kernel
-
-  const int wbeg = kw * c.words_per_warp;
+  const int kwi = warp % c.kw, rg = warp / c.kw, nrg = kConsumerWarps / c.kw;
+  pdl_wait();  // activations, scales and gamma may come from the preceding kernel
+  const int wbeg = kwi * c.words_per_warp;
   const int wend = min(wbeg + c.words_per_warp, c.words_per_row);
-  uint32_t xr[JMAX][4][MT];
-  int32_t xsum[MT];
-  float tscale[MT];
   const float gamma = __ldg(c.gamma);
-#pragma unroll
-  for (int t = 0; t < MT; ++t) {
-    xsum[t] = 0;
-    tscale[t] = t < c.ntok ? __fdiv_rn(gamma, __ldg(c.s + c.tok0 + t)) : 0.0f;
-  }
-#pragma unroll
-  for (int j = 0; j < JMAX; ++j) {
-    const int w = wbeg + lane + 32 * j;
-    const bool valid = j < c.J && w < wend;
+
+  float s_tok[MT];
+  if (FUSED) {
+    // per-token absmax over the whole row; every consumer thread takes 16-element words
 #pragma unroll
     for (int t = 0; t < MT; ++t) {
-      if (valid && t < c.ntok) {
-        const int4 v = __ldg(reinterpret_cast<const int4*>(c.xq + (int64_t)(c.tok0 + t) * c.K) + w);
-        uint32_t o[4];
-        transpose4x4((uint32_t)v.x, (uint32_t)v.y, (uint32_t)v.z, (uint32_t)v.w, o);
+      uint32_t m = 0;
+      if (t < c.ntok) {
+        const int64_t base = (int64_t)(c.tok0 + t) * c.K;
+        for (int w = threadIdx.x; w < c.words_per_row; w += 32 * kConsumerWarps) {
+          if (c.x_bf16) {
+            const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(c.X) + base + 16 * w);
+            const uint4 a = __ldg(p), b = __ldg(p + 1);
+            const uint32_t v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) xr[j][i][t] = o[i];
-        xsum[t] = __dp4a(v.x, 0x01010101, __dp4a(v.y, 0x01010101, __dp4a(v.z, 0x01010101, __dp4a(v.w, 0x01010101, xsum[t]))));
-      } else {
+            for (int i = 0; i < 8; ++i) m = max(m, max((v[i] << 16) & 0x7fff0000u, v[i] & 0x7fff0000u));
+          } else {
+            const uint4* p = reinterpret_cast<const uint4*>(static_cast<const float*>(c.X) + base + 16 * w);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) xr[j][i][t] = 0u;
+            for (int i = 0; i < 4; ++i) {
+              const uint4 v = __ldg(p + i);
+              m = max(m, max(max(v.x & 0x7fffffffu, v.y & 0x7fffffffu), max(v.z & 0x7fffffffu, v.w & 0x7fffffffu)));
+            }
+          }
+        }
       }
+      m = __reduce_max_sync(0xffffffffu, m);
+      if (lane == 0) amax_sm[warp * MT + t] = m;
+    }
+    consumer_bar();
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+      uint32_t m = 0;
+#pragma unroll
+      for (int w8 = 0; w8 < kConsumerWarps; ++w8) m = max(m, amax_sm[w8 * MT + t]);
+      float a = __uint_as_float(m);
+      if (a < kActClampEps) a = kActClampEps;
+      s_tok[t] = __fdiv_rn(127.0f, a);
+    }
+  } else {
+#pragma unroll
+    for (int t = 0; t < MT; ++t) s_tok[t] = t < c.ntok ? __ldg(c.s_in + c.tok0 + t) : 1.0f;
+  }
+  if (warp == 0 && lane < MT && lane < c.ntok) {
+    float st = s_tok[0];
+#pragma unroll
+    for (int t = 1; t < MT; ++t)
+      if (lane == t) st = s_tok[t];
+    tsc_sm[lane] = __fdiv_rn(gamma, st);
+    if (FUSED && blockIdx.x == 0) c.s_out[c.tok0 + lane] = st;
+  }
+
+  // activations of this lane's words, transposed, plus their sums
+  uint32_t xr[J][4][MT];
+  int32_t xsum[MT];
+#pragma unroll
+  for (int t = 0; t < MT; ++t) xsum[t] = 0;
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const int w = wbeg + lane + 32 * j;
+    const bool valid = w < wend;
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+      uint32_t nat[4] = {0u, 0u, 0u, 0u};
+      if (valid && t < c.ntok) {
+        const int64_t tok = c.tok0 + t;
+        if (FUSED) {
+          const char* xrow = static_cast<const char*>(c.X) + tok * c.K * (c.x_bf16 ? 2 : 4);
+          quant16(xrow, c.x_bf16, 16 * (int64_t)w, s_tok[t], nat);
+          if (blockIdx.x == 0 && rg == 0)
+            reinterpret_cast<uint4*>(c.xq_out + tok * c.K)[w] = make_uint4(nat[0], nat[1], nat[2], nat[3]);
+        } else {
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(c.xq_in + tok * c.K) + w);
+          nat[0] = v.x;
+          nat[1] = v.y;
+          nat[2] = v.z;
+          nat[3] = v.w;
+        }
+      }
+      uint32_t o[4];
+      transpose4x4(nat[0], nat[1], nat[2], nat[3], o);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) xr[j][i][t] = o[i];
+      xsum[t] = __dp4a((int)nat[0], 0x01010101,
+                       __dp4a((int)nat[1], 0x01010101,
+                              __dp4a((int)nat[2], 0x01010101, __dp4a((int)nat[3], 0x01010101, xsum[t]))));
     }
   }
 
   for (int st = 0; st < nstages; ++st) {
-    const int slot = st % kStages;
+    const int slot = st % NS;
     const int rows = min(SR, nrows - st * SR);
-    const bool ok = wait_or_abort(&full[slot], (uint32_t)(st / kStages) & 1u, c.err, kErrGemvFullWait, abort_flag);
+    const bool ok = wait_or_abort(&full[slot], (uint32_t)(st / NS) & 1u, c.err, kErrGemvFullWait, abort_flag);
     if (ok) {
       const uint8_t* base = smem + slot * stage_bytes;
-      for (int r = rw; r < rows; r += c.rwp) {
-        const uint32_t* rowp = reinterpret_cast<const uint32_t*>(base + r * c.row_bytes);
-        int32_t a[MT][4];
+      for (int r0 = rg * kRowsPerIter; r0 < rows; r0 += nrg * kRowsPerIter) {
+        int32_t a[kRowsPerIter][MT];
 #pragma unroll
-        for (int t = 0; t < MT; ++t)
+        for (int rr = 0; rr < kRowsPerIter; ++rr)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) a[t][i] = 0;
+          for (int t = 0; t < MT; ++t) a[rr][t] = 0;
 #pragma unroll
-        for (int j = 0; j < JMAX; ++j) {
-          const int w = wbeg + lane + 32 * j;
-          if (j < c.J && w < wend) {
-            const uint32_t P = rowp[w];
-            const uint32_t S[4] = {P & 0x03030303u, (P >> 2) & 0x03030303u, (P >> 4) & 0x03030303u,
-                                   (P >> 6) & 0x03030303u};
+        for (int rr = 0; rr < kRowsPerIter; ++rr) {
+          if (r0 + rr < rows) {
+            const uint32_t* rowp = reinterpret_cast<const uint32_t*>(base + (r0 + rr) * c.row_bytes);
 #pragma unroll
-            for (int t = 0; t < MT; ++t)
+            for (int j = 0; j < J; ++j) {
+              const int w = wbeg + lane + 32 * j;
+              if (w < wend) {
+                const uint32_t P = rowp[w];
 #pragma unroll
-              for (int i = 0; i < 4; ++i) a[t][i] = __dp4a((int)S[i], (int)xr[j][i][t], a[t][i]);
+                for (int i = 0; i < 4; ++i) {
+                  const int S = (int)((P >> (2 * i)) & 0x03030303u);
+#pragma unroll
+                  for (int t = 0; t < MT; ++t) a[rr][t] = __dp4a(S, (int)xr[j][i][t], a[rr][t]);
+                }
+              }
+            }
           }
         }
 #pragma unroll
-        for (int t = 0; t < MT; ++t) {
-          int32_t v = a[t][0] + a[t][1] + a[t][2] + a[t][3] - xsum[t];
+        for (int rr = 0; rr < kRowsPerIter; ++rr)
 #pragma unroll
-          for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-          if (lane == 0 && t < c.ntok) {
-            if (c.kw == 1) {
-              const int64_t n = row0 + (int64_t)st * SR + r;
-              const int64_t o = (int64_t)(c.tok0 + t) * c.N + n;
-              c.y[o] = __fmul_rn(__int2float_rn(v), tscale[t]);
-              if (c.acc) c.acc[o] = v;
-            } else {
-              atomicAdd(&red[(slot * SR + r) * MT + t], v);
-            }
+          for (int t = 0; t < MT; ++t) {
+            int32_t v = a[rr][t] - xsum[t];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+            a[rr][t] = v;
           }
+        if (lane == 0) {
+#pragma unroll
+          for (int rr = 0; rr < kRowsPerIter; ++rr)
+            if (r0 + rr < rows)
+#pragma unroll
+              for (int t = 0; t < MT; ++t) atomicAdd(&acc_sm[(st * SR + r0 + rr) * MT + t], a[rr][t]);
         }
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
-    if (c.kw > 1) {
-      named_bar_sync(1, n_consumers * 32);
-      if (ok) {
-        for (int idx = cw * 32 + lane; idx < rows * MT; idx += n_consumers * 32) {
-          const int r = idx / MT, t = idx % MT;
-          int32_t* cell = &red[(slot * SR + r) * MT + t];
-          if (t < c.ntok) {
-            const int32_t v = *cell;
-            const int64_t n = row0 + (int64_t)st * SR + r;
-            const int64_t o = (int64_t)(c.tok0 + t) * c.N + n;
-            float ts = tscale[0];
-#pragma unroll
-            for (int u = 1; u < MT; ++u)
-              if (t == u) ts = tscale[u];
-            c.y[o] = __fmul_rn(__int2float_rn(v), ts);
-            if (c.acc) c.acc[o] = v;
-          }
-          *cell = 0;
-        }
-      }
+  }
+  consumer_bar();
+  if (*abort_flag == 0u) {
+    for (int idx = threadIdx.x; idx < nrows * c.ntok; idx += 32 * kConsumerWarps) {
+      const int t = idx / nrows, r = idx - t * nrows;
+      const int32_t v = acc_sm[r * MT + t];
+      const int64_t o = (int64_t)(c.tok0 + t) * c.N + row0 + r;
+      c.y[o] = __fmul_rn(__int2float_rn(v), tsc_sm[t]);
+      if (c.acc) c.acc[o] = v;
     }
   }
 }
 
-template <int MT, int JMAX>
-cudaError_t launch_one(const GemvCfg& c, int grid, cudaStream_t stream) {
-  const int threads = 32 * (1 + c.kw * c.rwp);
-  const size_t smem = (size_t)kStages * c.rows_per_stage * c.row_bytes + 2 * kStages * sizeof(uint64_t) +
-                      (size_t)kStages * c.rows_per_stage * MT * sizeof(int32_t) + 16;
-  auto kern = gemv_kernel<MT, JMAX>;
+template <int MT, int J, bool FUSED>
+cudaError_t launch_one(const GemvCfg& c, int grid, size_t smem, bool pdl, cudaStream_t stream) {
+  auto kern = gemv_kernel<MT, J, FUSED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, threads, smem, stream>>>(c);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, c);
 }
 
-}  // namespace
+// Activation registers per lane are J*4*MT.  The preferred limit keeps every
+// variant free of register spills; the hard limit only serves K > 48K.
+constexpr int jmax_for(int mt) { return mt == 1 ? 16 : mt == 2 ? 8 : 4; }
+constexpr int jpref_for(int mt) { return mt == 1 ? 12 : mt == 2 ? 6 : 3; }
 
-cudaError_t launch_gemv(const ForwardArgs& a, int num_sms, cudaStream_t stream) {
+// The smallest instantiated J >= the J a launch needs.
+template <int MT, bool FUSED>
+cudaError_t dispatch_j(const GemvCfg& c, int J, int grid, size_t smem, bool pdl, cudaStream_t stream) {
+  switch (J) {
+    case 1: return launch_one<MT, 1, FUSED>(c, grid, smem, pdl, stream);
+    case 2: return launch_one<MT, 2, FUSED>(c, grid, smem, pdl, stream);
+    case 3: return launch_one<MT, 3, FUSED>(c, grid, smem, pdl, stream);
+    case 4: return launch_one<MT, 4, FUSED>(c, grid, smem, pdl, stream);
+    default: break;
+  }
+  if constexpr (MT <= 2) {
+    switch (J) {
+      case 5: return launch_one<MT, 5, FUSED>(c, grid, smem, pdl, stream);
+      case 6: return launch_one<MT, 6, FUSED>(c, grid, smem, pdl, stream);
+      case 7: return launch_one<MT, 7, FUSED>(c, grid, smem, pdl, stream);
+      case 8: return launch_one<MT, 8, FUSED>(c, grid, smem, pdl, stream);
+      default: break;
+    }
+  }
+  if constexpr (MT == 1) {
+    if (J <= 10) return launch_one<MT, 10, FUSED>(c, grid, smem, pdl, stream);
+    if (J <= 12) return launch_one<MT, 12, FUSED>(c, grid, smem, pdl, stream);
+    if (J <= 14) return launch_one<MT, 14, FUSED>(c, grid, smem, pdl, stream);
+    if (J <= 16) return launch_one<MT, 16, FUSED>(c, grid, smem, pdl, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t run(const ForwardArgs& a, const void* X, bool x_bf16, int8_t* xq_out, float* s_out, bool fused,
+                bool pdl, int num_sms, cudaStream_t stream) {
   GemvCfg c{};
   c.Wp = a.Wp;
   c.gamma = a.gamma;
-  c.xq = a.xq;
-  c.s = a.s;
+  c.xq_in = a.xq;
+  c.s_in = a.s;
+  c.X = X;
+  c.x_bf16 = x_bf16 ? 1 : 0;
+  c.xq_out = xq_out;
+  c.s_out = s_out;
   c.y = a.y;
   c.acc = a.acc;
   c.err = a.err;
@@ -274,35 +412,51 @@ cudaError_t launch_gemv(const ForwardArgs& a, int num_sms, cudaStream_t stream) 
   c.rows_per_cta = (int)((a.N + grid - 1) / grid);
   grid = (int)((a.N + c.rows_per_cta - 1) / c.rows_per_cta);
   int sr = kStageBytesTarget / c.row_bytes;
-  if (sr > kMaxRowsPerStage) sr = kMaxRowsPerStage;
   if (sr < 1) sr = 1;
   if (sr > c.rows_per_cta) sr = c.rows_per_cta;
   c.rows_per_stage = sr;
+  const int max_stages = (c.rows_per_cta + sr - 1) / sr;
+  c.nslots = max_stages < kStages ? max_stages : kStages;
 
-  // tokens per pass: the largest of 4, 2, 1 (<= M) whose k-split fits 16 warps.
-  // Each lane keeps 64 activation registers: JMAX words x 4 x MT tokens.
-  auto kw_for = [&](int jmax) { return (c.words_per_row + 32 * jmax - 1) / (32 * jmax); };
-  int mt = 1;
-  if (a.M >= 4 && kw_for(4) <= kMaxConsumerWarps) mt = 4;
-  else if (a.M >= 2 && kw_for(8) <= kMaxConsumerWarps) mt = 2;
-  const int jmax = 16 / mt;
-  c.kw = kw_for(jmax);
-  if (c.kw > kMaxConsumerWarps) return cudaErrorNotSupported;
+  // tokens per pass: 4, 2 or 1 (<= M), limited by the activation registers
+  int mt = a.M >= 4 ? 4 : a.M >= 2 ? 2 : 1;
+  while (mt > 1 && (c.words_per_row + 32 * kConsumerWarps - 1) / (32 * kConsumerWarps) > jmax_for(mt)) mt /= 2;
+  int kw = 1;
+  while (kw < kConsumerWarps && (c.words_per_row + 32 * kw - 1) / (32 * kw) > jpref_for(mt)) kw *= 2;
+  c.kw = kw;
   c.words_per_warp = (c.words_per_row + c.kw - 1) / c.kw;
-  c.J = (c.words_per_warp + 31) / 32;
-  c.rwp = kMaxConsumerWarps / c.kw;
-  if (c.rwp < 1) c.rwp = 1;
+  const int J = (c.words_per_warp + 31) / 32;
+  if (J > jmax_for(mt)) return cudaErrorInvalidValue;  // K beyond the GEMV's register budget
+  const size_t smem = (size_t)c.nslots * c.rows_per_stage * c.row_bytes + 2 * kStages * sizeof(uint64_t) +
+                      (size_t)c.rows_per_cta * mt * sizeof(int32_t) + (kConsumerWarps + 1) * mt * 4 + 16;
 
   for (int64_t t0 = 0; t0 < a.M; t0 += mt) {
     c.tok0 = (int)t0;
     c.ntok = (int)(a.M - t0 < mt ? a.M - t0 : mt);
     cudaError_t e;
-    if (mt == 4) e = launch_one<4, 4>(c, grid, stream);
-    else if (mt == 2) e = launch_one<2, 8>(c, grid, stream);
-    else e = launch_one<1, 16>(c, grid, stream);
+    if (fused) {
+      if (mt == 4) e = dispatch_j<4, true>(c, J, grid, smem, pdl, stream);
+      else if (mt == 2) e = dispatch_j<2, true>(c, J, grid, smem, pdl, stream);
+      else e = dispatch_j<1, true>(c, J, grid, smem, pdl, stream);
+    } else {
+      if (mt == 4) e = dispatch_j<4, false>(c, J, grid, smem, pdl, stream);
+      else if (mt == 2) e = dispatch_j<2, false>(c, J, grid, smem, pdl, stream);
+      else e = dispatch_j<1, false>(c, J, grid, smem, pdl, stream);
+    }
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_gemv(const ForwardArgs& a, int num_sms, cudaStream_t stream) {
+  return run(a, nullptr, false, nullptr, nullptr, false, false, num_sms, stream);
+}
+
+cudaError_t launch_gemv_fused(const ForwardArgs& a, const void* X, bool x_bf16, int8_t* xq_out, float* s_out,
+                              bool pdl, int num_sms, cudaStream_t stream) {
+  return run(a, X, x_bf16, xq_out, s_out, true, pdl, num_sms, stream);
 }
 
 }  // namespace bl

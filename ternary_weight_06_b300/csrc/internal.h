@@ -35,8 +35,17 @@ struct ForwardArgs {
   uint32_t* err;  // device error word
 };
 
-// Streaming GEMV for a few tokens (any M: tokens are taken in groups of <= 4).
+// Streaming GEMV for a few tokens (tokens are taken in groups of <= 4; K <= 65536).
 cudaError_t launch_gemv(const ForwardArgs& a, int num_sms, cudaStream_t stream);
+
+// The same GEMV with the per-token activation quantisation fused in: reads X
+// (bf16 or fp32) instead of x_q / s; the first CTA writes x_q and s out.
+// With pdl, launched as a programmatic dependent of the preceding kernel.
+cudaError_t launch_gemv_fused(const ForwardArgs& a, const void* X, bool x_bf16, int8_t* xq_out, float* s_out,
+                              bool pdl, int num_sms, cudaStream_t stream);
+
+constexpr int64_t kGemvMaxTokens = 4;
+constexpr int64_t kGemvMaxK = 65536;
 
 // Tensor-core GEMM (tcgen05) for more tokens than the GEMV handles well.
 cudaError_t launch_gemm_tc(const ForwardArgs& a, int num_sms, cudaStream_t stream);

@@ -33,7 +33,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ("bitlinear_pack_weights", "bitlinear_quant_act", "bitlinear_forward",
-                     "bitlinear_check_device_error", "bitlinear_status_string", "bitlinear_pack_workspace_bytes"):
+                     "bitlinear_quant_forward", "bitlinear_check_device_error", "bitlinear_status_string",
+                     "bitlinear_pack_workspace_bytes"):
         assert required in names
 
 
@@ -124,6 +125,24 @@ def test_forward_validation(bl):
     assert fwd(bl, g=GOOD + 1) == bl.BL_ERR_MISALIGNED
     assert fwd(bl, s=GOOD + 2) == bl.BL_ERR_MISALIGNED
     assert fwd(bl, acc=GOOD + 4) == bl.BL_ERR_MISALIGNED
+
+
+def qfwd(bl, Wp=GOOD, g=GOOD, X=GOOD, dt=1, M=1, N=16, K=64, y=GOOD, xq=GOOD, s=GOOD, acc=None, flags=0):
+    return bl.get_lib().bitlinear_quant_forward(Wp, g, X, dt, M, N, K, y, xq, s, acc, flags, None)
+
+
+def test_quant_forward_validation(bl):
+    for kw in ("Wp", "g", "X", "y", "xq", "s"):
+        assert qfwd(bl, **{kw: None}) == bl.BL_ERR_INVALID_ARG, kw
+    assert qfwd(bl, M=0) == bl.BL_ERR_INVALID_ARG
+    assert qfwd(bl, dt=3) == bl.BL_ERR_INVALID_ARG
+    assert qfwd(bl, flags=2) == bl.BL_ERR_INVALID_ARG
+    assert qfwd(bl, K=96) == bl.BL_ERR_UNSUPPORTED_SHAPE
+    assert qfwd(bl, K=131072 + 64) == bl.BL_ERR_UNSUPPORTED_SHAPE
+    assert qfwd(bl, X=GOOD + 2) == bl.BL_ERR_MISALIGNED
+    assert qfwd(bl, xq=GOOD + 4) == bl.BL_ERR_MISALIGNED
+    assert qfwd(bl, s=GOOD + 1) == bl.BL_ERR_MISALIGNED
+    assert qfwd(bl, acc=GOOD + 8) == bl.BL_ERR_MISALIGNED
 
 
 def test_python_binding_rejects_cpu_tensors(bl):

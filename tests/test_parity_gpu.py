@@ -283,3 +283,72 @@ def test_forward_runs_on_a_side_stream(bl):
     side.synchronize()
     assert torch.equal(y, ref_y)
     bl.bitlinear_check_device_error(side)
+
+
+# ---------------------------------------------------------------- fused quant + forward
+
+def fused_case(bl, p_ref, g_ref, X, K, rows, where, flags=0):
+    """The one-call path against the oracle: x_q, s, acc bit-exact, y to the contract."""
+    xq_ref, s_ref = oracle.quant_act(X.to(torch.float32).numpy())
+    Wp = gpu(torch.from_numpy(p_ref))
+    gamma = gpu(torch.tensor([g_ref], dtype=torch.float32))
+    y, xq, s, acc = bl.bitlinear_quant_forward(Wp, gamma, gpu(X), acc=True, flags=flags)
+    torch.cuda.synchronize()
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), s_ref.view(np.uint32)), where
+    assert np.array_equal(xq.cpu().numpy(), xq_ref), where
+    y_ref, acc_ref = oracle.forward(p_ref, g_ref, xq_ref[rows], s_ref[rows], K)
+    bad = np.count_nonzero(acc.cpu().numpy()[rows] != acc_ref)
+    assert bad == 0, f"{where}: {bad} int32 accumulators differ"
+    assert_y_close(y.cpu().numpy()[rows], y_ref, where)
+    bl.bitlinear_check_device_error()
+
+
+@pytest.mark.parametrize("wl_name,idx", all_activation_layers())
+def test_quant_forward_full_size(bl, wl_name, idx):
+    wl = workloads.WORKLOADS[wl_name]
+    L = wl.layers[idx]
+    p_ref, g_ref = packed_layer(wl_name, idx)
+    X = workloads.layer_activations(wl, idx)
+    rows = sample_rows(L.M, row_budget(L.N, L.K), seed=idx)
+    fused_case(bl, p_ref, g_ref, X, L.K, rows, f"fused {wl_name}[{idx}]", flags=bl.BITLINEAR_WEIGHTS_RESIDENT)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 9])
+@pytest.mark.parametrize("N,K", [(7, 64), (300, 1024), (999, 6912), (64, 65536), (40, 65536 + 64)])
+def test_quant_forward_edge_shapes(bl, dtype, M, N, K):
+    rng = np.random.default_rng(M * 7 + N)
+    q = rng.integers(-1, 2, size=(N, K)).astype(np.int8)
+    g = torch.Generator().manual_seed(N + M)
+    X = torch.randn((M, K), generator=g)
+    X[0, :3] = torch.tensor([2.0, 1.0 / 127 * 2.5, -0.5])
+    if M > 2:
+        X[2] = 0  # an all-zero token
+    X = X.to(dtype)
+    fused_case(bl, oracle.pack(q), np.float32(0.031), X, K, sample_rows(M, 16, seed=M), f"fused M={M} N={N} K={K}")
+
+
+def test_quant_forward_chain_with_resident_weights(bl):
+    """Back-to-back calls with early weight streaming, where each layer's
+    output is the next layer's input: an activation read before the
+    preceding kernel finished would change the result."""
+    rng = np.random.default_rng(5)
+    dims = [1024, 2048, 1024, 3072, 1024]
+    packs, refs = [], []
+    for i in range(4):
+        q = rng.integers(-1, 2, size=(dims[i + 1], dims[i])).astype(np.int8)
+        refs.append(oracle.pack(q))
+        packs.append(gpu(torch.from_numpy(refs[-1])))
+    gamma = gpu(torch.tensor([0.02], dtype=torch.float32))
+    x0 = torch.randn((1, dims[0]), generator=torch.Generator().manual_seed(1))
+    torch.cuda.synchronize()
+    x = gpu(x0)
+    for i in range(4):
+        x, _, _ = bl.bitlinear_quant_forward(packs[i], gamma, x, flags=bl.BITLINEAR_WEIGHTS_RESIDENT)
+    torch.cuda.synchronize()
+    xr = x0.numpy()
+    for i in range(4):
+        xq, s = oracle.quant_act(xr)
+        xr, _ = oracle.forward(refs[i], np.float32(0.02), xq, s, dims[i])
+    assert_y_close(x.cpu().numpy(), xr, "resident chain")
+    bl.bitlinear_check_device_error()
