@@ -192,10 +192,6 @@ def metric_for(wl) -> tuple[str, str]:
     return "BitLinear GEMM int8 TOPS (tensor roofline)", "TOPS"
 
 
-def fused_available(bl) -> bool:
-    return hasattr(bl, "bitlinear_quant_forward")
-
-
 # ---------------------------------------------------------------- CPU oracle (baseline and reference arm)
 
 def run_oracle(wl, budget_s: float, steps: int | None = None, warmup: int = 0):
@@ -240,6 +236,12 @@ def run_oracle(wl, budget_s: float, steps: int | None = None, warmup: int = 0):
 
 # ---------------------------------------------------------------- GPU arm
 
+def gemv_fused_layer(L) -> bool:
+    """True where bitlinear_quant_forward runs the layer as ONE kernel (the
+    fused quantise + GEMV: at most 4 tokens and K <= 32768)."""
+    return L.M <= 4 and L.K <= 32768
+
+
 def run_gpu(args, dist, rank, world, local):
     import ternary_weight_06_b300 as bl
 
@@ -251,8 +253,7 @@ def run_gpu(args, dist, rank, world, local):
     stream = torch.cuda.Stream(device=dev)  # graphs cannot be captured on the legacy default stream
     torch.cuda.set_stream(stream)
     fused = args.path == "fused"
-    if fused and not fused_available(bl):
-        raise SystemExit("--path fused needs bitlinear_quant_forward")
+    nlayers = len(wl.layers)
 
     # ---- resident inputs: pack each layer's weights once (timed as the "pack" figure)
     packed, gammas, Xs, Xs_host, ys, xqs, ss = [], [], [], [], [], [], []
@@ -277,60 +278,67 @@ def run_gpu(args, dist, rank, world, local):
         ys.append(torch.empty((L.M, L.N), dtype=torch.float32, device=dev))
         xqs.append(torch.empty((L.M, L.K), dtype=torch.int8, device=dev))
         ss.append(torch.empty((L.M,), dtype=torch.float32, device=dev))
-    step_input_bytes = sum(p.numel() + x.numel() * x.element_size() for p, x in zip(packed, Xs))
-    R = min(256, max(1, math.ceil(2 * l2 / step_input_bytes) + 1))
-    Wrot = [[p] + [p.clone() for _ in range(R - 1)] for p in packed]
-    Xrot = [[x] + [x.clone() for _ in range(R - 1)] for x in Xs]
+    # every layer rotates over enough copies of its packed weights and
+    # activations that one pass over them is more than twice L2
+    Rs = []
+    for p, x in zip(packed, Xs):
+        nbytes = p.numel() + x.numel() * x.element_size()
+        Rs.append(min(512, max(2, math.ceil(2 * l2 / nbytes) + 1)))
+    Wrot = [[p] + [p.clone() for _ in range(R - 1)] for p, R in zip(packed, Rs)]
+    Xrot = [[x] + [x.clone() for _ in range(R - 1)] for x, R in zip(Xs, Rs)]
+    # quantised activations of every copy, for timing the forward kernel alone
+    XQrot = [[bl.bitlinear_quant_act(x) for x in xr] for xr in Xrot]
     torch.cuda.synchronize()
 
-    def step(i, events=None, X_override=None):
-        r = i % R
-        for l in range(len(wl.layers)):
-            X = Xrot[l][r] if X_override is None else X_override[l]
-            if fused:
-                if events is not None:
-                    events[l][0].record(stream)
-                bl.bitlinear_quant_forward(Wrot[l][r], gammas[l], X, y=ys[l], x_q=xqs[l], s=ss[l],
-                                           flags=bl.BITLINEAR_WEIGHTS_RESIDENT, stream=stream)
-            else:
-                bl.bitlinear_quant_act(X, x_q=xqs[l], s=ss[l], stream=stream)
-                if events is not None:
-                    events[l][0].record(stream)
-                bl.bitlinear_forward(Wrot[l][r], gammas[l], xqs[l], ss[l], y=ys[l], stream=stream)
-            if events is not None:
-                events[l][1].record(stream)
+    def layer_call(l, r, X=None):
+        if fused:
+            bl.bitlinear_quant_forward(Wrot[l][r], gammas[l], Xrot[l][r] if X is None else X, y=ys[l], x_q=xqs[l],
+                                       s=ss[l], flags=bl.BITLINEAR_WEIGHTS_RESIDENT, stream=stream)
+        else:
+            bl.bitlinear_quant_act(Xrot[l][r] if X is None else X, x_q=xqs[l], s=ss[l], stream=stream)
+            bl.bitlinear_forward(Wrot[l][r], gammas[l], xqs[l], ss[l], y=ys[l], stream=stream)
+
+    def step(i, X_override=None):
+        for l in range(nlayers):
+            layer_call(l, i % Rs[l], None if X_override is None else X_override[l])
+
+    def kernel_call(l, r):
+        """The layer's dominant kernel alone: the fused quantise+GEMV where the
+        layer runs as one kernel, else the forward product (GEMV or GEMM) on
+        activations quantised beforehand."""
+        L = wl.layers[l]
+        if fused and gemv_fused_layer(L):
+            layer_call(l, r)
+        else:
+            xq, s = XQrot[l][r]
+            bl.bitlinear_forward(Wrot[l][r], gammas[l], xq, s, y=ys[l], stream=stream)
 
     K, Wm = args.steps, args.warmup
     for i in range(Wm):
         step(i)
     torch.cuda.synchronize()
     bl.bitlinear_check_device_error(stream)
-    launches = K * sum(1 if (fused and L.M <= 4) else 2 for L in wl.layers)
+    launches = K * sum(1 if (fused and gemv_fused_layer(L)) else 2 for L in wl.layers)
     peaks, peak_src = load_peaks()
 
     if args.eager:
-        return run_gpu_eager(args, bl, wl, step, K, stream, dist, world, unit, metric, R, launches)
+        return run_gpu_eager(args, bl, wl, step, K, stream, dist, world, unit, metric, Rs, launches)
 
-    # ---- capture: chunks of GRAPH_CHUNK steps; the last full chunk carries
-    # external timing events around every forward launch
+    # ---- capture: chunks of GRAPH_CHUNK steps
     chunk = min(GRAPH_CHUNK, K)
     nfull, rem = divmod(K, chunk)
-    nlayers = len(wl.layers)
-    ev = [[[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)] for _ in range(nlayers)]
-          for _ in range(chunk)]
 
-    def capture(n, with_events):
+    def capture(fn, n):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for j in range(n):
-                step(j, events=ev[j] if with_events else None)
+                fn(j)
         return g
 
-    g_plain = capture(chunk, False)
-    g_timed = capture(chunk, True)
-    g_rem = capture(rem, False) if rem else None
+    g_full = capture(step, chunk)
+    g_rem = capture(step, rem) if rem else None
     for _ in range(2):
-        g_plain.replay()
+        g_full.replay()
     torch.cuda.synchronize()
 
     # ---- timed region
@@ -340,8 +348,8 @@ def run_gpu(args, dist, rank, world, local):
         barrier(dist)
         torch.cuda.synchronize()
         t0e.record(stream)
-        for c in range(nfull):
-            (g_timed if c == nfull - 1 else g_plain).replay()
+        for _ in range(nfull):
+            g_full.replay()
         if g_rem is not None:
             g_rem.replay()
         t1e.record(stream)
@@ -350,7 +358,6 @@ def run_gpu(args, dist, rank, world, local):
     clocks = sampler.summary()
     ms_per_step = max_over_ranks(dist, t0e.elapsed_time(t1e)) / K
     bl.bitlinear_check_device_error(stream)
-    fwd_ms = [sum(ev[j][l][0].elapsed_time(ev[j][l][1]) for j in range(chunk)) / chunk for l in range(nlayers)]
 
     # ---- the graph-replayed outputs must equal an eager re-run of the last step
     last = [y.clone() for y in ys]
@@ -363,37 +370,60 @@ def run_gpu(args, dist, rank, world, local):
     value = world * (step_bytes / (ms_per_step * 1e-3) / 1e9 if unit == "GB/s"
                      else step_ops / (ms_per_step * 1e-3) / 1e12)
 
-    # ---- dominant kernel roofline (the forward kernel: GEMV or tcgen05 GEMM)
-    fwd_total_ms = sum(fwd_ms)
-    kname = "gemv_kernel" if max(L.M for L in wl.layers) <= 4 else "gemm_tc_kernel"
-    if unit == "GB/s":
-        achieved = sum(forward_kernel_bytes(L, fused) for L in wl.layers) / (fwd_total_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "peak_source": f"{peak_src} hbm_gbs (copy)"}
+    # ---- dominant kernel: each layer's forward kernel timed alone, back to back
+    # from a CUDA graph on the launching stream (CUDA events around the replay)
+    kchunk = 200
+    kern_us = []
+    for l in range(nlayers):
+        g = capture(lambda j, l=l: kernel_call(l, j % Rs[l]), kchunk)
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(3):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        kern_us.append(a.elapsed_time(b) * 1e3 / (3 * kchunk))
+        del g
+    kernel_names = ["gemv_kernel" if (L.M <= 4 and L.K <= 32768) else "gemm_tc_kernel" for L in wl.layers]
+    kname = max(set(kernel_names), key=lambda k: sum(t for t, n in zip(kern_us, kernel_names) if n == k))
+    sel = [i for i, n in enumerate(kernel_names) if n == kname]
+    tot_s = sum(kern_us[i] for i in sel) * 1e-6
+    if kname == "gemv_kernel":
+        kbytes = sum(forward_kernel_bytes(wl.layers[i], fused) for i in sel)
+        roof = {"bound": "hbm", "achieved": round(kbytes / tot_s / 1e9, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "peak_source": f"{peak_src} hbm_gbs (copy)",
+                "algorithmic_bytes_per_launch": [forward_kernel_bytes(wl.layers[i], fused) for i in sel]}
     else:
-        achieved = step_ops / (fwd_total_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "peak_source": f"{peak_src} bf16_tflops burst (kind::f16 runs at the bf16 rate)"}
+        kops = sum(layer_ops(wl.layers[i]) for i in sel)
+        roof = {"bound": "tensor", "achieved": round(kops / tot_s / 1e12, 1), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "peak_source": f"{peak_src} bf16_tflops burst (kind::f16 runs at the bf16 rate)",
+                "algorithmic_ops_per_launch": [layer_ops(wl.layers[i]) for i in sel]}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
     roof["traffic"] = ncu_traffic(kname, args.workload)
     roof["kernel"] = kname
-    roof["kernel_us"] = [round(x * 1e3, 3) for x in fwd_ms]
+    roof["kernel_us"] = [round(kern_us[i], 3) for i in sel]
+    roof["how"] = (f"each layer's kernel replayed {3 * kchunk} times back to back from a CUDA graph over its rotating "
+                   "buffers; CUDA events on the launching stream")
     if fused and kname == "gemv_kernel":
-        roof["note"] = "the timed kernel also quantises the activations (fused)"
+        roof["note"] = "the timed kernel also quantises the activations (fused); consecutive launches overlap (PDL)"
 
-    e2e = run_e2e(bl, wl, step, Xs_host, ys, R, K, Wm, stream, dist, world, unit, step_bytes, step_ops)
+    e2e = run_e2e(bl, wl, step, Xs_host, ys, K, Wm, stream, dist, world, unit, step_bytes, step_ops)
 
     return {
         "metric": metric, "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": K, "warmup": Wm,
         "ms_per_step": round(ms_per_step, 6), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "int8 x ternary -> int32 (fp32 rescale)", "data": "synthetic",
+        "dtype": "int8", "data": "synthetic",
         "config": {"workload": args.workload,
                    "layers": [f"M={L.M} K={L.K} N={L.N} X={L.x_dtype}" for L in wl.layers],
-                   "l2": f"inputs rotate over {R} copies ({R * step_input_bytes / 2**20:.0f} MiB > 2x L2 "
-                         f"{l2 / 2**20:.0f} MiB)",
+                   "l2": "inputs rotate per layer over " + ", ".join(
+                       f"{R} copies ({R * (p.numel() + x.numel() * x.element_size()) / 2**20:.0f} MiB)"
+                       for R, p, x in zip(Rs, packed, Xs)) + f" > 2x L2 ({l2 / 2**20:.0f} MiB)",
                    "launch": f"CUDA graphs of the C-ABI calls, {chunk} steps per graph",
-                   "path": ("bitlinear_quant_forward (quant fused into the GEMV for M <= 4; weights resident, "
-                            "programmatic dependent launch)") if fused else "bitlinear_quant_act + bitlinear_forward",
+                   "path": ("bitlinear_quant_forward (one fused quantise+GEMV kernel for M <= 4; quantise + tcgen05 "
+                            "GEMM otherwise; weights resident, programmatic dependent launch)") if fused
+                   else "bitlinear_quant_act + bitlinear_forward",
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,
         "e2e": e2e,
@@ -405,7 +435,7 @@ def run_gpu(args, dist, rank, world, local):
     }
 
 
-def run_gpu_eager(args, bl, wl, step, K, stream, dist, world, unit, metric, R, launches):
+def run_gpu_eager(args, bl, wl, step, K, stream, dist, world, unit, metric, Rs, launches):
     """Timed region with eager launches (for profilers; includes launch gaps)."""
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist)
@@ -422,13 +452,13 @@ def run_gpu_eager(args, bl, wl, step, K, stream, dist, world, unit, metric, R, l
     value = world * (step_bytes / (ms * 1e-3) / 1e9 if unit == "GB/s" else step_ops / (ms * 1e-3) / 1e12)
     return {"metric": metric, "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "int8 x ternary -> int32 (fp32 rescale)", "data": "synthetic",
+            "vs_baseline": None, "dtype": "int8", "data": "synthetic",
             "config": {"workload": args.workload, "launch": "eager (profiling mode)", "path": args.path,
-                       "l2": f"inputs rotate over {R} copies"},
+                       "l2": f"inputs rotate per layer over {Rs} copies"},
             "gpu_launches": launches}
 
 
-def run_e2e(bl, wl, step, Xs_host, ys, R, K, Wm, stream, dist, world, unit, step_bytes, step_ops):
+def run_e2e(bl, wl, step, Xs_host, ys, K, Wm, stream, dist, world, unit, step_bytes, step_ops):
     """The same step through the public API with host buffers: each step copies
     X from pinned host memory, runs the layer calls, and copies y back to
     pinned host memory; replayed from CUDA graphs like the device-side number."""
@@ -488,10 +518,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="decode", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--path", default="separate", choices=["fused", "separate"],
+    ap.add_argument("--path", default="fused", choices=["fused", "separate"],
                     help="fused: bitlinear_quant_forward; separate: bitlinear_quant_act + bitlinear_forward")
     ap.add_argument("--eager", action="store_true",
                     help="launch every step eagerly instead of from CUDA graphs (for profilers)")
+    ap.add_argument("--layers", default="", help="comma-separated layer indices of the workload (default: all)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -499,6 +530,12 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.steps is None:
         args.steps = DEFAULT_STEPS[args.workload]
+    if args.layers:
+        wl0 = workloads.WORKLOADS[args.workload]
+        idx = [int(v) for v in args.layers.split(",")]
+        if any(i < 0 or i >= len(wl0.layers) for i in idx):
+            ap.error(f"--layers indexes 0..{len(wl0.layers) - 1}")
+        workloads.WORKLOADS[args.workload] = workloads.select_layers(wl0, idx)
 
     dist, rank, world, local = dist_setup()
     wl = workloads.WORKLOADS[args.workload]

@@ -181,7 +181,7 @@ bl_status bitlinear_forward(const uint8_t* W_packed, const float* gamma, const i
  * bitlinear_forward, as one call: per-token absmax int8 quantisation of X
  * (anthology note-168, "What it does": activations at 8 bits) and the
  * ternary x int8 product with the gamma/s rescale.  For M <= 4 (and K <=
- * 65536) both run in ONE kernel (each CTA quantises the few token rows it
+ * 32768) both run in ONE kernel (each CTA quantises the few token rows it
  * needs; the first CTA writes x_q and s out), which removes a launch and a
  * round trip per layer in decode; otherwise it is the two kernels in
  * sequence.  Results are bit-identical to the two separate calls.

@@ -8,29 +8,35 @@
 // note-168, "The part that is a bet rather than a measurement").
 //
 // Layout of the work:
-//   * one CTA per SM owns a contiguous block of ~N/#SM output rows; packed rows
-//     are contiguous, so the block is one byte range, streamed into a ring of
-//     shared-memory stages by 1-D bulk async copies issued from one producer
-//     thread (mbarrier completion, bounded waits).  A decode-sized block fits
-//     the ring whole, so all of it is requested at kernel entry;
+//   * up to two CTAs per SM; each owns a contiguous block of output rows.
+//     Packed rows are contiguous, so the block is one byte range, streamed
+//     into a ring of shared-memory stages by 1-D bulk async copies issued by
+//     one producer thread (mbarrier completion, bounded waits);
 //   * the copies are issued BEFORE the kernel waits on its predecessor
-//     (griddepcontrol.wait), and the kernel lets its own successor launch
-//     early (griddepcontrol.launch_dependents).  Under programmatic dependent
-//     launch a chain of layers therefore streams the next layer's weights
-//     while the previous layer finishes; two CTAs fit per SM for that;
+//     (griddepcontrol.wait), and the kernel lets its successor launch early
+//     (griddepcontrol.launch_dependents).  Under programmatic dependent launch
+//     a chain of layers streams the next layer's weights while the previous
+//     layer finishes; registers and shared memory leave room for a third CTA
+//     per SM for that;
 //   * consumer warps own a fixed K slice: lane l of k-warp kw handles the
 //     16-code words w = kw*Cw + l + 32 j (j < J, J fixed at compile time) of
 //     every row, with the matching activations held in registers;
-//   * unpacking a 32-bit word P of 16 codes takes two ops per 4 weights:
-//     S_i = (P >> 2i) & 0x03030303 holds the codes c of weights 4j+i (j=0..3)
-//     as bytes in {0,1,2}; the activation word X'_i holds x[4j+i] (a 4x4 byte
-//     transpose of the natural 16 activations, done once), so
-//       sum_k (c_k - 1) x_k = sum_i dp4a(S_i, X'_i) - sum_k x_k,
-//     an exact int32 sum ("only involves integer addition");
-//   * a warp handles four rows per iteration (independent dependency chains),
-//     reduces each over its lanes and adds it into a per-CTA shared
-//     accumulator; after the last stage the CTA writes y = fp32(acc) *
-//     fp32(gamma / s[m]) with coalesced stores.
+//   * a 32-bit word P holds 16 codes c in {0,1,2}.  P & (3 << 2i) keeps, in
+//     byte j, the code of weight 4j+i scaled by 4^i (at most 128, so it is a
+//     valid unsigned byte).  With the activation word X'_i holding x[4j+i]
+//     (a 4x4 byte transpose of the natural 16 activations, done once),
+//       A_i += dp4a.u32.s32(P & (3 << 2i), X'_i)
+//     accumulates 4^i * sum c x over plane i: one AND and one dp4a per four
+//     weights and token.  At the end of a row segment
+//       sum_k (c_k - 1) x_k = A_0 + A_1/4 + A_2/16 + A_3/64 - sum_k x_k,
+//     where each division is an exact arithmetic shift (A_i is a multiple of
+//     4^i).  Every step is an exact int32 sum ("only involves integer
+//     addition");
+//   * each warp reduces its RI x MT row-token sums across lanes with a
+//     butterfly that halves the value count per exchange (RI*MT - 1 + 5 -
+//     log2(RI*MT) shuffles instead of 5 per value), adds them into a per-CTA
+//     shared accumulator, and after the last stage the CTA writes
+//     y = fp32(acc) * fp32(gamma / s[m]) with coalesced stores.
 // The fused variant quantises X itself (per-token absmax; the same IEEE
 // operations as the stand-alone kernel, so x_q and s are bit-identical); the
 // first CTA also writes x_q and s out.
@@ -42,12 +48,18 @@
 namespace bl {
 namespace {
 
-constexpr int kStages = 3;
-constexpr int kStageBytesTarget = 32768;
+constexpr int kStages = 4;
+constexpr int kStageBytesTarget = 16384;
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
-constexpr int kRowsPerIter = 4;
+constexpr int kCtasPerSm = 2;  // CTAs of one launch per SM (a third slot stays free for the next launch)
 constexpr float kActClampEps = 1e-5f;
+
+// rows each warp takes per iteration, by tokens per launch
+template <int MT>
+struct RowsPerIter {
+  static constexpr int value = MT == 1 ? 2 : 1;
+};
 
 struct GemvCfg {
   const uint8_t* Wp;
@@ -74,6 +86,65 @@ __device__ __forceinline__ void transpose4x4(uint32_t x0, uint32_t x1, uint32_t 
   o[1] = __byte_perm(t0, t1, 0x7632);
   o[2] = __byte_perm(t2, t3, 0x5410);
   o[3] = __byte_perm(t2, t3, 0x7632);
+}
+
+// 4-way dot product of unsigned bytes a with signed bytes b, plus c.
+__device__ __forceinline__ int32_t dp4a_us(uint32_t a, uint32_t b, int32_t c) {
+  int32_t d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Sum of V values (index v) over the 32 lanes of a warp.  Each exchange step
+// s sends half of the remaining values to the partner lane (lane ^ (16 >> s))
+// and keeps the other half, so after log2(V) steps each lane holds one partial
+// sum; plain xor-steps finish the reduction.  Lane l returns the total of
+// value index reduce_index<V>(l).
+template <int V>
+struct Log2 {
+  static constexpr int value = V <= 1 ? 0 : 1 + Log2<V / 2>::value;
+};
+template <>
+struct Log2<1> {
+  static constexpr int value = 0;
+};
+
+template <int V>
+__device__ __forceinline__ int32_t butterfly_sum(int32_t (&v)[V], int lane) {
+  constexpr int kSteps = Log2<V>::value;
+#pragma unroll
+  for (int s = 0; s < kSteps; ++s) {
+    const int half = V >> (s + 1);
+    const int o = 16 >> s;
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int k = 0; k < half; ++k) {
+      const int32_t send = upper ? v[k] : v[k + half];
+      const int32_t keep = upper ? v[k + half] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  int32_t r = v[0];
+#pragma unroll
+  for (int o = 16 >> kSteps; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+  return r;
+}
+
+template <int V>
+__device__ __forceinline__ int reduce_index(int lane) {
+  constexpr int kSteps = Log2<V>::value;
+  int idx = 0;
+#pragma unroll
+  for (int s = 0; s < kSteps; ++s)
+    if (lane & (16 >> s)) idx += V >> (s + 1);
+  return idx;
+}
+
+// Lanes that write a reduced value: one per value index.
+template <int V>
+__device__ __forceinline__ bool reduce_writer(int lane) {
+  constexpr int kSteps = Log2<V>::value;
+  return (lane & ((32 >> kSteps) - 1)) == 0;
 }
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t code,
@@ -122,7 +193,9 @@ __device__ __forceinline__ void quant16(const void* xrow, int x_bf16, int64_t k0
 }
 
 template <int MT, int J, bool FUSED>
-__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvCfg c) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm + 1) gemv_kernel(const GemvCfg c) {
+  constexpr int RI = RowsPerIter<MT>::value;
+  constexpr int V = RI * MT;
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int SR = c.rows_per_stage;
@@ -274,53 +347,50 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvCfg c) {
     }
   }
 
+  const bool writer = reduce_writer<V>(lane);
+  const int widx = reduce_index<V>(lane);
+  const int w_rr = widx / MT, w_t = widx % MT;
+
   for (int st = 0; st < nstages; ++st) {
     const int slot = st % NS;
     const int rows = min(SR, nrows - st * SR);
     const bool ok = wait_or_abort(&full[slot], (uint32_t)(st / NS) & 1u, c.err, kErrGemvFullWait, abort_flag);
     if (ok) {
       const uint8_t* base = smem + slot * stage_bytes;
-      for (int r0 = rg * kRowsPerIter; r0 < rows; r0 += nrg * kRowsPerIter) {
-        int32_t a[kRowsPerIter][MT];
+      for (int r0 = rg * RI; r0 < rows; r0 += nrg * RI) {
+        int32_t a[RI][MT][4];
 #pragma unroll
-        for (int rr = 0; rr < kRowsPerIter; ++rr)
+        for (int rr = 0; rr < RI; ++rr)
 #pragma unroll
-          for (int t = 0; t < MT; ++t) a[rr][t] = 0;
+          for (int t = 0; t < MT; ++t)
 #pragma unroll
-        for (int rr = 0; rr < kRowsPerIter; ++rr) {
-          if (r0 + rr < rows) {
-            const uint32_t* rowp = reinterpret_cast<const uint32_t*>(base + (r0 + rr) * c.row_bytes);
+            for (int i = 0; i < 4; ++i) a[rr][t][i] = 0;
 #pragma unroll
-            for (int j = 0; j < J; ++j) {
-              const int w = wbeg + lane + 32 * j;
-              if (w < wend) {
-                const uint32_t P = rowp[w];
+        for (int j = 0; j < J; ++j) {
+          const int w = wbeg + lane + 32 * j;
+          if (w < wend) {
+            uint32_t P[RI];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  const int S = (int)((P >> (2 * i)) & 0x03030303u);
+            for (int rr = 0; rr < RI; ++rr)
+              P[rr] = (r0 + rr < rows) ? reinterpret_cast<const uint32_t*>(base + (r0 + rr) * c.row_bytes)[w] : 0u;
 #pragma unroll
-                  for (int t = 0; t < MT; ++t) a[rr][t] = __dp4a(S, (int)xr[j][i][t], a[rr][t]);
-                }
+            for (int rr = 0; rr < RI; ++rr)
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const uint32_t m = P[rr] & (0x03030303u << (2 * i));
+#pragma unroll
+                for (int t = 0; t < MT; ++t) a[rr][t][i] = dp4a_us(m, xr[j][i][t], a[rr][t][i]);
               }
-            }
           }
         }
+        int32_t v[V];
 #pragma unroll
-        for (int rr = 0; rr < kRowsPerIter; ++rr)
+        for (int rr = 0; rr < RI; ++rr)
 #pragma unroll
-          for (int t = 0; t < MT; ++t) {
-            int32_t v = a[rr][t] - xsum[t];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-            a[rr][t] = v;
-          }
-        if (lane == 0) {
-#pragma unroll
-          for (int rr = 0; rr < kRowsPerIter; ++rr)
-            if (r0 + rr < rows)
-#pragma unroll
-              for (int t = 0; t < MT; ++t) atomicAdd(&acc_sm[(st * SR + r0 + rr) * MT + t], a[rr][t]);
-        }
+          for (int t = 0; t < MT; ++t)
+            v[rr * MT + t] = a[rr][t][0] + (a[rr][t][1] >> 2) + (a[rr][t][2] >> 4) + (a[rr][t][3] >> 6) - xsum[t];
+        const int32_t tot = butterfly_sum<V>(v, lane);
+        if (writer && r0 + w_rr < rows) atomicAdd(&acc_sm[(st * SR + r0 + w_rr) * MT + w_t], tot);
       }
     }
     __syncwarp();
@@ -356,10 +426,9 @@ cudaError_t launch_one(const GemvCfg& c, int grid, size_t smem, bool pdl, cudaSt
   return cudaLaunchKernelEx(&cfg, kern, c);
 }
 
-// Activation registers per lane are J*4*MT.  The preferred limit keeps every
-// variant free of register spills; the hard limit only serves K > 48K.
-constexpr int jmax_for(int mt) { return mt == 1 ? 16 : mt == 2 ? 8 : 4; }
-constexpr int jpref_for(int mt) { return mt == 1 ? 12 : mt == 2 ? 6 : 3; }
+// Activation registers per lane are J*4*MT.  The limits keep every variant
+// within the register budget of three resident CTAs per SM.
+constexpr int jmax_for(int mt) { return mt == 1 ? 8 : mt == 2 ? 4 : 2; }
 
 // The smallest instantiated J >= the J a launch needs.
 template <int MT, bool FUSED>
@@ -367,11 +436,16 @@ cudaError_t dispatch_j(const GemvCfg& c, int J, int grid, size_t smem, bool pdl,
   switch (J) {
     case 1: return launch_one<MT, 1, FUSED>(c, grid, smem, pdl, stream);
     case 2: return launch_one<MT, 2, FUSED>(c, grid, smem, pdl, stream);
-    case 3: return launch_one<MT, 3, FUSED>(c, grid, smem, pdl, stream);
-    case 4: return launch_one<MT, 4, FUSED>(c, grid, smem, pdl, stream);
     default: break;
   }
   if constexpr (MT <= 2) {
+    switch (J) {
+      case 3: return launch_one<MT, 3, FUSED>(c, grid, smem, pdl, stream);
+      case 4: return launch_one<MT, 4, FUSED>(c, grid, smem, pdl, stream);
+      default: break;
+    }
+  }
+  if constexpr (MT == 1) {
     switch (J) {
       case 5: return launch_one<MT, 5, FUSED>(c, grid, smem, pdl, stream);
       case 6: return launch_one<MT, 6, FUSED>(c, grid, smem, pdl, stream);
@@ -379,12 +453,6 @@ cudaError_t dispatch_j(const GemvCfg& c, int J, int grid, size_t smem, bool pdl,
       case 8: return launch_one<MT, 8, FUSED>(c, grid, smem, pdl, stream);
       default: break;
     }
-  }
-  if constexpr (MT == 1) {
-    if (J <= 10) return launch_one<MT, 10, FUSED>(c, grid, smem, pdl, stream);
-    if (J <= 12) return launch_one<MT, 12, FUSED>(c, grid, smem, pdl, stream);
-    if (J <= 14) return launch_one<MT, 14, FUSED>(c, grid, smem, pdl, stream);
-    if (J <= 16) return launch_one<MT, 16, FUSED>(c, grid, smem, pdl, stream);
   }
   return cudaErrorInvalidValue;
 }
@@ -408,7 +476,8 @@ cudaError_t run(const ForwardArgs& a, const void* X, bool x_bf16, int8_t* xq_out
   c.row_bytes = (int)(a.K / 4);
   c.words_per_row = (int)(a.K / 16);
 
-  int grid = (int)(a.N < num_sms ? a.N : num_sms);
+  const int64_t max_grid = (int64_t)num_sms * kCtasPerSm;
+  int grid = (int)(a.N < max_grid ? a.N : max_grid);
   c.rows_per_cta = (int)((a.N + grid - 1) / grid);
   grid = (int)((a.N + c.rows_per_cta - 1) / c.rows_per_cta);
   int sr = kStageBytesTarget / c.row_bytes;
@@ -422,7 +491,7 @@ cudaError_t run(const ForwardArgs& a, const void* X, bool x_bf16, int8_t* xq_out
   int mt = a.M >= 4 ? 4 : a.M >= 2 ? 2 : 1;
   while (mt > 1 && (c.words_per_row + 32 * kConsumerWarps - 1) / (32 * kConsumerWarps) > jmax_for(mt)) mt /= 2;
   int kw = 1;
-  while (kw < kConsumerWarps && (c.words_per_row + 32 * kw - 1) / (32 * kw) > jpref_for(mt)) kw *= 2;
+  while (kw < kConsumerWarps && (c.words_per_row + 32 * kw - 1) / (32 * kw) > jmax_for(mt)) kw *= 2;
   c.kw = kw;
   c.words_per_warp = (c.words_per_row + c.kw - 1) / c.kw;
   const int J = (c.words_per_warp + 31) / 32;

@@ -35,7 +35,7 @@ struct ForwardArgs {
   uint32_t* err;  // device error word
 };
 
-// Streaming GEMV for a few tokens (tokens are taken in groups of <= 4; K <= 65536).
+// Streaming GEMV for a few tokens (tokens are taken in groups of <= 4; K <= 32768).
 cudaError_t launch_gemv(const ForwardArgs& a, int num_sms, cudaStream_t stream);
 
 // The same GEMV with the per-token activation quantisation fused in: reads X
@@ -45,7 +45,7 @@ cudaError_t launch_gemv_fused(const ForwardArgs& a, const void* X, bool x_bf16, 
                               bool pdl, int num_sms, cudaStream_t stream);
 
 constexpr int64_t kGemvMaxTokens = 4;
-constexpr int64_t kGemvMaxK = 65536;
+constexpr int64_t kGemvMaxK = 32768;
 
 // Tensor-core GEMM (tcgen05) for more tokens than the GEMV handles well.
 cudaError_t launch_gemm_tc(const ForwardArgs& a, int num_sms, cudaStream_t stream);

@@ -315,7 +315,7 @@ def test_quant_forward_full_size(bl, wl_name, idx):
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 9])
-@pytest.mark.parametrize("N,K", [(7, 64), (300, 1024), (999, 6912), (64, 65536), (40, 65536 + 64)])
+@pytest.mark.parametrize("N,K", [(7, 64), (300, 1024), (999, 6912), (64, 32768), (40, 32768 + 64), (16, 65536)])
 def test_quant_forward_edge_shapes(bl, dtype, M, N, K):
     rng = np.random.default_rng(M * 7 + N)
     q = rng.integers(-1, 2, size=(N, K)).astype(np.int8)

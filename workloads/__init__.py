@@ -50,6 +50,7 @@ class Workload:
     seed: int
     layers: tuple
     eps: float = 1e-5
+    source_index: tuple = ()  # layer indices in the full workload (set by select_layers)
 
 
 WORKLOADS = {
@@ -71,6 +72,17 @@ WORKLOADS = {
         tuple(Layer(m, k, n, 0.01, "bf16") for m in (1, 16, 176) for (k, n) in ((8192, 28672), (28672, 8192))),
     ),
 }
+
+
+def select_layers(wl: Workload, indices) -> Workload:
+    """The workload restricted to some of its layers, each keeping the seeds it
+    has in the full workload (so its inputs are unchanged)."""
+    return Workload(wl.name, wl.seed, tuple(wl.layers[i] for i in indices), wl.eps,
+                    tuple(_layer_index(wl, i) for i in indices))
+
+
+def _layer_index(wl: Workload, i: int) -> int:
+    return wl.source_index[i] if wl.source_index else i
 
 
 def _gen(seed: int) -> torch.Generator:
@@ -104,8 +116,9 @@ def activations(M: int, K: int, dtype: str, seed: int, outlier_frac: float = 0.0
 def weight_seed(wl: Workload, index: int) -> int:
     """Layers of a workload that differ only in M are one weight matrix seen at
     several batch sizes: the weight seed depends on the (K, N) shape only."""
+    full = WORKLOADS[wl.name]
     shapes = []
-    for L in wl.layers:
+    for L in full.layers:
         if (L.K, L.N) not in shapes:
             shapes.append((L.K, L.N))
     L = wl.layers[index]
@@ -113,7 +126,7 @@ def weight_seed(wl: Workload, index: int) -> int:
 
 
 def activation_seed(wl: Workload, index: int) -> int:
-    return 1000 * wl.seed + 500 + index
+    return 1000 * wl.seed + 500 + _layer_index(wl, index)
 
 
 def layer_weights(wl: Workload, index: int) -> torch.Tensor:
