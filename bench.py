@@ -286,14 +286,15 @@ def run_gpu(args, dist, rank, world, local):
         Rs.append(min(512, max(2, math.ceil(2 * l2 / nbytes) + 1)))
     Wrot = [[p] + [p.clone() for _ in range(R - 1)] for p, R in zip(packed, Rs)]
     Xrot = [[x] + [x.clone() for _ in range(R - 1)] for x, R in zip(Xs, Rs)]
-    # quantised activations of every copy, for timing the forward kernel alone
-    XQrot = [[bl.bitlinear_quant_act(x) for x in xr] for xr in Xrot]
+    # quantised activations of every copy, made on first use, for timing the
+    # forward kernel alone on layers whose step runs quantise + forward
+    XQrot = [None] * nlayers
     torch.cuda.synchronize()
 
     def layer_call(l, r, X=None):
         if fused:
             bl.bitlinear_quant_forward(Wrot[l][r], gammas[l], Xrot[l][r] if X is None else X, y=ys[l], x_q=xqs[l],
-                                       s=ss[l], flags=bl.BITLINEAR_WEIGHTS_RESIDENT, stream=stream)
+                                       s=ss[l], stream=stream)
         else:
             bl.bitlinear_quant_act(Xrot[l][r] if X is None else X, x_q=xqs[l], s=ss[l], stream=stream)
             bl.bitlinear_forward(Wrot[l][r], gammas[l], xqs[l], ss[l], y=ys[l], stream=stream)
@@ -312,6 +313,12 @@ def run_gpu(args, dist, rank, world, local):
         else:
             xq, s = XQrot[l][r]
             bl.bitlinear_forward(Wrot[l][r], gammas[l], xq, s, y=ys[l], stream=stream)
+
+    def prepare_kernel_inputs(l):
+        L = wl.layers[l]
+        if not (fused and gemv_fused_layer(L)) and XQrot[l] is None:
+            XQrot[l] = [bl.bitlinear_quant_act(x, stream=stream) for x in Xrot[l]]
+            torch.cuda.synchronize()
 
     K, Wm = args.steps, args.warmup
     for i in range(Wm):
@@ -375,6 +382,7 @@ def run_gpu(args, dist, rank, world, local):
     kchunk = 200
     kern_us = []
     for l in range(nlayers):
+        prepare_kernel_inputs(l)
         g = capture(lambda j, l=l: kernel_call(l, j % Rs[l]), kchunk)
         g.replay()
         torch.cuda.synchronize()
@@ -401,13 +409,13 @@ def run_gpu(args, dist, rank, world, local):
                 "unit": "TFLOP/s", "peak_source": f"{peak_src} bf16_tflops burst (kind::f16 runs at the bf16 rate)",
                 "algorithmic_ops_per_launch": [layer_ops(wl.layers[i]) for i in sel]}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    roof["traffic"] = ncu_traffic(kname, args.workload)
+    roof["traffic"] = ncu_traffic(kname, args.workload) if not args.layers else None
     roof["kernel"] = kname
     roof["kernel_us"] = [round(kern_us[i], 3) for i in sel]
     roof["how"] = (f"each layer's kernel replayed {3 * kchunk} times back to back from a CUDA graph over its rotating "
                    "buffers; CUDA events on the launching stream")
     if fused and kname == "gemv_kernel":
-        roof["note"] = "the timed kernel also quantises the activations (fused); consecutive launches overlap (PDL)"
+        roof["note"] = "the timed kernel also quantises the activations (fused)"
 
     e2e = run_e2e(bl, wl, step, Xs_host, ys, K, Wm, stream, dist, world, unit, step_bytes, step_ops)
 
@@ -422,7 +430,7 @@ def run_gpu(args, dist, rank, world, local):
                        for R, p, x in zip(Rs, packed, Xs)) + f" > 2x L2 ({l2 / 2**20:.0f} MiB)",
                    "launch": f"CUDA graphs of the C-ABI calls, {chunk} steps per graph",
                    "path": ("bitlinear_quant_forward (one fused quantise+GEMV kernel for M <= 4; quantise + tcgen05 "
-                            "GEMM otherwise; weights resident, programmatic dependent launch)") if fused
+                            "GEMM otherwise)") if fused
                    else "bitlinear_quant_act + bitlinear_forward",
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,

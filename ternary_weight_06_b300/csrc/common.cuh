@@ -57,6 +57,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
   return done != 0;
 }
 
+// As mbar_try_wait, but the thread may be suspended in hardware for up to
+// `hint_ns` while the phase is incomplete instead of returning at once, so a
+// polling loop built on it does not take issue slots from working warps.
+// It returns as soon as the phase completes.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar_addr, uint32_t parity, uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar_addr), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
+// Suspend-time hint of the polling loops below.
+constexpr uint32_t kWaitHintNs = 20000;
+
 // Waits for the phase with the given parity to complete.  Returns false (and
 // records `code` in the error word) if it does not complete within
 // kWaitLimitNs; the caller then abandons its work without touching the
@@ -66,7 +83,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(a, parity)) return true;
+    if (mbar_try_wait_sleep(a, parity, kWaitHintNs)) return true;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       atomicOr(err, code);
       return false;

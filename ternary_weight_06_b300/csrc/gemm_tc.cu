@@ -127,7 +127,7 @@ __device__ __forceinline__ bool wait_flag(uint64_t* bar, uint32_t parity, uint32
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(a, parity)) return true;
+    if (mbar_try_wait_sleep(a, parity, kWaitHintNs)) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       atomicOr(err, kErrGemmWait);
@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = (issued > kRawStages ? issued - kRawStages : 0); kb < issued; ++kb) {
           const uint32_t a = smem_u32(&raw_full[kb % kRawStages]), par = (uint32_t)(kb / kRawStages) & 1u;
           const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(a, par) && globaltimer_ns() - t0 < kWaitLimitNs) {
+          while (!mbar_try_wait_sleep(a, par, kWaitHintNs) && globaltimer_ns() - t0 < kWaitLimitNs) {
           }
         }
       }
@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // issuer always commits acc_full, so this completes (bounded in any case).
     const uint32_t a = smem_u32(acc_full);
     const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(a, 0u) && globaltimer_ns() - t0 < kWaitLimitNs) {
+    while (!mbar_try_wait_sleep(a, 0u, kWaitHintNs) && globaltimer_ns() - t0 < kWaitLimitNs) {
     }
     tc_fence_after();
     tmem_dealloc(tmem, tmem_cols);

@@ -153,7 +153,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, ui
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(a, parity)) return true;
+    if (mbar_try_wait_sleep(a, parity, kWaitHintNs)) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       atomicOr(err, code);
@@ -171,17 +171,29 @@ __device__ __forceinline__ uint32_t q8(float x, float s) {
   return (uint32_t)q & 0xffu;
 }
 
+// 16 bf16 activations (two 16-byte chunks), quantised, as 4 natural int8 words.
+__device__ __forceinline__ void quant16_bf16(uint4 a, uint4 b, float s, uint32_t* out) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    out[i] = q8(__uint_as_float(w[2 * i] << 16), s) | (q8(__uint_as_float(w[2 * i] & 0xffff0000u), s) << 8) |
+             (q8(__uint_as_float(w[2 * i + 1] << 16), s) << 16) |
+             (q8(__uint_as_float(w[2 * i + 1] & 0xffff0000u), s) << 24);
+}
+
+__device__ __forceinline__ uint32_t absmax_bits_bf16(uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m = max(m, max((w[i] << 16) & 0x7fff0000u, w[i] & 0x7fff0000u));
+  return m;
+}
+
 // 16 activations of a token row starting at element k0, quantised, as 4 natural int8 words.
 __device__ __forceinline__ void quant16(const void* xrow, int x_bf16, int64_t k0, float s, uint32_t* out) {
   if (x_bf16) {
     const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(xrow) + k0);
-    const uint4 a = __ldg(p), b = __ldg(p + 1);
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      out[i] = q8(__uint_as_float(w[2 * i] << 16), s) | (q8(__uint_as_float(w[2 * i] & 0xffff0000u), s) << 8) |
-               (q8(__uint_as_float(w[2 * i + 1] << 16), s) << 16) |
-               (q8(__uint_as_float(w[2 * i + 1] & 0xffff0000u), s) << 24);
+    quant16_bf16(__ldg(p), __ldg(p + 1), s, out);
   } else {
     const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(xrow) + k0);
 #pragma unroll
@@ -244,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm + 1) gemv_kernel(const Ge
         for (int st = (issued > NS ? issued - NS : 0); st < issued; ++st) {
           const uint32_t a = smem_u32(&full[st % NS]), par = (uint32_t)(st / NS) & 1u;
           const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(a, par) && globaltimer_ns() - t0 < kWaitLimitNs) {
+          while (!mbar_try_wait_sleep(a, par, kWaitHintNs) && globaltimer_ns() - t0 < kWaitLimitNs) {
           }
         }
       }
@@ -260,27 +272,61 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm + 1) gemv_kernel(const Ge
   const float gamma = __ldg(c.gamma);
 
   float s_tok[MT];
-  if (FUSED) {
-    // per-token absmax over the whole row; every consumer thread takes 16-element words
+  // One-pass fused prologue (one token, bf16, at most 4 words per lane): each
+  // lane loads only its own words of X, once; the row groups of the CTA cover
+  // the row, so the CTA-wide maximum of the lanes' maxima is max|x|; the lane
+  // then quantises from the registers it loaded.
+  constexpr bool kOnePassShape = FUSED && MT == 1 && J <= 4;
+  constexpr int kRawJ = kOnePassShape ? J : 1;
+  uint4 raw[kRawJ][2];
+  const bool onepass = kOnePassShape && c.x_bf16 && c.ntok == 1;
+  if (FUSED && onepass) {
+    const uint4* xrow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(c.X) + (int64_t)c.tok0 * c.K);
+    uint32_t m = 0;
+#pragma unroll
+    for (int j = 0; j < kRawJ; ++j) {
+      const int w = wbeg + lane + 32 * j;
+      if (w < wend) {
+        raw[j][0] = __ldg(xrow + 2 * w);
+        raw[j][1] = __ldg(xrow + 2 * w + 1);
+      } else {
+        raw[j][0] = raw[j][1] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kRawJ; ++j) m = max(m, max(absmax_bits_bf16(raw[j][0]), absmax_bits_bf16(raw[j][1])));
+    m = __reduce_max_sync(0xffffffffu, m);
+    if (lane == 0) amax_sm[warp] = m;
+    consumer_bar();
+    uint32_t mm = 0;
+#pragma unroll
+    for (int w8 = 0; w8 < kConsumerWarps; ++w8) mm = max(mm, amax_sm[w8]);
+    float a = __uint_as_float(mm);
+    if (a < kActClampEps) a = kActClampEps;
+    s_tok[0] = __fdiv_rn(127.0f, a);
+  } else if (FUSED) {
+    // per-token absmax over the whole row: the row is read in 16-byte chunks,
+    // kChunksInFlight per thread issued together so a batch costs one round trip
+    constexpr int kChunksInFlight = 8;
+    constexpr int kCT = 32 * kConsumerWarps;
 #pragma unroll
     for (int t = 0; t < MT; ++t) {
       uint32_t m = 0;
       if (t < c.ntok) {
-        const int64_t base = (int64_t)(c.tok0 + t) * c.K;
-        for (int w = threadIdx.x; w < c.words_per_row; w += 32 * kConsumerWarps) {
-          if (c.x_bf16) {
-            const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(c.X) + base + 16 * w);
-            const uint4 a = __ldg(p), b = __ldg(p + 1);
-            const uint32_t v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        const int64_t esz = c.x_bf16 ? 2 : 4;
+        const uint4* row = reinterpret_cast<const uint4*>(static_cast<const char*>(c.X) + (c.tok0 + t) * c.K * esz);
+        const int nchunks = (int)(c.K * esz / 16);
+        for (int q0 = threadIdx.x; q0 < nchunks; q0 += kCT * kChunksInFlight) {
+          uint4 v[kChunksInFlight];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) m = max(m, max((v[i] << 16) & 0x7fff0000u, v[i] & 0x7fff0000u));
-          } else {
-            const uint4* p = reinterpret_cast<const uint4*>(static_cast<const float*>(c.X) + base + 16 * w);
+          for (int u = 0; u < kChunksInFlight; ++u)
+            v[u] = q0 + u * kCT < nchunks ? __ldg(row + q0 + u * kCT) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const uint4 v = __ldg(p + i);
-              m = max(m, max(max(v.x & 0x7fffffffu, v.y & 0x7fffffffu), max(v.z & 0x7fffffffu, v.w & 0x7fffffffu)));
-            }
+          for (int u = 0; u < kChunksInFlight; ++u) {
+            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              m = c.x_bf16 ? max(m, max((w[i] << 16) & 0x7fff0000u, w[i] & 0x7fff0000u)) : max(m, w[i] & 0x7fffffffu);
           }
         }
       }
@@ -325,8 +371,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm + 1) gemv_kernel(const Ge
       if (valid && t < c.ntok) {
         const int64_t tok = c.tok0 + t;
         if (FUSED) {
-          const char* xrow = static_cast<const char*>(c.X) + tok * c.K * (c.x_bf16 ? 2 : 4);
-          quant16(xrow, c.x_bf16, 16 * (int64_t)w, s_tok[t], nat);
+          if (onepass) {
+            quant16_bf16(raw[kOnePassShape ? j : 0][0], raw[kOnePassShape ? j : 0][1], s_tok[t], nat);
+          } else {
+            const char* xrow = static_cast<const char*>(c.X) + tok * c.K * (c.x_bf16 ? 2 : 4);
+            quant16(xrow, c.x_bf16, 16 * (int64_t)w, s_tok[t], nat);
+          }
           if (blockIdx.x == 0 && rg == 0)
             reinterpret_cast<uint4*>(c.xq_out + tok * c.K)[w] = make_uint4(nat[0], nat[1], nat[2], nat[3]);
         } else {
@@ -492,6 +542,9 @@ cudaError_t run(const ForwardArgs& a, const void* X, bool x_bf16, int8_t* xq_out
   while (mt > 1 && (c.words_per_row + 32 * kConsumerWarps - 1) / (32 * kConsumerWarps) > jmax_for(mt)) mt /= 2;
   int kw = 1;
   while (kw < kConsumerWarps && (c.words_per_row + 32 * kw - 1) / (32 * kw) > jmax_for(mt)) kw *= 2;
+  // the one-pass fused prologue wants at most 4 words per lane
+  if (fused && x_bf16 && mt == 1)
+    while (kw < kConsumerWarps && (c.words_per_row + 32 * kw - 1) / (32 * kw) > 4) kw *= 2;
   c.kw = kw;
   c.words_per_warp = (c.words_per_row + c.kw - 1) / c.kw;
   const int J = (c.words_per_warp + 31) / 32;
