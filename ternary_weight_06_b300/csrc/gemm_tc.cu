@@ -41,7 +41,7 @@ namespace {
 constexpr int kBM = 128;         // features per tile (MMA M)
 constexpr int kBK = 64;          // k per stage
 constexpr int kRawStages = 4;
-constexpr int kOpStages = 2;
+constexpr int kOpStages = 3;
 constexpr int kConvWarps = 8;
 constexpr int kThreads = 32 * (2 + kConvWarps);
 constexpr int kWRawBytes = kBM * kBK / 4;     // 2048
@@ -174,10 +174,23 @@ __device__ __forceinline__ void convert_x16_f16(uint4 v, uint32_t* h /* 8 words 
   }
 }
 
-// Store 16-byte unit u (0..7) of row r of a 128-byte-swizzled K-major tile.
-__device__ __forceinline__ void st_sw128(uint8_t* tile, int r, int u, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  uint4* p = reinterpret_cast<uint4*>(tile + r * 128 + ((u ^ (r & 7)) << 4));
-  *p = make_uint4(a, b, c, d);
+// Shared-memory accesses by 32-bit shared-window address (ld/st.shared, not
+// generic loads through a converted pointer).
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
+  return v;
+}
+
+// Store 16-byte unit u (0..7) of row r of a 128-byte-swizzled K-major tile at shared address `tile`.
+__device__ __forceinline__ void st_sw128(uint32_t tile, int r, int u, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  const uint32_t addr = tile + (uint32_t)(r * 128 + ((u ^ (r & 7)) << 4));
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -282,14 +295,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = wait_flag(&op_empty[os], ((uint32_t)(kb / kOpStages) & 1u) ^ 1u, c.err, abort_flag) &&
            wait_flag(&raw_full[slot], (uint32_t)(kb / kRawStages) & 1u, c.err, abort_flag);
       if (!ok) break;
-      const uint8_t* wraw = raw_base + slot * (kWRawBytes + x_raw_bytes);
-      const uint8_t* xraw = wraw + kWRawBytes;
-      uint8_t* aop = op_base + os * (kAOpBytes + b_op_bytes);
-      uint8_t* bop = aop + kAOpBytes;
+      const uint32_t wraw = smem_u32(raw_base + slot * (kWRawBytes + x_raw_bytes));
+      const uint32_t xraw = wraw + kWRawBytes;
+      const uint32_t aop = smem_u32(op_base + os * (kAOpBytes + b_op_bytes));
+      const uint32_t bop = aop + kAOpBytes;
       // W: thread -> (row r, half h): 8 packed bytes = 32 codes = 4 swizzle units
       {
         const int r = ct >> 1, h = ct & 1;
-        const uint2 pw = *reinterpret_cast<const uint2*>(wraw + r * 16 + h * 8);
+        const uint2 pw = lds64(wraw + (uint32_t)(r * 16 + h * 8));
         uint32_t f[8];
         unpack_word_f16(pw.x, f);
         st_sw128(aop, r, 4 * h + 0, f[0], f[1], f[2], f[3]);
@@ -301,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // x: 16-byte chunk q of token row t -> swizzle units 2q, 2q+1
       for (int idx = ct; idx < BN * 4; idx += 32 * kConvWarps) {
         const int t = idx >> 2, q = idx & 3;
-        const uint4 v = *reinterpret_cast<const uint4*>(xraw + t * kBK + q * 16);
+        const uint4 v = lds128(xraw + (uint32_t)(t * kBK + q * 16));
         uint32_t f[8];
         convert_x16_f16(v, f);
         st_sw128(bop, t, 2 * q, f[0], f[1], f[2], f[3]);
@@ -314,15 +327,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&op_full[os]);
       }
     }
-    // ---- epilogue: warp w reads tensor-memory lanes 32*(w%4) .. +31 = features
-    if (warp < 6) {  // four warps cover the 128 lanes
+    // ---- epilogue: warp w reads tensor-memory lanes 32*(w%4) .. +31 = features;
+    // the two warps of a lane quarter take alternate 16-token column chunks
+    {
       const bool done = wait_flag(acc_full, 0u, c.err, abort_flag);
       tc_fence_after();
       if (done) {
         const int q = warp & 3;
         const int f = q * 32 + lane;
         const int n = n0 + f;
-        for (int j0 = 0; j0 < BN; j0 += 16) {
+        for (int j0 = ((warp - 2) >> 2) * 16; j0 < BN; j0 += 32) {
           uint32_t r[16];
           tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)j0, r);
           if (n < c.N) {
