@@ -291,13 +291,17 @@ def run_gpu(args, dist, rank, world, local):
     XQrot = [None] * nlayers
     torch.cuda.synchronize()
 
+    # one workspace serves every layer's call (the calls run in stream order)
+    ws_bytes = max(bl.bitlinear_forward_workspace_bytes(L.M, L.N, L.K) for L in wl.layers)
+    workspace = torch.empty((max(ws_bytes, 16),), dtype=torch.uint8, device=dev)
+
     def layer_call(l, r, X=None):
         if fused:
-            bl.bitlinear_quant_forward(Wrot[l][r], gammas[l], Xrot[l][r] if X is None else X, y=ys[l], x_q=xqs[l],
-                                       s=ss[l], stream=stream)
+            bl.bitlinear_quant_forward_ws(Wrot[l][r], gammas[l], Xrot[l][r] if X is None else X, y=ys[l],
+                                          x_q=xqs[l], s=ss[l], workspace=workspace, stream=stream)
         else:
             bl.bitlinear_quant_act(Xrot[l][r] if X is None else X, x_q=xqs[l], s=ss[l], stream=stream)
-            bl.bitlinear_forward(Wrot[l][r], gammas[l], xqs[l], ss[l], y=ys[l], stream=stream)
+            bl.bitlinear_forward_ws(Wrot[l][r], gammas[l], xqs[l], ss[l], y=ys[l], workspace=workspace, stream=stream)
 
     def step(i, X_override=None):
         for l in range(nlayers):
@@ -312,7 +316,7 @@ def run_gpu(args, dist, rank, world, local):
             layer_call(l, r)
         else:
             xq, s = XQrot[l][r]
-            bl.bitlinear_forward(Wrot[l][r], gammas[l], xq, s, y=ys[l], stream=stream)
+            bl.bitlinear_forward_ws(Wrot[l][r], gammas[l], xq, s, y=ys[l], workspace=workspace, stream=stream)
 
     def prepare_kernel_inputs(l):
         L = wl.layers[l]
@@ -325,7 +329,8 @@ def run_gpu(args, dist, rank, world, local):
         step(i)
     torch.cuda.synchronize()
     bl.bitlinear_check_device_error(stream)
-    launches = K * sum(1 if (fused and gemv_fused_layer(L)) else 2 for L in wl.layers)
+    # kernels per layer: fused GEMV 1; quantise + GEMV 2; quantise + fp16 expansion + GEMM 3
+    launches = K * sum((1 if fused else 2) if gemv_fused_layer(L) else 3 for L in wl.layers)
     peaks, peak_src = load_peaks()
 
     if args.eager:
@@ -394,7 +399,7 @@ def run_gpu(args, dist, rank, world, local):
         torch.cuda.synchronize()
         kern_us.append(a.elapsed_time(b) * 1e3 / (3 * kchunk))
         del g
-    kernel_names = ["gemv_kernel" if (L.M <= 4 and L.K <= 32768) else "gemm_tc_kernel" for L in wl.layers]
+    kernel_names = ["gemv_kernel" if (L.M <= 4 and L.K <= 32768) else "gemm_tc_x16_kernel" for L in wl.layers]
     kname = max(set(kernel_names), key=lambda k: sum(t for t, n in zip(kern_us, kernel_names) if n == k))
     sel = [i for i, n in enumerate(kernel_names) if n == kname]
     tot_s = sum(kern_us[i] for i in sel) * 1e-6
@@ -414,6 +419,9 @@ def run_gpu(args, dist, rank, world, local):
     roof["kernel_us"] = [round(kern_us[i], 3) for i in sel]
     roof["how"] = (f"each layer's kernel replayed {3 * kchunk} times back to back from a CUDA graph over its rotating "
                    "buffers; CUDA events on the launching stream")
+    if kname == "gemm_tc_x16_kernel":
+        roof["note"] = ("time of the bitlinear_forward_ws call: the fp16 expansion of x_q (x16_prepass_kernel) "
+                        "plus the GEMM")
     if fused and kname == "gemv_kernel":
         roof["note"] = "the timed kernel also quantises the activations (fused)"
 
@@ -429,9 +437,9 @@ def run_gpu(args, dist, rank, world, local):
                        f"{R} copies ({R * (p.numel() + x.numel() * x.element_size()) / 2**20:.0f} MiB)"
                        for R, p, x in zip(Rs, packed, Xs)) + f" > 2x L2 ({l2 / 2**20:.0f} MiB)",
                    "launch": f"CUDA graphs of the C-ABI calls, {chunk} steps per graph",
-                   "path": ("bitlinear_quant_forward (one fused quantise+GEMV kernel for M <= 4; quantise + tcgen05 "
-                            "GEMM otherwise)") if fused
-                   else "bitlinear_quant_act + bitlinear_forward",
+                   "path": ("bitlinear_quant_forward_ws (one fused quantise+GEMV kernel for M <= 4; quantise, fp16 "
+                            "expansion of x_q and tcgen05 GEMM otherwise)") if fused
+                   else "bitlinear_quant_act + bitlinear_forward_ws",
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,
         "e2e": e2e,

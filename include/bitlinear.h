@@ -200,6 +200,47 @@ bl_status bitlinear_quant_forward(const uint8_t* W_packed, const float* gamma, c
                                   unsigned flags, cudaStream_t stream);
 
 /*
+ * bitlinear_forward_workspace_bytes -- device workspace, in bytes, that
+ * bitlinear_forward_ws and bitlinear_quant_forward_ws need for an M x K -> N
+ * problem: 0 where the streaming GEMV serves it (M <= 4 and K <= 32768),
+ * otherwise 2*M*K (the activations expanded once to fp16).
+ */
+size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * bitlinear_forward_ws -- bitlinear_forward with a caller-owned workspace
+ * (same product, identical y and acc bit for bit).  For the tensor-core path
+ * the int8 activations are expanded to fp16 once per call into the workspace
+ * (in the order the MMA consumes them) instead of once per 128-feature tile
+ * inside the GEMM, which removes most of the GEMM's operand-conversion work
+ * for many tokens.  The product is that of bitlinear_forward (anthology
+ * note-168, "The part that is a bet rather than a measurement"; yousumm.com
+ * transcript: unpacked next to the math engine).
+ *
+ *   arguments as bitlinear_forward, plus
+ *   workspace        tmp  >= bitlinear_forward_workspace_bytes(M, N, K)
+ *                         bytes, 16-byte aligned (may be NULL when that is
+ *                         0); clobbered; reusable once the call's work on
+ *                         `stream` is done
+ *   workspace_bytes  in   its size
+ *
+ * Errors as bitlinear_forward, plus BL_ERR_WORKSPACE if the workspace is
+ * missing or too small and BL_ERR_MISALIGNED if it is not 16-byte aligned.
+ */
+bl_status bitlinear_forward_ws(const uint8_t* W_packed, const float* gamma, const int8_t* x_q, const float* s,
+                               int64_t M, int64_t N, int64_t K, float* y, int32_t* acc, void* workspace,
+                               size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * bitlinear_quant_forward_ws -- bitlinear_quant_forward with the workspace of
+ * bitlinear_forward_ws (used for more than 4 tokens or K > 32768; the fused
+ * GEMV path needs none).  Outputs are bit-identical to bitlinear_quant_forward.
+ */
+bl_status bitlinear_quant_forward_ws(const uint8_t* W_packed, const float* gamma, const void* X, bl_dtype dtype,
+                                     int64_t M, int64_t N, int64_t K, float* y, int8_t* x_q, float* s, int32_t* acc,
+                                     unsigned flags, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * bitlinear_check_device_error -- waits for `stream`, then reports and clears
  * the library's device error word: BL_ERR_TIMEOUT if a kernel gave up on a
  * bounded wait since the last check, BL_ERR_CUDA if the stream itself failed,

@@ -12,6 +12,8 @@ Functions carry the C names:
 * :func:`bitlinear_pack_weights` -- latent fp32 W [N, K] -> (packed uint8 [N, K/4], gamma fp32 [1])
 * :func:`bitlinear_quant_act`    -- X bf16/fp32 [M, K]   -> (x_q int8 [M, K], s fp32 [M])
 * :func:`bitlinear_forward`      -- packed W, gamma, x_q, s -> y fp32 [M, N] (and int32 acc)
+* :func:`bitlinear_forward_ws`, :func:`bitlinear_quant_forward_ws` -- the same with a
+  caller workspace (:func:`bitlinear_forward_workspace_bytes`) for the tensor-core path
 * :func:`bitlinear_check_device_error`, :func:`bitlinear_status_string`
 """
 from __future__ import annotations
@@ -30,6 +32,9 @@ __all__ = [
     "bitlinear_quant_act",
     "bitlinear_forward",
     "bitlinear_quant_forward",
+    "bitlinear_forward_workspace_bytes",
+    "bitlinear_forward_ws",
+    "bitlinear_quant_forward_ws",
     "bitlinear_check_device_error",
     "bitlinear_status_string",
     "BITLINEAR_WEIGHTS_RESIDENT",
@@ -50,6 +55,9 @@ EXPORTED_SYMBOLS = (
     "bitlinear_quant_act",
     "bitlinear_forward",
     "bitlinear_quant_forward",
+    "bitlinear_forward_workspace_bytes",
+    "bitlinear_forward_ws",
+    "bitlinear_quant_forward_ws",
     "bitlinear_check_device_error",
     "bitlinear_status_string",
 )
@@ -79,6 +87,12 @@ def _load() -> ctypes.CDLL:
     L.bitlinear_pack_weights_noalloc.restype = i32
     L.bitlinear_quant_forward.argtypes = [P, P, P, i32, i64, i64, i64, P, P, P, P, ctypes.c_uint, P]
     L.bitlinear_quant_forward.restype = i32
+    L.bitlinear_forward_workspace_bytes.argtypes = [i64, i64, i64]
+    L.bitlinear_forward_workspace_bytes.restype = sz
+    L.bitlinear_forward_ws.argtypes = [P, P, P, P, i64, i64, i64, P, P, P, sz, P]
+    L.bitlinear_forward_ws.restype = i32
+    L.bitlinear_quant_forward_ws.argtypes = [P, P, P, i32, i64, i64, i64, P, P, P, P, ctypes.c_uint, P, sz, P]
+    L.bitlinear_quant_forward_ws.restype = i32
     L.bitlinear_check_device_error.argtypes = [P]
     L.bitlinear_check_device_error.restype = i32
     L.bitlinear_status_string.argtypes = [i32]
@@ -221,6 +235,78 @@ def bitlinear_quant_forward(W_packed: torch.Tensor, gamma: torch.Tensor, X: torc
                                              _dev(y, "y", torch.float32), _dev(x_q, "x_q", torch.int8),
                                              _dev(s, "s", torch.float32), acc_ptr, int(flags), _stream(stream)),
            "bitlinear_quant_forward")
+    return (y, x_q, s, acc) if want_acc else (y, x_q, s)
+
+
+def bitlinear_forward_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(get_lib().bitlinear_forward_workspace_bytes(int(M), int(N), int(K)))
+
+
+def _workspace(M: int, N: int, K: int, workspace, device):
+    need = bitlinear_forward_workspace_bytes(M, N, K)
+    if workspace is None:
+        workspace = torch.empty((max(need, 16),), dtype=torch.uint8, device=device)
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
+
+def bitlinear_forward_ws(W_packed: torch.Tensor, gamma: torch.Tensor, x_q: torch.Tensor, s: torch.Tensor,
+                         y: torch.Tensor | None = None, acc: torch.Tensor | bool | None = None,
+                         workspace: torch.Tensor | None = None, stream=None):
+    """:func:`bitlinear_forward` with a workspace of
+    ``bitlinear_forward_workspace_bytes(M, N, K)`` bytes (allocated here if not given)."""
+    N, K4 = W_packed.shape
+    M, K = x_q.shape
+    if K4 * 4 != K:
+        raise ValueError(f"W_packed has K/4 = {K4} but x_q has K = {K}")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x_q.device)
+    want_acc = acc is not None and acc is not False
+    if acc is True:
+        acc = torch.empty((M, N), dtype=torch.int32, device=x_q.device)
+    acc_ptr = _dev(acc, "acc", torch.int32) if want_acc else None
+    ws_ptr, ws_bytes = _workspace(M, N, K, workspace, x_q.device)
+    _check(get_lib().bitlinear_forward_ws(_dev(W_packed, "W_packed", torch.uint8), _dev(gamma, "gamma", torch.float32),
+                                          _dev(x_q, "x_q", torch.int8), _dev(s, "s", torch.float32), M, N, K,
+                                          _dev(y, "y", torch.float32), acc_ptr, ws_ptr, ws_bytes, _stream(stream)),
+           "bitlinear_forward_ws")
+    return (y, acc) if want_acc else y
+
+
+def bitlinear_quant_forward_ws(W_packed: torch.Tensor, gamma: torch.Tensor, X: torch.Tensor,
+                               y: torch.Tensor | None = None, x_q: torch.Tensor | None = None,
+                               s: torch.Tensor | None = None, acc: torch.Tensor | bool | None = None, flags: int = 0,
+                               workspace: torch.Tensor | None = None, stream=None):
+    """:func:`bitlinear_quant_forward` with a workspace of
+    ``bitlinear_forward_workspace_bytes(M, N, K)`` bytes (allocated here if not given)."""
+    N, K4 = W_packed.shape
+    M, K = X.shape
+    if K4 * 4 != K:
+        raise ValueError(f"W_packed has K/4 = {K4} but X has K = {K}")
+    if X.dtype == torch.bfloat16:
+        dt = BL_BF16
+    elif X.dtype == torch.float32:
+        dt = BL_F32
+    else:
+        raise ValueError(f"X must be bf16 or fp32, got {X.dtype}")
+    dev = X.device
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    if x_q is None:
+        x_q = torch.empty((M, K), dtype=torch.int8, device=dev)
+    if s is None:
+        s = torch.empty((M,), dtype=torch.float32, device=dev)
+    want_acc = acc is not None and acc is not False
+    if acc is True:
+        acc = torch.empty((M, N), dtype=torch.int32, device=dev)
+    acc_ptr = _dev(acc, "acc", torch.int32) if want_acc else None
+    ws_ptr, ws_bytes = _workspace(M, N, K, workspace, dev)
+    _check(get_lib().bitlinear_quant_forward_ws(_dev(W_packed, "W_packed", torch.uint8),
+                                                _dev(gamma, "gamma", torch.float32), _dev(X, "X"), dt, M, N, K,
+                                                _dev(y, "y", torch.float32), _dev(x_q, "x_q", torch.int8),
+                                                _dev(s, "s", torch.float32), acc_ptr, int(flags), ws_ptr, ws_bytes,
+                                                _stream(stream)), "bitlinear_quant_forward_ws")
     return (y, x_q, s, acc) if want_acc else (y, x_q, s)
 
 

@@ -118,6 +118,67 @@ bl_status bitlinear_quant_forward(const uint8_t* W_packed, const float* gamma, c
   return from_cuda(bl::launch_gemm_tc(a, d.num_sms, stream));
 }
 
+size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  (void)N;
+  if (M < 1 || K < 1) return 0;
+  if (M <= bl::kGemvMaxTokens && K <= bl::kGemvMaxK) return 0;  // the GEMV needs none
+  return bl::gemm_x16_workspace_bytes(M, K);
+}
+
+namespace {
+
+// Checks the workspace of the *_ws calls against the requirement of the path taken.
+bl_status check_workspace(int64_t M, int64_t N, int64_t K, const void* workspace, size_t workspace_bytes) {
+  const size_t need = bitlinear_forward_workspace_bytes(M, N, K);
+  if (need == 0) return BL_OK;
+  if (!workspace || workspace_bytes < need) return BL_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return BL_ERR_MISALIGNED;
+  return BL_OK;
+}
+
+}  // namespace
+
+bl_status bitlinear_forward_ws(const uint8_t* W_packed, const float* gamma, const int8_t* x_q, const float* s,
+                               int64_t M, int64_t N, int64_t K, float* y, int32_t* acc, void* workspace,
+                               size_t workspace_bytes, cudaStream_t stream) {
+  if (!W_packed || !gamma || !x_q || !s || !y) return BL_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1) return BL_ERR_INVALID_ARG;
+  if (K % 64 != 0 || K > BITLINEAR_MAX_K || M > INT32_MAX || N > INT32_MAX) return BL_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(W_packed, 16) || !aligned(x_q, 16) || !aligned(y, 16) || !aligned(gamma, 4) || !aligned(s, 4) ||
+      (acc && !aligned(acc, 16)))
+    return BL_ERR_MISALIGNED;
+  if (bl_status st = check_workspace(M, N, K, workspace, workspace_bytes)) return st;
+  DeviceInfo d;
+  if (bl_status st = device_info(&d)) return st;
+  bl::ForwardArgs a{W_packed, gamma, x_q, s, M, N, K, y, acc, d.err};
+  if (M <= bl::kGemvMaxTokens && K <= bl::kGemvMaxK) return from_cuda(bl::launch_gemv(a, d.num_sms, stream));
+  if (cudaError_t e = bl::launch_x16_prepass(x_q, M, K, workspace, d.num_sms, stream)) return from_cuda(e);
+  return from_cuda(bl::launch_gemm_tc_x16(a, workspace, d.num_sms, stream));
+}
+
+bl_status bitlinear_quant_forward_ws(const uint8_t* W_packed, const float* gamma, const void* X, bl_dtype dtype,
+                                     int64_t M, int64_t N, int64_t K, float* y, int8_t* x_q, float* s, int32_t* acc,
+                                     unsigned flags, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!W_packed || !gamma || !X || !y || !x_q || !s) return BL_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1) return BL_ERR_INVALID_ARG;
+  if (dtype != BL_F32 && dtype != BL_BF16) return BL_ERR_INVALID_ARG;
+  if (flags & ~BITLINEAR_WEIGHTS_RESIDENT) return BL_ERR_INVALID_ARG;
+  if (K % 64 != 0 || K > BITLINEAR_MAX_K || M > INT32_MAX || N > INT32_MAX) return BL_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(W_packed, 16) || !aligned(X, 16) || !aligned(x_q, 16) || !aligned(y, 16) || !aligned(gamma, 4) ||
+      !aligned(s, 4) || (acc && !aligned(acc, 16)))
+    return BL_ERR_MISALIGNED;
+  if (bl_status st = check_workspace(M, N, K, workspace, workspace_bytes)) return st;
+  DeviceInfo d;
+  if (bl_status st = device_info(&d)) return st;
+  bl::ForwardArgs a{W_packed, gamma, x_q, s, M, N, K, y, acc, d.err};
+  if (M <= bl::kGemvMaxTokens && K <= bl::kGemvMaxK)
+    return from_cuda(bl::launch_gemv_fused(a, X, dtype == BL_BF16, x_q, s, (flags & BITLINEAR_WEIGHTS_RESIDENT) != 0,
+                                           d.num_sms, stream));
+  if (cudaError_t e = bl::launch_quant_act(X, dtype == BL_BF16, M, K, x_q, s, stream)) return from_cuda(e);
+  if (cudaError_t e = bl::launch_x16_prepass(x_q, M, K, workspace, d.num_sms, stream)) return from_cuda(e);
+  return from_cuda(bl::launch_gemm_tc_x16(a, workspace, d.num_sms, stream));
+}
+
 bl_status bitlinear_check_device_error(cudaStream_t stream) {
   DeviceInfo d;
   if (bl_status st = device_info(&d)) return st;

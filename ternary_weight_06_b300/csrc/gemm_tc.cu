@@ -193,6 +193,31 @@ __device__ __forceinline__ void st_sw128(uint32_t tile, int r, int u, uint32_t a
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+// Epilogue of one 128 x BN tile: warp w (2..9) reads tensor-memory lanes
+// 32*(w%4) .. +31 (= features) and the two warps of a lane quarter take
+// alternate 16-token column chunks; y = fp32(acc) * fp32(gamma / s[m]).
+__device__ __forceinline__ void epilogue_store(const GemmCfg& c, uint32_t tmem, const float* tscale, int warp,
+                                               int lane, int n0, int m0) {
+  const int q = warp & 3;
+  const int n = n0 + q * 32 + lane;
+  for (int j0 = ((warp - 2) >> 2) * 16; j0 < c.BN; j0 += 32) {
+    uint32_t r[16];
+    tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)j0, r);
+    if (n < c.N) {
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) {
+        const int m = m0 + j0 + jj;
+        if (m < c.M) {
+          const float v = __uint_as_float(r[jj]);
+          const int64_t o = (int64_t)m * c.N + n;
+          c.y[o] = __fmul_rn(v, tscale[j0 + jj]);
+          if (c.acc) c.acc[o] = __float2int_rn(v);
+        }
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- the kernel
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -327,32 +352,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&op_full[os]);
       }
     }
-    // ---- epilogue: warp w reads tensor-memory lanes 32*(w%4) .. +31 = features;
-    // the two warps of a lane quarter take alternate 16-token column chunks
+    // ---- epilogue
     {
       const bool done = wait_flag(acc_full, 0u, c.err, abort_flag);
       tc_fence_after();
-      if (done) {
-        const int q = warp & 3;
-        const int f = q * 32 + lane;
-        const int n = n0 + f;
-        for (int j0 = ((warp - 2) >> 2) * 16; j0 < BN; j0 += 32) {
-          uint32_t r[16];
-          tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)j0, r);
-          if (n < c.N) {
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-              const int m = m0 + j0 + jj;
-              if (m < c.M) {
-                const float v = __uint_as_float(r[jj]);
-                const int64_t o = (int64_t)m * c.N + n;
-                c.y[o] = __fmul_rn(v, tscale[j0 + jj]);
-                if (c.acc) c.acc[o] = __float2int_rn(v);
-              }
-            }
-          }
-        }
-      }
+      if (done) epilogue_store(c, tmem, tscale, warp, lane, n0, m0);
       tc_fence_before();
     }
   }
@@ -360,6 +364,159 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     // Every MMA issued must have finished before its accumulator is freed; the
     // issuer always commits acc_full, so this completes (bounded in any case).
+    const uint32_t a = smem_u32(acc_full);
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait_sleep(a, 0u, kWaitHintNs) && globaltimer_ns() - t0 < kWaitLimitNs) {
+    }
+    tc_fence_after();
+    tmem_dealloc(tmem, tmem_cols);
+  }
+}
+
+// ---------------------------------------------------------------- activations expanded once per call
+//
+// With a workspace, the int8 activations are expanded to fp16 ONCE per call,
+// in the operand order above (p = 4i + j within every 16 k), instead of once
+// per 128-feature tile inside the GEMM: every tile of a prefill-sized problem
+// would otherwise repeat the same conversion N/128 times.  The GEMM then loads
+// the fp16 operand straight into its 128-byte-swizzled layout with a TMA copy.
+
+__global__ void __launch_bounds__(256) x16_prepass_kernel(const uint4* __restrict__ xq, uint64_t ngroups,
+                                                          uint4* __restrict__ x16) {
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < ngroups; i += stride) {
+    uint32_t f[8];
+    convert_x16_f16(__ldg(xq + i), f);
+    x16[2 * i] = make_uint4(f[0], f[1], f[2], f[3]);
+    x16[2 * i + 1] = make_uint4(f[4], f[5], f[6], f[7]);
+  }
+}
+
+constexpr int kX16Stages = 4;
+
+// The GEMM on pre-expanded activations.  Stage s of the ring holds
+// [A op 16 KB | B op BN*128 | packed W 2 KB]; the producer fills B (fp16 x,
+// swizzled by TMA) and the packed W tile, the converter warps expand W into A,
+// and one thread issues the MMAs.  Barriers per stage: tma_full (TMA bytes),
+// op_full (eight converter warps), op_empty (MMA commit).
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_x16_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x16,
+                       const GemmCfg c) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int BN = c.BN;
+  const int b_bytes = BN * kARowBytes;
+  const int stage_bytes = kAOpBytes + b_bytes + kWRawBytes;  // a multiple of 1024
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kX16Stages * stage_bytes);
+  uint64_t* tma_full = bars;
+  uint64_t* op_full = tma_full + kX16Stages;
+  uint64_t* op_empty = op_full + kX16Stages;
+  uint64_t* acc_full = op_empty + kX16Stages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+  float* tscale = reinterpret_cast<float*>(tmem_slot + 4);  // [BN]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * kBM;
+  const int m0 = blockIdx.y * BN;
+  const int nkb = c.K / kBK;
+  const uint32_t tmem_cols = BN <= 32 ? 32u : BN <= 64 ? 64u : BN <= 128 ? 128u : 256u;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kX16Stages; ++i) {
+      mbar_init(&tma_full[i], 1);
+      mbar_init(&op_full[i], kConvWarps);
+      mbar_init(&op_empty[i], 1);
+    }
+    mbar_init(acc_full, 1);
+    *abort_flag = 0u;
+    fence_mbarrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, tmem_cols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer
+    if (lane == 0) {
+      pdl_wait();  // the activations may come from the preceding kernel
+      int issued = 0;
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int os = kb % kX16Stages;
+        if (!wait_flag(&op_empty[os], ((uint32_t)(kb / kX16Stages) & 1u) ^ 1u, c.err, abort_flag)) break;
+        uint8_t* st = smem + os * stage_bytes;
+        mbar_arrive_expect_tx(&tma_full[os], (uint32_t)(b_bytes + kWRawBytes));
+        tma_load_2d(st + kAOpBytes + b_bytes, &tmap_w, kb * (kBK / 4), n0, &tma_full[os]);
+        tma_load_2d(st + kAOpBytes, &tmap_x16, kb * kBK, m0, &tma_full[os]);
+        issued = kb + 1;
+      }
+      if (*abort_flag) {
+        for (int kb = (issued > kX16Stages ? issued - kX16Stages : 0); kb < issued; ++kb) {
+          const uint32_t a = smem_u32(&tma_full[kb % kX16Stages]), par = (uint32_t)(kb / kX16Stages) & 1u;
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait_sleep(a, par, kWaitHintNs) && globaltimer_ns() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = f16_idesc(kBM, BN);
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int os = kb % kX16Stages;
+        const uint32_t par = (uint32_t)(kb / kX16Stages) & 1u;
+        if (!wait_flag(&op_full[os], par, c.err, abort_flag) || !wait_flag(&tma_full[os], par, c.err, abort_flag))
+          break;
+        tc_fence_after();
+        const uint32_t a_base = smem_u32(smem + os * stage_bytes);
+        const uint32_t b_base = a_base + kAOpBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          mma_f16(tmem, sw128_desc(a_base + kk * 32), sw128_desc(b_base + kk * 32), idesc, (kb | kk) ? 1u : 0u);
+        mma_commit(&op_empty[os]);
+      }
+      mma_commit(acc_full);
+    }
+  } else {
+    // ---------------- W converters, then epilogue
+    const int ct = threadIdx.x - 64;  // 0 .. 255
+    pdl_wait();
+    const float gamma = __ldg(c.gamma);
+    for (int j = ct; j < BN; j += 32 * kConvWarps) {
+      const int m = m0 + j;
+      tscale[j] = m < c.M ? __fdiv_rn(gamma, __ldg(c.s + m)) : 0.0f;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kConvWarps) : "memory");
+    for (int kb = 0; kb < nkb; ++kb) {
+      const int os = kb % kX16Stages;
+      if (!wait_flag(&tma_full[os], (uint32_t)(kb / kX16Stages) & 1u, c.err, abort_flag)) break;
+      const uint32_t aop = smem_u32(smem + os * stage_bytes);
+      const uint32_t wraw = aop + kAOpBytes + b_bytes;
+      const int r = ct >> 1, h = ct & 1;
+      const uint2 pw = lds64(wraw + (uint32_t)(r * 16 + h * 8));
+      uint32_t f[8];
+      unpack_word_f16(pw.x, f);
+      st_sw128(aop, r, 4 * h + 0, f[0], f[1], f[2], f[3]);
+      st_sw128(aop, r, 4 * h + 1, f[4], f[5], f[6], f[7]);
+      unpack_word_f16(pw.y, f);
+      st_sw128(aop, r, 4 * h + 2, f[0], f[1], f[2], f[3]);
+      st_sw128(aop, r, 4 * h + 3, f[4], f[5], f[6], f[7]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&op_full[os]);
+    }
+    {
+      const bool done = wait_flag(acc_full, 0u, c.err, abort_flag);
+      tc_fence_after();
+      if (done) epilogue_store(c, tmem, tscale, warp, lane, n0, m0);
+      tc_fence_before();
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
     const uint32_t a = smem_u32(acc_full);
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait_sleep(a, 0u, kWaitHintNs) && globaltimer_ns() - t0 < kWaitLimitNs) {
@@ -401,14 +558,60 @@ bool encode_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t o
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp16 [outer, inner] row-major, box {64 elements = 128 bytes, box_outer}, 128-byte swizzle.
+bool encode_f16_2d_sw128(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {64, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Token tiles of equal size, rounded up to the MMA's N granularity of 16.
+int token_tile(int64_t M, int64_t* ntiles) {
+  *ntiles = (M + 255) / 256;
+  const int BN = (int)((M + *ntiles - 1) / *ntiles);
+  return (BN + 15) / 16 * 16;
+}
+
 }  // namespace
+
+size_t gemm_x16_workspace_bytes(int64_t M, int64_t K) { return (size_t)M * (size_t)K * 2; }
+
+cudaError_t launch_x16_prepass(const int8_t* xq, int64_t M, int64_t K, void* x16, int num_sms, cudaStream_t stream) {
+  const uint64_t ngroups = (uint64_t)M * (uint64_t)K / 16;
+  const uint64_t want = (ngroups + 255) / 256;
+  const int grid = (int)(want < (uint64_t)num_sms * 8 ? (want ? want : 1) : (uint64_t)num_sms * 8);
+  x16_prepass_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint4*>(xq), ngroups,
+                                               reinterpret_cast<uint4*>(x16));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_tc_x16(const ForwardArgs& a, const void* x16, int num_sms, cudaStream_t stream) {
+  (void)num_sms;
+  int64_t ntiles = 0;
+  const int BN = token_tile(a.M, &ntiles);
+  CUtensorMap tw, tx;
+  if (!encode_u8_2d(&tw, a.Wp, (uint64_t)a.K / 4, (uint64_t)a.N, kBK / 4, kBM)) return cudaErrorInvalidValue;
+  if (!encode_f16_2d_sw128(&tx, x16, (uint64_t)a.K, (uint64_t)a.M, (uint32_t)BN)) return cudaErrorInvalidValue;
+  GemmCfg c{a.gamma, a.s, a.y, a.acc, a.err, (int)a.M, (int)a.N, (int)a.K, BN};
+  const size_t smem = 1024 + (size_t)kX16Stages * (kAOpBytes + BN * kARowBytes + kWRawBytes) +
+                      (3 * kX16Stages + 1) * 8 + 16 + (size_t)BN * 4;
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_x16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)((a.N + kBM - 1) / kBM), (unsigned)ntiles);
+  gemm_tc_x16_kernel<<<grid, kThreads, smem, stream>>>(tw, tx, c);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gemm_tc(const ForwardArgs& a, int num_sms, cudaStream_t stream) {
   (void)num_sms;
-  // token tiles of equal size, rounded up to the MMA's N granularity of 16
-  const int64_t ntiles = (a.M + 255) / 256;
-  int BN = (int)((a.M + ntiles - 1) / ntiles);
-  BN = (BN + 15) / 16 * 16;
+  int64_t ntiles = 0;
+  const int BN = token_tile(a.M, &ntiles);
   CUtensorMap tw, tx;
   if (!encode_u8_2d(&tw, a.Wp, (uint64_t)a.K / 4, (uint64_t)a.N, kBK / 4, kBM)) return cudaErrorInvalidValue;
   if (!encode_u8_2d(&tx, a.xq, (uint64_t)a.K, (uint64_t)a.M, kBK, (uint32_t)BN)) return cudaErrorInvalidValue;

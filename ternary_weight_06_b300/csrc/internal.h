@@ -50,4 +50,11 @@ constexpr int64_t kGemvMaxK = 32768;
 // Tensor-core GEMM (tcgen05) for more tokens than the GEMV handles well.
 cudaError_t launch_gemm_tc(const ForwardArgs& a, int num_sms, cudaStream_t stream);
 
+// The same GEMM with the activations expanded to fp16 once per call into a
+// workspace of gemm_x16_workspace_bytes(M, K) bytes (16-byte aligned):
+// launch_x16_prepass writes it from x_q, then launch_gemm_tc_x16 reads it.
+size_t gemm_x16_workspace_bytes(int64_t M, int64_t K);
+cudaError_t launch_x16_prepass(const int8_t* xq, int64_t M, int64_t K, void* x16, int num_sms, cudaStream_t stream);
+cudaError_t launch_gemm_tc_x16(const ForwardArgs& a, const void* x16, int num_sms, cudaStream_t stream);
+
 }  // namespace bl

@@ -34,7 +34,8 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ("bitlinear_pack_weights", "bitlinear_quant_act", "bitlinear_forward",
                      "bitlinear_quant_forward", "bitlinear_check_device_error", "bitlinear_status_string",
-                     "bitlinear_pack_workspace_bytes"):
+                     "bitlinear_pack_workspace_bytes", "bitlinear_forward_workspace_bytes", "bitlinear_forward_ws",
+                     "bitlinear_quant_forward_ws"):
         assert required in names
 
 
@@ -143,6 +144,48 @@ def test_quant_forward_validation(bl):
     assert qfwd(bl, xq=GOOD + 4) == bl.BL_ERR_MISALIGNED
     assert qfwd(bl, s=GOOD + 1) == bl.BL_ERR_MISALIGNED
     assert qfwd(bl, acc=GOOD + 8) == bl.BL_ERR_MISALIGNED
+
+
+def test_forward_workspace_bytes(bl):
+    f = bl.bitlinear_forward_workspace_bytes
+    assert f(1, 6912, 2560) == 0 and f(4, 100, 32768) == 0  # the GEMV path needs none
+    assert f(5, 100, 64) == 2 * 5 * 64
+    assert f(2048, 6912, 2560) == 2 * 2048 * 2560
+    assert f(1, 100, 32768 + 64) == 2 * (32768 + 64)  # K beyond the GEMV goes to the GEMM
+    assert f(0, 1, 64) == 0
+
+
+def fwd_ws(bl, M=8, N=16, K=64, ws=GOOD, ws_bytes=1 << 20, **kw):
+    args = dict(Wp=GOOD, g=GOOD, xq=GOOD, s=GOOD, y=GOOD, acc=None)
+    args.update(kw)
+    return bl.get_lib().bitlinear_forward_ws(args["Wp"], args["g"], args["xq"], args["s"], M, N, K, args["y"],
+                                             args["acc"], ws, ws_bytes, None)
+
+
+def qfwd_ws(bl, M=8, N=16, K=64, ws=GOOD, ws_bytes=1 << 20, dt=1, flags=0, **kw):
+    args = dict(Wp=GOOD, g=GOOD, X=GOOD, y=GOOD, xq=GOOD, s=GOOD, acc=None)
+    args.update(kw)
+    return bl.get_lib().bitlinear_quant_forward_ws(args["Wp"], args["g"], args["X"], dt, M, N, K, args["y"],
+                                                   args["xq"], args["s"], args["acc"], flags, ws, ws_bytes, None)
+
+
+def test_forward_ws_validation(bl):
+    for kw in ("Wp", "g", "xq", "s", "y"):
+        assert fwd_ws(bl, **{kw: None}) == bl.BL_ERR_INVALID_ARG, kw
+    assert fwd_ws(bl, M=0) == bl.BL_ERR_INVALID_ARG
+    assert fwd_ws(bl, K=96) == bl.BL_ERR_UNSUPPORTED_SHAPE
+    assert fwd_ws(bl, Wp=GOOD + 4) == bl.BL_ERR_MISALIGNED
+    assert fwd_ws(bl, ws=None) == bl.BL_ERR_WORKSPACE
+    assert fwd_ws(bl, ws_bytes=2 * 8 * 64 - 1) == bl.BL_ERR_WORKSPACE
+    assert fwd_ws(bl, ws=GOOD + 8) == bl.BL_ERR_MISALIGNED
+    for kw in ("Wp", "g", "X", "y", "xq", "s"):
+        assert qfwd_ws(bl, **{kw: None}) == bl.BL_ERR_INVALID_ARG, kw
+    assert qfwd_ws(bl, dt=3) == bl.BL_ERR_INVALID_ARG
+    assert qfwd_ws(bl, flags=2) == bl.BL_ERR_INVALID_ARG
+    assert qfwd_ws(bl, X=GOOD + 2) == bl.BL_ERR_MISALIGNED
+    assert qfwd_ws(bl, ws=None) == bl.BL_ERR_WORKSPACE
+    assert qfwd_ws(bl, ws_bytes=100) == bl.BL_ERR_WORKSPACE
+    assert qfwd_ws(bl, ws=GOOD + 4) == bl.BL_ERR_MISALIGNED
 
 
 def test_python_binding_rejects_cpu_tensors(bl):

@@ -181,10 +181,11 @@ def sample_rows(M: int, limit: int, seed: int) -> np.ndarray:
     return np.array(sorted(rows))
 
 
-def forward_case(bl, p_ref, g_ref, xq_ref, s_ref, K, rows, where):
+def forward_case(bl, p_ref, g_ref, xq_ref, s_ref, K, rows, where, ws=False):
     Wp = gpu(torch.from_numpy(p_ref))
     gamma = gpu(torch.tensor([g_ref], dtype=torch.float32))
-    y, acc = bl.bitlinear_forward(Wp, gamma, gpu(torch.from_numpy(xq_ref)), gpu(torch.from_numpy(s_ref)), acc=True)
+    call = bl.bitlinear_forward_ws if ws else bl.bitlinear_forward
+    y, acc = call(Wp, gamma, gpu(torch.from_numpy(xq_ref)), gpu(torch.from_numpy(s_ref)), acc=True)
     torch.cuda.synchronize()
     y_ref, acc_ref = oracle.forward(p_ref, g_ref, xq_ref[rows], s_ref[rows], K)
     acc_gpu = acc.cpu().numpy()[rows]
@@ -287,12 +288,13 @@ def test_forward_runs_on_a_side_stream(bl):
 
 # ---------------------------------------------------------------- fused quant + forward
 
-def fused_case(bl, p_ref, g_ref, X, K, rows, where, flags=0):
+def fused_case(bl, p_ref, g_ref, X, K, rows, where, flags=0, ws=False):
     """The one-call path against the oracle: x_q, s, acc bit-exact, y to the contract."""
     xq_ref, s_ref = oracle.quant_act(X.to(torch.float32).numpy())
     Wp = gpu(torch.from_numpy(p_ref))
     gamma = gpu(torch.tensor([g_ref], dtype=torch.float32))
-    y, xq, s, acc = bl.bitlinear_quant_forward(Wp, gamma, gpu(X), acc=True, flags=flags)
+    call = bl.bitlinear_quant_forward_ws if ws else bl.bitlinear_quant_forward
+    y, xq, s, acc = call(Wp, gamma, gpu(X), acc=True, flags=flags)
     torch.cuda.synchronize()
     assert np.array_equal(s.cpu().numpy().view(np.uint32), s_ref.view(np.uint32)), where
     assert np.array_equal(xq.cpu().numpy(), xq_ref), where
@@ -352,3 +354,83 @@ def test_quant_forward_chain_with_resident_weights(bl):
         xr, _ = oracle.forward(refs[i], np.float32(0.02), xq, s, dims[i])
     assert_y_close(x.cpu().numpy(), xr, "resident chain")
     bl.bitlinear_check_device_error()
+
+
+# ---------------------------------------------------------------- workspace variants (activations expanded once)
+
+@pytest.mark.parametrize("wl_name,idx", all_activation_layers())
+def test_forward_ws_full_size(bl, wl_name, idx):
+    wl = workloads.WORKLOADS[wl_name]
+    L = wl.layers[idx]
+    p_ref, g_ref = packed_layer(wl_name, idx)
+    X = workloads.layer_activations(wl, idx)
+    xq_ref, s_ref = oracle.quant_act(workloads.x_as_f32_numpy(X))
+    rows = sample_rows(L.M, row_budget(L.N, L.K), seed=idx)
+    forward_case(bl, p_ref, g_ref, xq_ref, s_ref, L.K, rows, f"ws {wl_name}[{idx}] M={L.M} K={L.K} N={L.N}", ws=True)
+
+
+@pytest.mark.parametrize("M", [1, 5, 8, 16, 17, 64, 130, 257])
+@pytest.mark.parametrize("N,K", [(1, 64), (13, 128), (255, 576), (1000, 2560), (1025, 8640), (130, 32768 + 64)])
+def test_forward_ws_edge_shapes(bl, M, N, K):
+    rng = np.random.default_rng(M * 1000 + N + 7)
+    q = rng.integers(-1, 2, size=(N, K)).astype(np.int8)
+    xq = rng.integers(-128, 128, size=(M, K)).astype(np.int8)
+    if M > 1:
+        xq[1, :] = 0
+    s = rng.uniform(0.5, 300, size=M).astype(np.float32)
+    forward_case(bl, oracle.pack(q), np.float32(0.0123), xq, s, K, sample_rows(M, 64, seed=M),
+                 f"ws edge M={M} N={N} K={K}", ws=True)
+
+
+@pytest.mark.parametrize("M", [5, 64, 256])
+def test_forward_ws_extreme_magnitudes_exact(bl, M):
+    K, N = 8192, 384
+    q = np.ones((N, K), np.int8)
+    q[1::3] = -1
+    q[2::3, ::2] = 1
+    q[2::3, 1::2] = -1
+    xq = np.full((M, K), 127, np.int8)
+    xq[1::2] = -128
+    xq[0, K // 2:] = -127
+    forward_case(bl, oracle.pack(q), np.float32(1.0), xq, np.ones((M,), np.float32), K, np.arange(M),
+                 f"ws extreme M={M}", ws=True)
+
+
+def test_forward_ws_equals_forward_bitwise(bl):
+    rng = np.random.default_rng(11)
+    M, N, K = 300, 700, 1024
+    Wp = gpu(torch.from_numpy(oracle.pack(rng.integers(-1, 2, size=(N, K)).astype(np.int8))))
+    xq = gpu(torch.from_numpy(rng.integers(-128, 128, size=(M, K)).astype(np.int8)))
+    s = gpu(torch.from_numpy(rng.uniform(0.1, 10, size=M).astype(np.float32)))
+    g = gpu(torch.tensor([0.05]))
+    y0 = bl.bitlinear_forward(Wp, g, xq, s)
+    ws = torch.empty((bl.bitlinear_forward_workspace_bytes(M, N, K),), dtype=torch.uint8, device="cuda")
+    y1 = bl.bitlinear_forward_ws(Wp, g, xq, s, workspace=ws)
+    y2 = bl.bitlinear_forward_ws(Wp, g, xq, s, workspace=ws)  # the workspace is reused as is
+    torch.cuda.synchronize()
+    assert torch.equal(y0.view(torch.int32), y1.view(torch.int32)) and torch.equal(y1, y2)
+
+
+@pytest.mark.parametrize("wl_name,idx", all_activation_layers())
+def test_quant_forward_ws_full_size(bl, wl_name, idx):
+    wl = workloads.WORKLOADS[wl_name]
+    L = wl.layers[idx]
+    p_ref, g_ref = packed_layer(wl_name, idx)
+    X = workloads.layer_activations(wl, idx)
+    rows = sample_rows(L.M, row_budget(L.N, L.K), seed=idx)
+    fused_case(bl, p_ref, g_ref, X, L.K, rows, f"ws fused {wl_name}[{idx}]", ws=True)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("M", [1, 5, 9, 64])
+@pytest.mark.parametrize("N,K", [(7, 64), (300, 1024), (999, 6912), (40, 32768 + 64)])
+def test_quant_forward_ws_edge_shapes(bl, dtype, M, N, K):
+    rng = np.random.default_rng(M * 13 + N)
+    q = rng.integers(-1, 2, size=(N, K)).astype(np.int8)
+    g = torch.Generator().manual_seed(N + M + 3)
+    X = torch.randn((M, K), generator=g)
+    if M > 2:
+        X[2] = 0
+    X = X.to(dtype)
+    fused_case(bl, oracle.pack(q), np.float32(0.031), X, K, sample_rows(M, 16, seed=M),
+               f"ws fused M={M} N={N} K={K}", ws=True)
