@@ -55,6 +55,8 @@ struct GemmCfg {
   int32_t* acc;
   uint32_t* err;
   int M, N, K, BN;
+  int nstages;  // ring depth (the GEMM on pre-expanded activations)
+  int ksplit;   // CTAs of a cluster that split K (1 = no split)
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -392,26 +394,65 @@ __global__ void __launch_bounds__(256) x16_prepass_kernel(const uint4* __restric
   }
 }
 
-constexpr int kX16Stages = 4;
+constexpr int kX16MaxStages = 12;
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// All threads of every CTA of the cluster; release/acquire orders the shared
+// memory written before it against the peers' reads after it.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void sts_f32(uint32_t addr, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
 
 // The GEMM on pre-expanded activations.  Stage s of the ring holds
 // [A op 16 KB | B op BN*128 | packed W 2 KB]; the producer fills B (fp16 x,
 // swizzled by TMA) and the packed W tile, the converter warps expand W into A,
 // and one thread issues the MMAs.  Barriers per stage: tma_full (TMA bytes),
-// op_full (eight converter warps), op_empty (MMA commit).
+// op_full (eight converter warps), op_empty (MMA commit).  The ring depth
+// c.nstages is chosen on the host from the shared memory a stage needs.
+//
+// Split K (c.ksplit = S > 1): the S CTAs of a thread-block cluster share one
+// output tile and take consecutive ranges of k-blocks.  Each stores its partial
+// accumulator in its own (by then idle) ring memory as R[token][feature]; after
+// a cluster barrier, rank r reduces the 16-token column chunks c with
+// c % S == r by reading the S partials (its own and its peers', over
+// distributed shared memory) in rank order and writes y.  Every partial is an
+// integer of magnitude < 2^24, so the fp32 sums are exact in any order.
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_x16_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x16,
                        const GemmCfg c) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int BN = c.BN;
+  const int NS = c.nstages;
+  const int S = c.ksplit;
   const int b_bytes = BN * kARowBytes;
   const int stage_bytes = kAOpBytes + b_bytes + kWRawBytes;  // a multiple of 1024
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kX16Stages * stage_bytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NS * stage_bytes);
   uint64_t* tma_full = bars;
-  uint64_t* op_full = tma_full + kX16Stages;
-  uint64_t* op_empty = op_full + kX16Stages;
-  uint64_t* acc_full = op_empty + kX16Stages;
+  uint64_t* op_full = tma_full + kX16MaxStages;
+  uint64_t* op_empty = op_full + kX16MaxStages;
+  uint64_t* acc_full = op_empty + kX16MaxStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   float* tscale = reinterpret_cast<float*>(tmem_slot + 4);  // [BN]
@@ -419,11 +460,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * kBM;
   const int m0 = blockIdx.y * BN;
-  const int nkb = c.K / kBK;
+  const int nkb_all = c.K / kBK;
+  const int z = (int)blockIdx.z;  // = rank in the cluster (cluster dims 1 x 1 x S)
+  const int kb0 = (int)((int64_t)z * nkb_all / S), kb1 = (int)((int64_t)(z + 1) * nkb_all / S);
+  const int nkb = kb1 - kb0;
   const uint32_t tmem_cols = BN <= 32 ? 32u : BN <= 64 ? 64u : BN <= 128 ? 128u : 256u;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kX16Stages; ++i) {
+    for (int i = 0; i < NS; ++i) {
       mbar_init(&tma_full[i], 1);
       mbar_init(&op_full[i], kConvWarps);
       mbar_init(&op_empty[i], 1);
@@ -442,19 +486,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- TMA producer
     if (lane == 0) {
       pdl_wait();  // the activations may come from the preceding kernel
-      int issued = 0;
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int os = kb % kX16Stages;
-        if (!wait_flag(&op_empty[os], ((uint32_t)(kb / kX16Stages) & 1u) ^ 1u, c.err, abort_flag)) break;
+      int issued = 0, os = 0;
+      uint32_t ph = 0;  // ring slot and phase parity, advanced without divisions
+      for (int i = 0; i < nkb; ++i) {
+        if (!wait_flag(&op_empty[os], ph ^ 1u, c.err, abort_flag)) break;
         uint8_t* st = smem + os * stage_bytes;
+        const int kb = kb0 + i;
         mbar_arrive_expect_tx(&tma_full[os], (uint32_t)(b_bytes + kWRawBytes));
         tma_load_2d(st + kAOpBytes + b_bytes, &tmap_w, kb * (kBK / 4), n0, &tma_full[os]);
         tma_load_2d(st + kAOpBytes, &tmap_x16, kb * kBK, m0, &tma_full[os]);
-        issued = kb + 1;
+        issued = i + 1;
+        if (++os == NS) {
+          os = 0;
+          ph ^= 1u;
+        }
       }
       if (*abort_flag) {
-        for (int kb = (issued > kX16Stages ? issued - kX16Stages : 0); kb < issued; ++kb) {
-          const uint32_t a = smem_u32(&tma_full[kb % kX16Stages]), par = (uint32_t)(kb / kX16Stages) & 1u;
+        for (int i = (issued > NS ? issued - NS : 0); i < issued; ++i) {
+          const uint32_t a = smem_u32(&tma_full[i % NS]), par = (uint32_t)(i / NS) & 1u;
           const uint64_t t0 = globaltimer_ns();
           while (!mbar_try_wait_sleep(a, par, kWaitHintNs) && globaltimer_ns() - t0 < kWaitLimitNs) {
           }
@@ -465,9 +514,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = f16_idesc(kBM, BN);
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int os = kb % kX16Stages;
-        const uint32_t par = (uint32_t)(kb / kX16Stages) & 1u;
+      int os = 0;
+      uint32_t par = 0;
+      for (int i = 0; i < nkb; ++i) {
         if (!wait_flag(&op_full[os], par, c.err, abort_flag) || !wait_flag(&tma_full[os], par, c.err, abort_flag))
           break;
         tc_fence_after();
@@ -475,13 +524,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t b_base = a_base + kAOpBytes;
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk)
-          mma_f16(tmem, sw128_desc(a_base + kk * 32), sw128_desc(b_base + kk * 32), idesc, (kb | kk) ? 1u : 0u);
+          mma_f16(tmem, sw128_desc(a_base + kk * 32), sw128_desc(b_base + kk * 32), idesc, (i | kk) ? 1u : 0u);
         mma_commit(&op_empty[os]);
+        if (++os == NS) {
+          os = 0;
+          par ^= 1u;
+        }
       }
       mma_commit(acc_full);
     }
   } else {
-    // ---------------- W converters, then epilogue
+    // ---------------- W converters
     const int ct = threadIdx.x - 64;  // 0 .. 255
     pdl_wait();
     const float gamma = __ldg(c.gamma);
@@ -490,9 +543,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tscale[j] = m < c.M ? __fdiv_rn(gamma, __ldg(c.s + m)) : 0.0f;
     }
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kConvWarps) : "memory");
-    for (int kb = 0; kb < nkb; ++kb) {
-      const int os = kb % kX16Stages;
-      if (!wait_flag(&tma_full[os], (uint32_t)(kb / kX16Stages) & 1u, c.err, abort_flag)) break;
+    int os = 0;
+    uint32_t par = 0;
+    for (int i = 0; i < nkb; ++i) {
+      if (!wait_flag(&tma_full[os], par, c.err, abort_flag)) break;
       const uint32_t aop = smem_u32(smem + os * stage_bytes);
       const uint32_t wraw = aop + kAOpBytes + b_bytes;
       const int r = ct >> 1, h = ct & 1;
@@ -507,14 +561,63 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&op_full[os]);
-    }
-    {
-      const bool done = wait_flag(acc_full, 0u, c.err, abort_flag);
-      tc_fence_after();
-      if (done) epilogue_store(c, tmem, tscale, warp, lane, n0, m0);
-      tc_fence_before();
+      if (++os == NS) {
+        os = 0;
+        par ^= 1u;
+      }
     }
   }
+
+  // ---------------- epilogue (converter warps 2..9)
+  const bool epi = warp >= 2;
+  bool done = false;
+  if (epi) {
+    done = wait_flag(acc_full, 0u, c.err, abort_flag);
+    tc_fence_after();
+  }
+  if (S == 1) {
+    if (epi && done) epilogue_store(c, tmem, tscale, warp, lane, n0, m0);
+  } else {
+    // partial accumulator -> R[token][feature] in this CTA's ring memory
+    const uint32_t R = smem_u32(smem);
+    const int q = warp & 3, f = q * 32 + lane;
+    if (epi && done) {
+      for (int j0 = ((warp - 2) >> 2) * 16; j0 < BN; j0 += 32) {
+        uint32_t r[16];
+        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)j0, r);
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) sts_f32(R + (uint32_t)(((j0 + jj) * kBM + f) * 4), __uint_as_float(r[jj]));
+      }
+    }
+    __syncwarp();
+    cluster_sync_all();
+    if (epi) {
+      const uint32_t rank = cluster_ctarank();
+      const int n = n0 + f;
+      // 16-token chunks: chunk index c16 = j0/16; rank takes c16 % S == rank, the two
+      // warps of a lane quarter alternate over those chunks
+      int seq = 0;
+      for (int j0 = 0; j0 < BN; j0 += 16) {
+        if ((j0 / 16) % S != (int)rank) continue;
+        if ((seq++ & 1) != ((warp - 2) >> 2)) continue;
+        if (n >= c.N) continue;
+#pragma unroll 4
+        for (int jj = 0; jj < 16; ++jj) {
+          const int m = m0 + j0 + jj;
+          if (m >= c.M) break;
+          const uint32_t off = (uint32_t)(((j0 + jj) * kBM + f) * 4);
+          float v = 0.0f;
+          for (int pr = 0; pr < S; ++pr) v += ld_cluster_f32(map_to_rank(R + off, (uint32_t)pr));
+          const int64_t o = (int64_t)m * c.N + n;
+          c.y[o] = __fmul_rn(v, tscale[j0 + jj]);
+          if (c.acc) c.acc[o] = __float2int_rn(v);
+        }
+      }
+    }
+    __syncwarp();
+    cluster_sync_all();  // peers keep their shared memory until every read is done
+  }
+  if (epi) tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     const uint32_t a = smem_u32(acc_full);
@@ -591,21 +694,101 @@ cudaError_t launch_x16_prepass(const int8_t* xq, int64_t M, int64_t K, void* x16
   return cudaGetLastError();
 }
 
+namespace {
+
+constexpr size_t kMaxDynSmem = 227 * 1024;       // per CTA (opt-in limit)
+constexpr size_t kSmemPerSm = 228 * 1024;        // per SM
+constexpr size_t kSmemReservedPerCta = 1024;     // reserved by the system per resident CTA
+
+size_t x16_smem_bytes(int BN, int NS) {
+  return 1024 + (size_t)NS * (kAOpBytes + (size_t)BN * kARowBytes + kWRawBytes) + (3 * kX16MaxStages + 1) * 8 + 16 +
+         (size_t)BN * 4;
+}
+
+// Largest cluster size S <= 8 (and <= k-blocks / 4) for which every cluster of
+// the grid is resident at once, when the tile grid alone fills fewer than all
+// SMs; 1 otherwise.  Results are cached per (tiles, k-blocks, BN, stages).
+int choose_ksplit(int64_t tiles, int nkb, int BN, int NS, size_t smem, int num_sms) {
+  if (tiles >= num_sms) return 1;
+  struct Entry {
+    int64_t tiles;
+    int nkb, BN, NS, S;
+  };
+  static std::mutex mu;
+  static Entry cache[64];
+  static int ncache = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < ncache; ++i)
+      if (cache[i].tiles == tiles && cache[i].nkb == nkb && cache[i].BN == BN && cache[i].NS == NS) return cache[i].S;
+  }
+  int best = 1;
+  for (int S = 8; S >= 2; --S) {
+    if (tiles * S > 2 * (int64_t)num_sms || nkb / S < 4) continue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, (unsigned)S);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = (unsigned)S;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int nclusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&nclusters, gemm_tc_x16_kernel, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      continue;
+    }
+    if (nclusters >= tiles) {
+      best = S;
+      break;
+    }
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (ncache < 64) cache[ncache++] = Entry{tiles, nkb, BN, NS, best};
+  return best;
+}
+
+}  // namespace
+
 cudaError_t launch_gemm_tc_x16(const ForwardArgs& a, const void* x16, int num_sms, cudaStream_t stream) {
-  (void)num_sms;
   int64_t ntiles = 0;
   const int BN = token_tile(a.M, &ntiles);
   CUtensorMap tw, tx;
   if (!encode_u8_2d(&tw, a.Wp, (uint64_t)a.K / 4, (uint64_t)a.N, kBK / 4, kBM)) return cudaErrorInvalidValue;
   if (!encode_f16_2d_sw128(&tx, x16, (uint64_t)a.K, (uint64_t)a.M, (uint32_t)BN)) return cudaErrorInvalidValue;
-  GemmCfg c{a.gamma, a.s, a.y, a.acc, a.err, (int)a.M, (int)a.N, (int)a.K, BN};
-  const size_t smem = 1024 + (size_t)kX16Stages * (kAOpBytes + BN * kARowBytes + kWRawBytes) +
-                      (3 * kX16Stages + 1) * 8 + 16 + (size_t)BN * 4;
+  // Ring depth: two CTAs per SM when that still leaves >= 4 stages (small
+  // token tiles: the grid then fits in fewer waves), else one CTA with the
+  // deepest ring that fits.
+  const size_t stage = kAOpBytes + (size_t)BN * kARowBytes + kWRawBytes;
+  const size_t fixed = x16_smem_bytes(BN, 0);
+  int NS = (int)((kSmemPerSm / 2 - kSmemReservedPerCta - fixed) / stage);
+  if (NS < 4) NS = (int)((kMaxDynSmem - fixed) / stage);
+  if (NS > kX16MaxStages) NS = kX16MaxStages;
+  const size_t smem = x16_smem_bytes(BN, NS);
   cudaError_t e = cudaFuncSetAttribute(gemm_tc_x16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)((a.N + kBM - 1) / kBM), (unsigned)ntiles);
-  gemm_tc_x16_kernel<<<grid, kThreads, smem, stream>>>(tw, tx, c);
-  return cudaGetLastError();
+  const int ntn = (int)((a.N + kBM - 1) / kBM);
+  const int nkb = (int)(a.K / kBK);
+  int S = choose_ksplit((int64_t)ntn * ntiles, nkb, BN, NS, smem, num_sms);
+  // the split partials live in the ring memory: 128 x BN fp32
+  if ((size_t)kBM * BN * 4 > (size_t)NS * stage) S = 1;
+  GemmCfg c{a.gamma, a.s, a.y, a.acc, a.err, (int)a.M, (int)a.N, (int)a.K, BN, NS, S};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ntn, (unsigned)ntiles, (unsigned)S);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = (unsigned)S;
+  cfg.attrs = attr;
+  cfg.numAttrs = S > 1 ? 1 : 0;  // an unsplit grid is launched without clusters
+  return cudaLaunchKernelEx(&cfg, gemm_tc_x16_kernel, tw, tx, c);
 }
 
 cudaError_t launch_gemm_tc(const ForwardArgs& a, int num_sms, cudaStream_t stream) {
@@ -615,7 +798,7 @@ cudaError_t launch_gemm_tc(const ForwardArgs& a, int num_sms, cudaStream_t strea
   CUtensorMap tw, tx;
   if (!encode_u8_2d(&tw, a.Wp, (uint64_t)a.K / 4, (uint64_t)a.N, kBK / 4, kBM)) return cudaErrorInvalidValue;
   if (!encode_u8_2d(&tx, a.xq, (uint64_t)a.K, (uint64_t)a.M, kBK, (uint32_t)BN)) return cudaErrorInvalidValue;
-  GemmCfg c{a.gamma, a.s, a.y, a.acc, a.err, (int)a.M, (int)a.N, (int)a.K, BN};
+  GemmCfg c{a.gamma, a.s, a.y, a.acc, a.err, (int)a.M, (int)a.N, (int)a.K, BN, 0, 1};
   const size_t smem = 1024 + (size_t)kOpStages * (kAOpBytes + BN * kARowBytes) +
                       (size_t)kRawStages * (kWRawBytes + BN * kBK) + (2 * kRawStages + 2 * kOpStages + 1) * 8 + 16 +
                       (size_t)BN * 4;
