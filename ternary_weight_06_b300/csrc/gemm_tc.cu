@@ -629,6 +629,216 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- persistent variant for large grids
+//
+// One CTA per SM walks the output tiles t = blockIdx.x, blockIdx.x + gridDim.x,
+// ... (feature tiles fastest, so CTAs running at the same time share the
+// activation tile in L2).  Two accumulators in tensor memory (2 x 256 columns)
+// let four epilogue warps drain tile t while the MMA warp and the converters
+// already work on tile t+1.  Warps: 0 TMA producer, 1 MMA issuer, 2..9 W
+// converters, 10..13 epilogue.  The ring of stages and its barriers run on
+// across tiles; acc_full[b] / acc_empty[b] hand accumulator b between the MMA
+// warp and the epilogue warps.
+
+constexpr int kPEpiWarps = 4;
+constexpr int kPThreads = 32 * (2 + kConvWarps + kPEpiWarps);
+
+__global__ void __launch_bounds__(kPThreads, 1)
+    gemm_tc_x16_persistent_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                                  const __grid_constant__ CUtensorMap tmap_x16, const GemmCfg c) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int BN = c.BN;
+  const int NS = c.nstages;
+  const int b_bytes = BN * kARowBytes;
+  const int stage_bytes = kAOpBytes + b_bytes + kWRawBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NS * stage_bytes);
+  uint64_t* tma_full = bars;
+  uint64_t* op_full = tma_full + kX16MaxStages;
+  uint64_t* op_empty = op_full + kX16MaxStages;
+  uint64_t* acc_full = op_empty + kX16MaxStages;  // [2]
+  uint64_t* acc_empty = acc_full + 2;             // [2]
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+  float* tscale = reinterpret_cast<float*>(tmem_slot + 4);  // [2][BN]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nkb = c.K / kBK;
+  const int ntn = (c.N + kBM - 1) / kBM;
+  const int ntiles = ntn * ((c.M + BN - 1) / BN);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&tma_full[i], 1);
+      mbar_init(&op_full[i], kConvWarps);
+      mbar_init(&op_empty[i], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], kPEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0u;
+    fence_mbarrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer
+    if (lane == 0) {
+      pdl_wait();
+      int os = 0, issued = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        const int n0 = (t % ntn) * kBM, m0 = (t / ntn) * BN;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!wait_flag(&op_empty[os], ph ^ 1u, c.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + os * stage_bytes;
+          mbar_arrive_expect_tx(&tma_full[os], (uint32_t)(b_bytes + kWRawBytes));
+          tma_load_2d(st + kAOpBytes + b_bytes, &tmap_w, kb * (kBK / 4), n0, &tma_full[os]);
+          tma_load_2d(st + kAOpBytes, &tmap_x16, kb * kBK, m0, &tma_full[os]);
+          ++issued;
+          if (++os == NS) {
+            os = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        for (int g = (issued > NS ? issued - NS : 0); g < issued; ++g) {
+          const uint32_t a = smem_u32(&tma_full[g % NS]), par = (uint32_t)(g / NS) & 1u;
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait_sleep(a, par, kWaitHintNs) && globaltimer_ns() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = f16_idesc(kBM, BN);
+      int os = 0, lt = 0;
+      uint32_t par = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++lt) {
+        const int b = lt & 1;
+        if (!wait_flag(&acc_empty[b], ((uint32_t)(lt >> 1) & 1u) ^ 1u, c.err, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(b * 256);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!wait_flag(&op_full[os], par, c.err, abort_flag) || !wait_flag(&tma_full[os], par, c.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smem + os * stage_bytes);
+          const uint32_t b_base = a_base + kAOpBytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            mma_f16(d, sw128_desc(a_base + kk * 32), sw128_desc(b_base + kk * 32), idesc, (kb | kk) ? 1u : 0u);
+          mma_commit(&op_empty[os]);
+          if (++os == NS) {
+            os = 0;
+            par ^= 1u;
+          }
+        }
+        if (ok) mma_commit(&acc_full[b]);
+      }
+    }
+  } else if (warp < 2 + kConvWarps) {
+    // ---------------- W converters
+    const int ct = threadIdx.x - 64;  // 0 .. 255
+    const int r = ct >> 1, h = ct & 1;
+    int os = 0;
+    uint32_t par = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!wait_flag(&tma_full[os], par, c.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint32_t aop = smem_u32(smem + os * stage_bytes);
+        const uint2 pw = lds64(aop + kAOpBytes + b_bytes + (uint32_t)(r * 16 + h * 8));
+        uint32_t f[8];
+        unpack_word_f16(pw.x, f);
+        st_sw128(aop, r, 4 * h + 0, f[0], f[1], f[2], f[3]);
+        st_sw128(aop, r, 4 * h + 1, f[4], f[5], f[6], f[7]);
+        unpack_word_f16(pw.y, f);
+        st_sw128(aop, r, 4 * h + 2, f[0], f[1], f[2], f[3]);
+        st_sw128(aop, r, 4 * h + 3, f[4], f[5], f[6], f[7]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&op_full[os]);
+        if (++os == NS) {
+          os = 0;
+          par ^= 1u;
+        }
+      }
+    }
+  } else {
+    // ---------------- epilogue warps: tensor-memory lane quarter q = warp % 4
+    const int et = threadIdx.x - 32 * (2 + kConvWarps);  // 0 .. 127
+    const int q = warp & 3;
+    pdl_wait();
+    const float gamma = __ldg(c.gamma);
+    int lt = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
+      const int b = lt & 1;
+      const int n0 = (t % ntn) * kBM, m0 = (t / ntn) * BN;
+      float* ts = tscale + b * BN;
+      for (int j = et; j < BN; j += 32 * kPEpiWarps) {
+        const int m = m0 + j;
+        ts[j] = m < c.M ? __fdiv_rn(gamma, __ldg(c.s + m)) : 0.0f;
+      }
+      asm volatile("bar.sync 2, %0;" ::"n"(32 * kPEpiWarps) : "memory");
+      if (!wait_flag(&acc_full[b], (uint32_t)(lt >> 1) & 1u, c.err, abort_flag)) break;
+      tc_fence_after();
+      const int n = n0 + q * 32 + lane;
+      for (int j0 = 0; j0 < BN; j0 += 16) {
+        uint32_t rr[16];
+        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * 256 + j0), rr);
+        if (n < c.N) {
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int m = m0 + j0 + jj;
+            if (m < c.M) {
+              const float v = __uint_as_float(rr[jj]);
+              const int64_t o = (int64_t)m * c.N + n;
+              c.y[o] = __fmul_rn(v, ts[j0 + jj]);
+              if (c.acc) c.acc[o] = __float2int_rn(v);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[b]);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    // every MMA this thread issued has finished before tensor memory is freed
+    if (lane == 0) mma_commit(drain);
+    __syncwarp();
+    const uint32_t a = smem_u32(drain);
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait_sleep(a, 0u, kWaitHintNs) && globaltimer_ns() - t0 < kWaitLimitNs) {
+    }
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -759,6 +969,22 @@ cudaError_t launch_gemm_tc_x16(const ForwardArgs& a, const void* x16, int num_sm
   CUtensorMap tw, tx;
   if (!encode_u8_2d(&tw, a.Wp, (uint64_t)a.K / 4, (uint64_t)a.N, kBK / 4, kBM)) return cudaErrorInvalidValue;
   if (!encode_f16_2d_sw128(&tx, x16, (uint64_t)a.K, (uint64_t)a.M, (uint32_t)BN)) return cudaErrorInvalidValue;
+  const int64_t tiles = (a.N + kBM - 1) / kBM * ntiles;
+  if (tiles > num_sms && BN >= 128) {
+    // persistent: one CTA per SM, the deepest ring that fits beside [2][BN] scales
+    const size_t stage = kAOpBytes + (size_t)BN * kARowBytes + kWRawBytes;
+    const size_t fixed = 1024 + (3 * kX16MaxStages + 5) * 8 + 16 + (size_t)BN * 8;
+    int NS = (int)((kMaxDynSmem - fixed) / stage);
+    if (NS > kX16MaxStages) NS = kX16MaxStages;
+    const size_t smem = fixed + (size_t)NS * stage;
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_tc_x16_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    GemmCfg c{a.gamma, a.s, a.y, a.acc, a.err, (int)a.M, (int)a.N, (int)a.K, BN, NS, 1};
+    const int grid = (int)(tiles < num_sms ? tiles : num_sms);
+    gemm_tc_x16_persistent_kernel<<<grid, kPThreads, smem, stream>>>(tw, tx, c);
+    return cudaGetLastError();
+  }
   // Ring depth: two CTAs per SM when that still leaves >= 4 stages (small
   // token tiles: the grid then fits in fewer waves), else one CTA with the
   // deepest ring that fits.
