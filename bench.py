@@ -236,6 +236,19 @@ def run_oracle(wl, budget_s: float, steps: int | None = None, warmup: int = 0):
 
 # ---------------------------------------------------------------- GPU arm
 
+def gemm_variant(L, num_sms: int) -> str:
+    """Which forward kernel the library picks for a layer (the library's own
+    rule, restated here only to label the bench line)."""
+    if L.M <= 4 and L.K <= 32768:
+        return "gemv_kernel"
+    ntiles_m = -(-L.M // 256)
+    bn = -(-(-(-L.M // ntiles_m)) // 16) * 16
+    tiles = -(-L.N // 128) * ntiles_m
+    if tiles > num_sms and bn >= 128:
+        return "gemm_tc_x16_persistent_kernel"
+    return "gemm_tc_x16_kernel" + (" (split K over a cluster)" if tiles < num_sms else "")
+
+
 def gemv_fused_layer(L) -> bool:
     """True where bitlinear_quant_forward runs the layer as ONE kernel (the
     fused quantise + GEMV: at most 4 tokens and K <= 32768)."""
@@ -400,6 +413,7 @@ def run_gpu(args, dist, rank, world, local):
         kern_us.append(a.elapsed_time(b) * 1e3 / (3 * kchunk))
         del g
     kernel_names = ["gemv_kernel" if (L.M <= 4 and L.K <= 32768) else "gemm_tc_x16_kernel" for L in wl.layers]
+    kernel_variant = [gemm_variant(L, props.multi_processor_count) for L in wl.layers]
     kname = max(set(kernel_names), key=lambda k: sum(t for t, n in zip(kern_us, kernel_names) if n == k))
     sel = [i for i, n in enumerate(kernel_names) if n == kname]
     tot_s = sum(kern_us[i] for i in sel) * 1e-6
@@ -417,6 +431,7 @@ def run_gpu(args, dist, rank, world, local):
     roof["traffic"] = ncu_traffic(kname, args.workload) if not args.layers else None
     roof["kernel"] = kname
     roof["kernel_us"] = [round(kern_us[i], 3) for i in sel]
+    roof["variants"] = [kernel_variant[i] for i in sel]
     roof["how"] = (f"each layer's kernel replayed {3 * kchunk} times back to back from a CUDA graph over its rotating "
                    "buffers; CUDA events on the launching stream")
     if kname == "gemm_tc_x16_kernel":

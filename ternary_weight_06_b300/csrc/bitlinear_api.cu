@@ -174,8 +174,8 @@ bl_status bitlinear_quant_forward_ws(const uint8_t* W_packed, const float* gamma
   if (M <= bl::kGemvMaxTokens && K <= bl::kGemvMaxK)
     return from_cuda(bl::launch_gemv_fused(a, X, dtype == BL_BF16, x_q, s, (flags & BITLINEAR_WEIGHTS_RESIDENT) != 0,
                                            d.num_sms, stream));
-  if (cudaError_t e = bl::launch_quant_act(X, dtype == BL_BF16, M, K, x_q, s, stream)) return from_cuda(e);
-  if (cudaError_t e = bl::launch_x16_prepass(x_q, M, K, workspace, d.num_sms, stream)) return from_cuda(e);
+  if (cudaError_t e = bl::launch_quant_act_x16(X, dtype == BL_BF16, M, K, x_q, s, workspace, stream))
+    return from_cuda(e);
   return from_cuda(bl::launch_gemm_tc_x16(a, workspace, d.num_sms, stream));
 }
 

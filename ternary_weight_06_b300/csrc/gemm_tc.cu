@@ -141,15 +141,6 @@ __device__ __forceinline__ bool wait_flag(uint64_t* bar, uint32_t parity, uint32
 
 // ---------------------------------------------------------------- operand expansion
 
-// Two fp16 of 1024 + byte, from bytes b0, b1 of w (selector 0x4140) or b2, b3 (0x4342).
-__device__ __forceinline__ uint32_t bytes_to_h2(uint32_t w, uint32_t sel) { return __byte_perm(w, 0x64646464u, sel); }
-
-__device__ __forceinline__ uint32_t h2_sub(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
 // 16 codes (one 32-bit packed word) -> 16 fp16 in order p = 4i + j (k = 4j + i), values c - 1.
 __device__ __forceinline__ void unpack_word_f16(uint32_t P, uint32_t* h /* 8 words */) {
   const uint32_t k1025 = 0x64016401u;  // fp16 (1025, 1025)
@@ -158,21 +149,6 @@ __device__ __forceinline__ void unpack_word_f16(uint32_t P, uint32_t* h /* 8 wor
     const uint32_t S = (P >> (2 * i)) & 0x03030303u;
     h[2 * i] = h2_sub(bytes_to_h2(S, 0x4140), k1025);
     h[2 * i + 1] = h2_sub(bytes_to_h2(S, 0x4342), k1025);
-  }
-}
-
-// 16 int8 activations (natural order, 4 words) -> 16 fp16 in order p = 4i + j.
-__device__ __forceinline__ void convert_x16_f16(uint4 v, uint32_t* h /* 8 words */) {
-  const uint32_t x0 = v.x ^ 0x80808080u, x1 = v.y ^ 0x80808080u, x2 = v.z ^ 0x80808080u, x3 = v.w ^ 0x80808080u;
-  const uint32_t t0 = __byte_perm(x0, x1, 0x5140), t1 = __byte_perm(x2, x3, 0x5140);
-  const uint32_t t2 = __byte_perm(x0, x1, 0x7362), t3 = __byte_perm(x2, x3, 0x7362);
-  const uint32_t o[4] = {__byte_perm(t0, t1, 0x5410), __byte_perm(t0, t1, 0x7632), __byte_perm(t2, t3, 0x5410),
-                         __byte_perm(t2, t3, 0x7632)};
-  const uint32_t k1152 = 0x64806480u;  // fp16 (1152, 1152): undoes the +128 bias and the 1024 offset
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    h[2 * i] = h2_sub(bytes_to_h2(o[i], 0x4140), k1152);
-    h[2 * i + 1] = h2_sub(bytes_to_h2(o[i], 0x4342), k1152);
   }
 }
 

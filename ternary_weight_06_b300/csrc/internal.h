@@ -24,6 +24,11 @@ cudaError_t launch_pack(const float* W, uint64_t n, float eps, uint8_t* Wp, floa
 cudaError_t launch_quant_act(const void* X, bool bf16, int64_t M, int64_t K, int8_t* xq, float* s,
                              cudaStream_t stream);
 
+// The same quantisation, also writing the GEMM's fp16 activation operand
+// (gemm_x16_workspace_bytes(M, K) bytes at x16, 16-byte aligned); K % 16 == 0.
+cudaError_t launch_quant_act_x16(const void* X, bool bf16, int64_t M, int64_t K, int8_t* xq, float* s, void* x16,
+                                 cudaStream_t stream);
+
 struct ForwardArgs {
   const uint8_t* Wp;
   const float* gamma;

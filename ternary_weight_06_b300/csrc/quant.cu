@@ -32,9 +32,10 @@ __device__ __forceinline__ uint32_t q8(float x, float s) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-template <bool BF16>
+template <bool BF16, bool X16>
 __global__ void __launch_bounds__(1024) quant_act_kernel(const void* __restrict__ X, int64_t K, bool vec,
-                                                         int8_t* __restrict__ xq, float* __restrict__ s) {
+                                                         int8_t* __restrict__ xq, float* __restrict__ s,
+                                                         uint4* __restrict__ x16) {
   constexpr int kEsize = BF16 ? 2 : 4;
   const int64_t m = blockIdx.x;
   const char* row = static_cast<const char*>(X) + m * K * kEsize;
@@ -76,7 +77,36 @@ __global__ void __launch_bounds__(1024) quant_act_kernel(const void* __restrict_
   const float sm = __fdiv_rn(127.0f, a);
   if (tid == 0) s[m] = sm;
 
-  if (vec) {
+  if (X16) {
+    // groups of 16 activations: x_q (natural order) and the GEMM's fp16 operand
+    // (order p = 4i + j within the group); K % 16 == 0
+    const uint4* r4 = reinterpret_cast<const uint4*>(row);
+    uint4* xo = x16 + m * (K / 8);
+    for (int64_t g = tid; g < K / 16; g += nt) {
+      uint32_t nat[4];
+      if (BF16) {
+        const uint4 a = __ldg(r4 + 2 * g), b = __ldg(r4 + 2 * g + 1);
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          nat[i] = q8(bf16_lo(w[2 * i]), sm) | (q8(bf16_hi(w[2 * i]), sm) << 8) | (q8(bf16_lo(w[2 * i + 1]), sm) << 16) |
+                   (q8(bf16_hi(w[2 * i + 1]), sm) << 24);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 v = __ldg(r4 + 4 * g + i);
+          nat[i] = q8(__uint_as_float(v.x), sm) | (q8(__uint_as_float(v.y), sm) << 8) |
+                   (q8(__uint_as_float(v.z), sm) << 16) | (q8(__uint_as_float(v.w), sm) << 24);
+        }
+      }
+      const uint4 q4 = make_uint4(nat[0], nat[1], nat[2], nat[3]);
+      reinterpret_cast<uint4*>(out)[g] = q4;
+      uint32_t h[8];
+      convert_x16_f16(q4, h);
+      xo[2 * g] = make_uint4(h[0], h[1], h[2], h[3]);
+      xo[2 * g + 1] = make_uint4(h[4], h[5], h[6], h[7]);
+    }
+  } else if (vec) {
     const uint4* r4 = reinterpret_cast<const uint4*>(row);
     const int64_t nch = K * kEsize / 16;
     for (int64_t c = tid; c < nch; c += nt) {
@@ -113,8 +143,20 @@ cudaError_t launch_quant_act(const void* X, bool bf16, int64_t M, int64_t K, int
   int threads = (int)((work + 31) / 32 * 32);
   if (threads > 1024) threads = 1024;
   if (threads < 32) threads = 32;
-  if (bf16) quant_act_kernel<true><<<(unsigned)M, threads, 0, stream>>>(X, K, vec, xq, s);
-  else quant_act_kernel<false><<<(unsigned)M, threads, 0, stream>>>(X, K, vec, xq, s);
+  if (bf16) quant_act_kernel<true, false><<<(unsigned)M, threads, 0, stream>>>(X, K, vec, xq, s, nullptr);
+  else quant_act_kernel<false, false><<<(unsigned)M, threads, 0, stream>>>(X, K, vec, xq, s, nullptr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_act_x16(const void* X, bool bf16, int64_t M, int64_t K, int8_t* xq, float* s, void* x16,
+                                 cudaStream_t stream) {
+  // one 16-element group per thread in the second pass (K % 16 == 0)
+  int threads = (int)((K / 16 + 31) / 32 * 32);
+  if (threads > 1024) threads = 1024;
+  if (threads < 64) threads = 64;
+  uint4* o = static_cast<uint4*>(x16);
+  if (bf16) quant_act_kernel<true, true><<<(unsigned)M, threads, 0, stream>>>(X, K, true, xq, s, o);
+  else quant_act_kernel<false, true><<<(unsigned)M, threads, 0, stream>>>(X, K, true, xq, s, o);
   return cudaGetLastError();
 }
 
