@@ -434,3 +434,17 @@ def test_quant_forward_ws_edge_shapes(bl, dtype, M, N, K):
     X = X.to(dtype)
     fused_case(bl, oracle.pack(q), np.float32(0.031), X, K, sample_rows(M, 16, seed=M),
                f"ws fused M={M} N={N} K={K}", ws=True)
+
+
+@pytest.mark.parametrize("M,N,K", [(333, 19000, 192), (130, 19201, 320), (1000, 9000, 128)])
+def test_forward_ws_persistent_grid_exhaustive(bl, M, N, K):
+    """Shapes with more output tiles than SMs (the persistent tensor-core
+    kernel, accumulators double-buffered in tensor memory), ragged in M and N,
+    checked on every output against the oracle."""
+    rng = np.random.default_rng(M + N + K)
+    q = rng.integers(-1, 2, size=(N, K)).astype(np.int8)
+    xq = rng.integers(-128, 128, size=(M, K)).astype(np.int8)
+    xq[-1, :] = 127
+    s = rng.uniform(0.5, 300, size=M).astype(np.float32)
+    forward_case(bl, oracle.pack(q), np.float32(0.0123), xq, s, K, np.arange(M), f"persistent M={M} N={N} K={K}",
+                 ws=True)
