@@ -83,6 +83,30 @@ struct AbsmeanAcc {
     if (hi) atomicAdd(&sb[G], hi);
     if (G >= 1u && lo) atomicAdd(&sb[G - 1u], lo);
   }
+
+  // Warp-wide flush: where every lane holds the same top group G (the common
+  // case: a weight matrix's magnitudes span a few binades), the register sums
+  // are added across the warp first and one lane issues the two atomics, so a
+  // CTA's threads do not serialise on the same two shared buckets.  Integer
+  // sums, so the result is the same in any order.  All 32 lanes must call it.
+  __device__ __forceinline__ void flush_warp(unsigned long long* sb) {
+    int same = 0;
+    __match_all_sync(0xffffffffu, G, &same);
+    if (!same) {
+      flush(sb);
+      return;
+    }
+    unsigned long long h = hi, l = lo;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      h += __shfl_xor_sync(0xffffffffu, h, off);
+      l += __shfl_xor_sync(0xffffffffu, l, off);
+    }
+    if ((threadIdx.x & 31u) == 0) {
+      if (h) atomicAdd(&sb[G], h);
+      if (G >= 1u && l) atomicAdd(&sb[G - 1u], l);
+    }
+  }
 };
 
 constexpr int kPackThreads = 256;
@@ -106,7 +130,7 @@ __global__ void __launch_bounds__(kPackThreads) absmean_hist_kernel(const float4
     for (int u = 0; u < 4; ++u) acc.add4(v[u], sb);
   }
   for (; i < n4; i += stride) acc.add4(__ldg(W4 + i), sb);
-  acc.flush(sb);
+  acc.flush_warp(sb);
   if (acc.nonfinite) snf = 1;
   __syncthreads();
   if (threadIdx.x < 32 && sb[threadIdx.x]) atomicAdd(&ws->bucket[threadIdx.x], sb[threadIdx.x]);
