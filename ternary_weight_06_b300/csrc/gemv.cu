@@ -48,18 +48,12 @@
 namespace bl {
 namespace {
 
-constexpr int kStages = 4;
-constexpr int kStageBytesTarget = 16384;
+constexpr int kStages = 3;
+constexpr int kStageBytesTarget = 32768;
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 constexpr int kCtasPerSm = 2;  // CTAs of one launch per SM (a third slot stays free for the next launch)
 constexpr float kActClampEps = 1e-5f;
-
-// rows each warp takes per iteration, by tokens per launch
-template <int MT>
-struct RowsPerIter {
-  static constexpr int value = MT == 1 ? 2 : 1;
-};
 
 struct GemvCfg {
   const uint8_t* Wp;
@@ -204,9 +198,9 @@ __device__ __forceinline__ void quant16(const void* xrow, int x_bf16, int64_t k0
   }
 }
 
-template <int MT, int J, bool FUSED>
+// RI: rows each warp takes per iteration (its butterfly reduces RI * MT values at once).
+template <int MT, int J, int RI, bool FUSED>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm + 1) gemv_kernel(const GemvCfg c) {
-  constexpr int RI = RowsPerIter<MT>::value;
   constexpr int V = RI * MT;
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -460,7 +454,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm + 1) gemv_kernel(const Ge
 
 template <int MT, int J, bool FUSED>
 cudaError_t launch_one(const GemvCfg& c, int grid, size_t smem, bool pdl, cudaStream_t stream) {
-  auto kern = gemv_kernel<MT, J, FUSED>;
+  // four rows per warp iteration where a stage holds enough rows for every row
+  // group and the activation registers leave room (J <= 4)
+  const bool four = MT == 1 && J <= 4 && c.rows_per_stage >= 4 * (kConsumerWarps / c.kw);
+  auto kern = four ? gemv_kernel<MT, J, (MT == 1 ? 4 : 1), FUSED> : gemv_kernel<MT, J, (MT == 1 ? 2 : 1), FUSED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -542,8 +539,9 @@ cudaError_t run(const ForwardArgs& a, const void* X, bool x_bf16, int8_t* xq_out
   while (mt > 1 && (c.words_per_row + 32 * kConsumerWarps - 1) / (32 * kConsumerWarps) > jmax_for(mt)) mt /= 2;
   int kw = 1;
   while (kw < kConsumerWarps && (c.words_per_row + 32 * kw - 1) / (32 * kw) > jmax_for(mt)) kw *= 2;
-  // the one-pass fused prologue wants at most 4 words per lane
-  if (fused && x_bf16 && mt == 1)
+  // one token: at most 4 words per lane where possible (the one-pass fused
+  // prologue needs it, and four rows per iteration fit the registers)
+  if (mt == 1)
     while (kw < kConsumerWarps && (c.words_per_row + 32 * kw - 1) / (32 * kw) > 4) kw *= 2;
   c.kw = kw;
   c.words_per_warp = (c.words_per_row + c.kw - 1) / c.kw;
