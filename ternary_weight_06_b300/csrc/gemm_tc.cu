@@ -568,25 +568,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     cluster_sync_all();
     if (epi) {
-      const uint32_t rank = cluster_ctarank();
-      const int n = n0 + f;
-      // 16-token chunks: chunk index c16 = j0/16; rank takes c16 % S == rank, the two
-      // warps of a lane quarter alternate over those chunks
-      int seq = 0;
-      for (int j0 = 0; j0 < BN; j0 += 16) {
-        if ((j0 / 16) % S != (int)rank) continue;
-        if ((seq++ & 1) != ((warp - 2) >> 2)) continue;
-        if (n >= c.N) continue;
-#pragma unroll 4
-        for (int jj = 0; jj < 16; ++jj) {
-          const int m = m0 + j0 + jj;
-          if (m >= c.M) break;
-          const uint32_t off = (uint32_t)(((j0 + jj) * kBM + f) * 4);
-          float v = 0.0f;
-          for (int pr = 0; pr < S; ++pr) v += ld_cluster_f32(map_to_rank(R + off, (uint32_t)pr));
-          const int64_t o = (int64_t)m * c.N + n;
-          c.y[o] = __fmul_rn(v, tscale[j0 + jj]);
-          if (c.acc) c.acc[o] = __float2int_rn(v);
+      // Units of work: (16-token chunk, lane quarter) pairs, dealt round-robin to
+      // the S ranks; the two warps of a quarter take 8 tokens each, and a
+      // thread's 8 reads from one peer are issued together.
+      const int rank = (int)cluster_ctarank();
+      const int h = (warp - 2) >> 2;
+      const int npairs = (BN / 16) * 4;
+      for (int pair = rank; pair < npairs; pair += S) {
+        if ((pair & 3) != q) continue;
+        const int j0 = (pair >> 2) * 16 + 8 * h;
+        const int n = n0 + f;
+        float v[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) v[jj] = 0.0f;
+        for (int pr = 0; pr < S; ++pr) {
+          const uint32_t base = map_to_rank(R + (uint32_t)((j0 * kBM + f) * 4), (uint32_t)pr);
+          float w[8];
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) w[jj] = ld_cluster_f32(base + (uint32_t)(jj * kBM * 4));
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) v[jj] += w[jj];
+        }
+        if (n < c.N) {
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const int m = m0 + j0 + jj;
+            if (m < c.M) {
+              const int64_t o = (int64_t)m * c.N + n;
+              c.y[o] = __fmul_rn(v[jj], tscale[j0 + jj]);
+              if (c.acc) c.acc[o] = __float2int_rn(v[jj]);
+            }
+          }
         }
       }
     }
