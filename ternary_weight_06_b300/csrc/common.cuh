@@ -107,6 +107,16 @@ __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepc
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 
+// Sets a kernel's dynamic shared memory limit and asks for the largest
+// shared-memory carveout, so that as many CTAs as the shared memory allows
+// are resident per SM (the default carveout can leave room for only one).
+template <typename Kernel>
+inline cudaError_t set_smem_attrs(Kernel kern, size_t smem_bytes) {
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+}
+
 // ---- exact int8 -> fp16 operand expansion (shared by the GEMM and the
 // activation quantisation, which can write the GEMM's operand directly)
 

@@ -458,7 +458,7 @@ cudaError_t launch_one(const GemvCfg& c, int grid, size_t smem, bool pdl, cudaSt
   // group and the activation registers leave room (J <= 4)
   const bool four = MT == 1 && J <= 4 && c.rows_per_stage >= 4 * (kConsumerWarps / c.kw);
   auto kern = four ? gemv_kernel<MT, J, (MT == 1 ? 4 : 1), FUSED> : gemv_kernel<MT, J, (MT == 1 ? 2 : 1), FUSED>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = set_smem_attrs(kern, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
