@@ -176,6 +176,14 @@ bl_status bitlinear_forward(const uint8_t* W_packed, const float* gamma, const i
  * dependent launch); activations are still read only after it completes. */
 #define BITLINEAR_WEIGHTS_RESIDENT 1u
 
+/* Test hook of bitlinear_quant_forward(_ws), not for production use: on the
+ * one-kernel path (M <= 4, K <= 32768) the kernel issues no weight copies, so
+ * its bounded waits run out (after about two seconds); it then records
+ * BL_ERR_TIMEOUT in the device error word, writes no y, and exits cleanly.
+ * Lets a test exercise the timeout path without faulting or hanging the GPU.
+ * Rejected with BL_ERR_INVALID_ARG on the multi-kernel path. */
+#define BITLINEAR_TEST_STALL 0x80000000u
+
 /*
  * bitlinear_quant_forward -- bitlinear_quant_act followed by
  * bitlinear_forward, as one call: per-token absmax int8 quantisation of X

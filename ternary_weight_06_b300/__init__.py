@@ -38,6 +38,7 @@ __all__ = [
     "bitlinear_check_device_error",
     "bitlinear_status_string",
     "BITLINEAR_WEIGHTS_RESIDENT",
+    "BITLINEAR_TEST_STALL",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -47,6 +48,7 @@ BL_OK, BL_ERR_INVALID_ARG, BL_ERR_UNSUPPORTED_SHAPE, BL_ERR_MISALIGNED, BL_ERR_W
     BL_ERR_TIMEOUT = range(7)
 BL_F32, BL_BF16 = 0, 1
 BITLINEAR_WEIGHTS_RESIDENT = 1
+BITLINEAR_TEST_STALL = 0x80000000  # test hook: the one-kernel path's bounded waits run out
 
 EXPORTED_SYMBOLS = (
     "bitlinear_pack_workspace_bytes",

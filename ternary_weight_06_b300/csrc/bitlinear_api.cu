@@ -103,7 +103,7 @@ bl_status bitlinear_quant_forward(const uint8_t* W_packed, const float* gamma, c
   if (!W_packed || !gamma || !X || !y || !x_q || !s) return BL_ERR_INVALID_ARG;
   if (M < 1 || N < 1 || K < 1) return BL_ERR_INVALID_ARG;
   if (dtype != BL_F32 && dtype != BL_BF16) return BL_ERR_INVALID_ARG;
-  if (flags & ~BITLINEAR_WEIGHTS_RESIDENT) return BL_ERR_INVALID_ARG;
+  if (flags & ~(BITLINEAR_WEIGHTS_RESIDENT | BITLINEAR_TEST_STALL)) return BL_ERR_INVALID_ARG;
   if (K % 64 != 0 || K > BITLINEAR_MAX_K || M > INT32_MAX || N > INT32_MAX) return BL_ERR_UNSUPPORTED_SHAPE;
   if (!aligned(W_packed, 16) || !aligned(X, 16) || !aligned(x_q, 16) || !aligned(y, 16) || !aligned(gamma, 4) ||
       !aligned(s, 4) || (acc && !aligned(acc, 16)))
@@ -111,9 +111,11 @@ bl_status bitlinear_quant_forward(const uint8_t* W_packed, const float* gamma, c
   DeviceInfo d;
   if (bl_status st = device_info(&d)) return st;
   bl::ForwardArgs a{W_packed, gamma, x_q, s, M, N, K, y, acc, d.err};
+  const bool stall = (flags & BITLINEAR_TEST_STALL) != 0;
   if (M <= bl::kGemvMaxTokens && K <= bl::kGemvMaxK)
     return from_cuda(bl::launch_gemv_fused(a, X, dtype == BL_BF16, x_q, s, (flags & BITLINEAR_WEIGHTS_RESIDENT) != 0,
-                                           d.num_sms, stream));
+                                           stall, d.num_sms, stream));
+  if (stall) return BL_ERR_INVALID_ARG;  // the test hook exists on the one-kernel path only
   if (cudaError_t e = bl::launch_quant_act(X, dtype == BL_BF16, M, K, x_q, s, stream)) return from_cuda(e);
   return from_cuda(bl::launch_gemm_tc(a, d.num_sms, stream));
 }
@@ -162,7 +164,7 @@ bl_status bitlinear_quant_forward_ws(const uint8_t* W_packed, const float* gamma
   if (!W_packed || !gamma || !X || !y || !x_q || !s) return BL_ERR_INVALID_ARG;
   if (M < 1 || N < 1 || K < 1) return BL_ERR_INVALID_ARG;
   if (dtype != BL_F32 && dtype != BL_BF16) return BL_ERR_INVALID_ARG;
-  if (flags & ~BITLINEAR_WEIGHTS_RESIDENT) return BL_ERR_INVALID_ARG;
+  if (flags & ~(BITLINEAR_WEIGHTS_RESIDENT | BITLINEAR_TEST_STALL)) return BL_ERR_INVALID_ARG;
   if (K % 64 != 0 || K > BITLINEAR_MAX_K || M > INT32_MAX || N > INT32_MAX) return BL_ERR_UNSUPPORTED_SHAPE;
   if (!aligned(W_packed, 16) || !aligned(X, 16) || !aligned(x_q, 16) || !aligned(y, 16) || !aligned(gamma, 4) ||
       !aligned(s, 4) || (acc && !aligned(acc, 16)))
@@ -171,9 +173,11 @@ bl_status bitlinear_quant_forward_ws(const uint8_t* W_packed, const float* gamma
   DeviceInfo d;
   if (bl_status st = device_info(&d)) return st;
   bl::ForwardArgs a{W_packed, gamma, x_q, s, M, N, K, y, acc, d.err};
+  const bool stall = (flags & BITLINEAR_TEST_STALL) != 0;
   if (M <= bl::kGemvMaxTokens && K <= bl::kGemvMaxK)
     return from_cuda(bl::launch_gemv_fused(a, X, dtype == BL_BF16, x_q, s, (flags & BITLINEAR_WEIGHTS_RESIDENT) != 0,
-                                           d.num_sms, stream));
+                                           stall, d.num_sms, stream));
+  if (stall) return BL_ERR_INVALID_ARG;  // the test hook exists on the one-kernel path only
   if (cudaError_t e = bl::launch_quant_act_x16(X, dtype == BL_BF16, M, K, x_q, s, workspace, stream))
     return from_cuda(e);
   return from_cuda(bl::launch_gemm_tc_x16(a, workspace, d.num_sms, stream));

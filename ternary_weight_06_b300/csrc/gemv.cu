@@ -71,6 +71,7 @@ struct GemvCfg {
   int x_bf16;
   int rows_per_cta, rows_per_stage, row_bytes, nslots;  // nslots <= kStages ring slots
   int kw, words_per_row, words_per_warp;
+  int test_stall;  // test hook: the producer issues no copies, so the bounded waits expire
 };
 
 __device__ __forceinline__ void transpose4x4(uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3, uint32_t* o) {
@@ -233,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm + 1) gemv_kernel(const Ge
     // ---------------- producer: weights only, so it may run ahead of griddepcontrol.wait
     if (lane == 0) {
       int issued = 0;
-      for (int st = 0; st < nstages; ++st) {
+      for (int st = 0; st < (c.test_stall ? 0 : nstages); ++st) {
         const int slot = st % NS;
         if (st >= NS && !wait_or_abort(&empty[slot], (uint32_t)((st / NS) - 1) & 1u, c.err, kErrGemvEmptyWait,
                                        abort_flag))
@@ -505,8 +506,9 @@ cudaError_t dispatch_j(const GemvCfg& c, int J, int grid, size_t smem, bool pdl,
 }
 
 cudaError_t run(const ForwardArgs& a, const void* X, bool x_bf16, int8_t* xq_out, float* s_out, bool fused,
-                bool pdl, int num_sms, cudaStream_t stream) {
+                bool pdl, bool test_stall, int num_sms, cudaStream_t stream) {
   GemvCfg c{};
+  c.test_stall = test_stall ? 1 : 0;
   c.Wp = a.Wp;
   c.gamma = a.gamma;
   c.xq_in = a.xq;
@@ -571,12 +573,12 @@ cudaError_t run(const ForwardArgs& a, const void* X, bool x_bf16, int8_t* xq_out
 }  // namespace
 
 cudaError_t launch_gemv(const ForwardArgs& a, int num_sms, cudaStream_t stream) {
-  return run(a, nullptr, false, nullptr, nullptr, false, false, num_sms, stream);
+  return run(a, nullptr, false, nullptr, nullptr, false, false, false, num_sms, stream);
 }
 
 cudaError_t launch_gemv_fused(const ForwardArgs& a, const void* X, bool x_bf16, int8_t* xq_out, float* s_out,
-                              bool pdl, int num_sms, cudaStream_t stream) {
-  return run(a, X, x_bf16, xq_out, s_out, true, pdl, num_sms, stream);
+                              bool pdl, bool test_stall, int num_sms, cudaStream_t stream) {
+  return run(a, X, x_bf16, xq_out, s_out, true, pdl, test_stall, num_sms, stream);
 }
 
 }  // namespace bl

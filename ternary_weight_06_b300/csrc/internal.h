@@ -47,7 +47,7 @@ cudaError_t launch_gemv(const ForwardArgs& a, int num_sms, cudaStream_t stream);
 // (bf16 or fp32) instead of x_q / s; the first CTA writes x_q and s out.
 // With pdl, launched as a programmatic dependent of the preceding kernel.
 cudaError_t launch_gemv_fused(const ForwardArgs& a, const void* X, bool x_bf16, int8_t* xq_out, float* s_out,
-                              bool pdl, int num_sms, cudaStream_t stream);
+                              bool pdl, bool test_stall, int num_sms, cudaStream_t stream);
 
 constexpr int64_t kGemvMaxTokens = 4;
 constexpr int64_t kGemvMaxK = 32768;
