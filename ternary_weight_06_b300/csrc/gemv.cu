@@ -525,7 +525,12 @@ cudaError_t run(const ForwardArgs& a, const void* X, bool x_bf16, int8_t* xq_out
   c.row_bytes = (int)(a.K / 4);
   c.words_per_row = (int)(a.K / 16);
 
-  const int64_t max_grid = (int64_t)num_sms * kCtasPerSm;
+  // CTAs per SM: two, except on the fused path when one CTA per SM still gets
+  // its whole share of the weights in a single stage (decode-sized matrices):
+  // there every CTA repeats the activation quantisation, and fewer CTAs finish
+  // sooner (measured on B300).
+  const bool small = (int64_t)a.N * c.row_bytes <= (int64_t)num_sms * kStageBytesTarget;
+  const int64_t max_grid = (int64_t)num_sms * ((fused && small) ? 1 : kCtasPerSm);
   int grid = (int)(a.N < max_grid ? a.N : max_grid);
   c.rows_per_cta = (int)((a.N + grid - 1) / grid);
   grid = (int)((a.N + c.rows_per_cta - 1) / c.rows_per_cta);
