@@ -622,13 +622,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 // One CTA per SM walks the output tiles t = blockIdx.x, blockIdx.x + gridDim.x,
 // ... (feature tiles fastest, so CTAs running at the same time share the
 // activation tile in L2).  Two accumulators in tensor memory (2 x 256 columns)
-// let four epilogue warps drain tile t while the MMA warp and the converters
+// let eight epilogue warps drain tile t while the MMA warp and the converters
 // already work on tile t+1.  Warps: 0 TMA producer, 1 MMA issuer, 2..9 W
-// converters, 10..13 epilogue.  The ring of stages and its barriers run on
+// converters, 10..17 epilogue (two per tensor-memory lane quarter).  The ring of stages and its barriers run on
 // across tiles; acc_full[b] / acc_empty[b] hand accumulator b between the MMA
 // warp and the epilogue warps.
 
-constexpr int kPEpiWarps = 4;
+constexpr int kPEpiWarps = 8;  // two per tensor-memory lane quarter
 constexpr int kPThreads = 32 * (2 + kConvWarps + kPEpiWarps);
 
 __global__ void __launch_bounds__(kPThreads, 1)
@@ -792,7 +792,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
       if (!wait_flag(&acc_full[b], (uint32_t)(lt >> 1) & 1u, c.err, abort_flag)) break;
       tc_fence_after();
       const int n = n0 + q * 32 + lane;
-      for (int j0 = 0; j0 < BN; j0 += 16) {
+      // the two warps of a lane quarter take alternate 16-token chunks
+      for (int j0 = ((warp - (2 + kConvWarps)) >> 2) * 16; j0 < BN; j0 += 32) {
         uint32_t rr[16];
         tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * 256 + j0), rr);
         if (n < c.N) {
