@@ -392,6 +392,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm + 1) gemv_kernel(const Ge
     }
   }
 
+  const int lane_off = 4 * (wbeg + lane);  // byte offset of this lane's first word in a row
   const bool writer = reduce_writer<V>(lane);
   const int widx = reduce_index<V>(lane);
   const int w_rr = widx / MT, w_t = widx % MT;
@@ -411,22 +412,26 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm + 1) gemv_kernel(const Ge
 #pragma unroll
             for (int i = 0; i < 4; ++i) a[rr][t][i] = 0;
 #pragma unroll
+        // one pointer per row (rows past the stage's last valid row read that
+        // row again; their sums are discarded), words at immediate offsets.
+        // Words past this lane's K slice multiply activations held as zero,
+        // and the allocation has slack for reads past the end of a row.
+        const uint8_t* rp[RI];
+#pragma unroll
+        for (int rr = 0; rr < RI; ++rr) rp[rr] = base + min(r0 + rr, rows - 1) * c.row_bytes + lane_off;
+#pragma unroll
         for (int j = 0; j < J; ++j) {
-          const int w = wbeg + lane + 32 * j;
-          if (w < wend) {
-            uint32_t P[RI];
+          uint32_t P[RI];
 #pragma unroll
-            for (int rr = 0; rr < RI; ++rr)
-              P[rr] = (r0 + rr < rows) ? reinterpret_cast<const uint32_t*>(base + (r0 + rr) * c.row_bytes)[w] : 0u;
+          for (int rr = 0; rr < RI; ++rr) P[rr] = *reinterpret_cast<const uint32_t*>(rp[rr] + 128 * j);
 #pragma unroll
-            for (int rr = 0; rr < RI; ++rr)
+          for (int rr = 0; rr < RI; ++rr)
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const uint32_t m = P[rr] & (0x03030303u << (2 * i));
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t m = P[rr] & (0x03030303u << (2 * i));
 #pragma unroll
-                for (int t = 0; t < MT; ++t) a[rr][t][i] = dp4a_us(m, xr[j][i][t], a[rr][t][i]);
-              }
-          }
+              for (int t = 0; t < MT; ++t) a[rr][t][i] = dp4a_us(m, xr[j][i][t], a[rr][t][i]);
+            }
         }
         int32_t v[V];
 #pragma unroll
@@ -554,8 +559,10 @@ cudaError_t run(const ForwardArgs& a, const void* X, bool x_bf16, int8_t* xq_out
   c.words_per_warp = (c.words_per_row + c.kw - 1) / c.kw;
   const int J = (c.words_per_warp + 31) / 32;
   if (J > jmax_for(mt)) return cudaErrorInvalidValue;  // K beyond the GEMV's register budget
+  // slack: a lane may read up to 32 * J * kw words past the end of the last row
+  const size_t slack = (size_t)128 * J * c.kw;
   const size_t smem = (size_t)c.nslots * c.rows_per_stage * c.row_bytes + 2 * kStages * sizeof(uint64_t) +
-                      (size_t)c.rows_per_cta * mt * sizeof(int32_t) + (kConsumerWarps + 1) * mt * 4 + 16;
+                      (size_t)c.rows_per_cta * mt * sizeof(int32_t) + (kConsumerWarps + 1) * mt * 4 + 16 + slack;
 
   for (int64_t t0 = 0; t0 < a.M; t0 += mt) {
     c.tok0 = (int)t0;
