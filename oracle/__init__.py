@@ -61,6 +61,8 @@ def _load():
         lib.oracle_quant_act.argtypes = [P, i64, i64, ctypes.c_float, P, P]
         lib.oracle_matmul_int.argtypes = [P, P, i64, i64, i64, P]
         lib.oracle_dequant.argtypes = [P, ctypes.c_float, P, i64, i64, P]
+        lib.oracle_rmsnorm_quant_act.argtypes = [P, i64, i64, P, ctypes.c_float, ctypes.c_float, P, P]
+        lib.oracle_relu2.argtypes = [P, i64]
         lib.oracle_forward.argtypes = [P, ctypes.c_float, P, P, i64, i64, i64, P, P]
         lib.oracle_forward.restype = i64
         _lib = lib
@@ -135,6 +137,28 @@ def quant_act(X: np.ndarray, clamp_eps=ACT_CLAMP_EPS) -> tuple[np.ndarray, np.nd
     s = np.empty((M,), dtype=np.float32)
     _load().oracle_quant_act(_p(X), M, K, float(np.float32(clamp_eps)), _p(xq), _p(s))
     return xq, s
+
+
+def rmsnorm_quant_act(X: np.ndarray, gain=None, eps=np.float32(1e-5), clamp_eps=ACT_CLAMP_EPS):
+    """Sub-layer RMS normalisation folded into the absmax quantisation (reading
+    R9): x_q = quant_act(X * gain), s = s(X * gain) * sqrt(mean(X^2) + eps)."""
+    X = _c(X, np.float32)
+    M, K = X.shape
+    g = None if gain is None else _c(gain, np.float32)
+    if g is not None and g.shape != (K,):
+        raise ValueError("gain must have K entries")
+    xq = np.empty((M, K), dtype=np.int8)
+    s = np.empty((M,), dtype=np.float32)
+    _load().oracle_rmsnorm_quant_act(_p(X), M, K, None if g is None else _p(g), float(np.float32(eps)),
+                                     float(np.float32(clamp_eps)), _p(xq), _p(s))
+    return xq, s
+
+
+def relu2(y: np.ndarray) -> np.ndarray:
+    """Squared ReLU, fp32(max(y, 0)^2) (reading R10).  Returns a new array."""
+    out = _c(y, np.float32).copy()
+    _load().oracle_relu2(_p(out), out.size)
+    return out
 
 
 def matmul_int(q: np.ndarray, x_q: np.ndarray) -> np.ndarray:

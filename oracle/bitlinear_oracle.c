@@ -36,6 +36,10 @@
  *   R5  x * s is one fp32 multiplication (RNE), then round-half-to-even.
  *   R6  dequant is t = fp32(gamma / s[m]) followed by y = fp32(fp32(acc) * t);
  *       fp32(acc) is exact because |acc| <= 127*K < 2^24.
+ *   R9  the sub-layer norm ahead of a BitLinear is RMS normalisation with an
+ *       optional per-channel gain; it leaves x_q = quant(x * g) and scales s
+ *       by sqrt(mean(x^2) + eps) (see the function).
+ *   R10 squared ReLU on the output is fp32(max(y,0) * max(y,0)).
  *
  * Build: plain C11, -O2 -ffp-contract=off, no fast-math (so every float
  * operation is a single IEEE-754 binary32 operation with RNE).
@@ -233,6 +237,45 @@ void oracle_quant_act(const float* X, int64_t M, int64_t K, float clamp_eps, int
       if (r < -128.0f) r = -128.0f;
       x_q[m * K + k] = (int8_t)r;
     }
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* R9: sub-layer RMS normalisation ahead of the activation quantisation.     */
+/* The transcript names a "sub-layer norm" in the BitNet b1.58 2B4T block    */
+/* (paragraph after the poker-chip analogy); its formula is not on the       */
+/* pages.  Reading: x_n = x * g / sqrt(mean(x^2) + eps) per token, g an       */
+/* optional per-channel gain.  The per-token factor 1/sqrt(...) does not     */
+/* change the absmax codes (absmax quantisation is invariant to a positive   */
+/* per-token scale), so x_q = quant_act(x * g) exactly and only the scale    */
+/* changes: s = s(x * g) * sqrt(mean(x^2) + eps).  mean(x^2) is formed in    */
+/* double, in index order, and s is rounded once to fp32.                    */
+/* ------------------------------------------------------------------------ */
+
+void oracle_rmsnorm_quant_act(const float* X, int64_t M, int64_t K, const float* gain, float eps, float clamp_eps,
+                              int8_t* x_q, float* s) {
+  float* xg = (float*)malloc((size_t)K * sizeof(float));
+  if (!xg) return;
+  for (int64_t m = 0; m < M; ++m) {
+    const float* row = X + m * K;
+    double ss = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+      ss += (double)row[k] * (double)row[k];
+      xg[k] = gain ? row[k] * gain[k] : row[k];
+    }
+    float sg;
+    oracle_quant_act(xg, 1, K, clamp_eps, x_q + m * K, &sg);
+    s[m] = (float)((double)sg * sqrt(ss / (double)K + (double)eps));
+  }
+  free(xg);
+}
+
+/* R10: squared ReLU on the BitLinear output ("a simpler squared ReLU", the  */
+/* same transcript paragraph): y' = fp32(max(y, 0) * max(y, 0)).             */
+void oracle_relu2(float* y, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) {
+    const float r = y[i] > 0.0f ? y[i] : 0.0f;
+    y[i] = r * r;
   }
 }
 

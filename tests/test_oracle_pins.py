@@ -383,3 +383,62 @@ def test_forward_end_to_end_tiny():
     assert abs(cos(y, np.roll(yf, 1, axis=1))) < 0.3
     with pytest.raises(ValueError):
         oracle.forward(np.full((N, K // 4), 0xFF, np.uint8), g, xq, s, K)
+
+
+# ---------------------------------------------------------------- sub-layer RMS norm and squared ReLU (R9, R10)
+
+def test_rmsnorm_quant_worked_example():
+    # x = [3, -4, 0, 0], eps = 0: max|x| = 4, s(x) = 127/4 = 31.75, x_q = [rint(95.25), -127, 0, 0];
+    # mean(x^2) = 25/4, sqrt = 2.5, so s = 31.75 * 2.5 = 79.375 (all exact in fp32)
+    xq, s = oracle.rmsnorm_quant_act(np.array([[3.0, -4.0, 0.0, 0.0]], np.float32), eps=np.float32(0.0))
+    assert xq.tolist() == [[95, -127, 0, 0]]
+    assert s.tolist() == [79.375]
+
+
+def test_rmsnorm_quant_is_invariant_to_token_scale():
+    # RMS normalisation makes the BitLinear input independent of a per-token scale:
+    # x_q and s must not change when a row is multiplied by 2^k (plain absmax
+    # quantisation would divide s by 2^k)
+    rng = np.random.default_rng(9)
+    X = rng.standard_normal((5, 96)).astype(np.float32)
+    xq0, s0 = oracle.rmsnorm_quant_act(X, eps=np.float32(0.0))
+    for k in (-3, 1, 6):
+        xq1, s1 = oracle.rmsnorm_quant_act(X * np.float32(2.0 ** k), eps=np.float32(0.0))
+        assert np.array_equal(xq0, xq1)
+        assert np.array_equal(s0, s1)
+    _, sp0 = oracle.quant_act(X)
+    _, sp1 = oracle.quant_act(X * np.float32(8.0))
+    assert np.array_equal(sp1 * np.float32(8.0), sp0)
+
+
+def test_rmsnorm_quant_gain():
+    rng = np.random.default_rng(10)
+    X = rng.standard_normal((3, 64)).astype(np.float32)
+    xq0, s0 = oracle.rmsnorm_quant_act(X)
+    # a uniform gain of 2 doubles every normalised value: same codes, half the scale
+    xq2, s2 = oracle.rmsnorm_quant_act(X, gain=np.full(64, 2.0, np.float32))
+    assert np.array_equal(xq0, xq2) and np.array_equal(s2 * np.float32(2.0), s0)
+    # channels with zero gain quantise to zero; the others keep their sign
+    g = np.ones(64, np.float32)
+    g[::4] = 0.0
+    xqg, _ = oracle.rmsnorm_quant_act(X, gain=g)
+    assert np.all(xqg[:, ::4] == 0)
+    nz = (xqg != 0)
+    assert np.all(np.sign(xqg[nz]) == np.sign(X[nz]))
+
+
+def test_rmsnorm_quant_constant_and_zero_rows():
+    # constant row c: mean(x^2) = c^2, s = (127/|c|) * |c| = 127 with eps = 0
+    xq, s = oracle.rmsnorm_quant_act(np.full((2, 40), -0.5, np.float32), eps=np.float32(0.0))
+    assert np.all(xq == -127) and np.all(s == 127.0)
+    # an all-zero token stays finite (the absmax clamp) and quantises to zeros
+    xq, s = oracle.rmsnorm_quant_act(np.zeros((1, 16), np.float32))
+    assert np.all(xq == 0) and np.isfinite(s).all() and s[0] > 0
+
+
+def test_relu2_values():
+    y = np.array([-1.5, -0.0, 0.0, 2.5, 3.0e20, np.float32(1e-23)], np.float32)
+    out = oracle.relu2(y)
+    assert out[:4].tolist() == [0.0, 0.0, 0.0, 6.25]
+    assert np.isinf(out[4]) and out[4] > 0          # overflows to +inf in fp32
+    assert out[5] == np.float32(np.float32(1e-23) * np.float32(1e-23))  # rounds to the nearest fp32 (a subnormal)
