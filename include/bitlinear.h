@@ -146,6 +146,30 @@ bl_status bitlinear_quant_act(const void* X, bl_dtype dtype, int64_t M, int64_t 
                               cudaStream_t stream);
 
 /*
+ * bitlinear_rmsnorm_quant_act -- the normalisation that BitNet b1.58 2B4T adds
+ * inside each sub-layer, ahead of a BitLinear (yousumm.com transcript, the
+ * paragraph after the poker-chip analogy), folded into the per-token absmax
+ * quantisation.  The pages give no
+ * formula; this is RMS normalisation with an optional per-channel gain,
+ * x_n = X * gain / sqrt(mean(X^2) + eps).  The RMS factor is one positive
+ * number per token and absmax codes are invariant to it, so
+ *   x_q = quantisation of X * gain   (bit-identical to bitlinear_quant_act of
+ *                                     the fp32 products X * gain)
+ *   s[m] = s(X * gain) * sqrt(mean(X[m,:]^2) + eps)
+ * and bitlinear_forward(..., x_q, s, ...) then yields W_q applied to x_n.
+ *
+ *   X       in   [M, K] row-major, BL_BF16 or BL_F32, element-aligned
+ *   gain    in   fp32 [K] (4-byte aligned) or NULL for all ones
+ *   eps     in   finite, >= 0
+ *   x_q, s  out  as for bitlinear_quant_act (x_q needs no alignment here)
+ *
+ * mean(X^2) is summed in fp64 in an unspecified order, so s may differ from
+ * an fp64 sequential sum in its last bit; x_q does not depend on it.
+ */
+bl_status bitlinear_rmsnorm_quant_act(const void* X, bl_dtype dtype, int64_t M, int64_t K, const float* gain,
+                                      float eps, int8_t* x_q, float* s, cudaStream_t stream);
+
+/*
  * bitlinear_forward -- y = (W_q . x_q) * gamma / s: the ternary-times-int8
  * product accumulated exactly in int32, rescaled per token by gamma/s[m] in
  * a fused epilogue (anthology note-168, "The part that is a bet rather than a
@@ -176,6 +200,13 @@ bl_status bitlinear_forward(const uint8_t* W_packed, const float* gamma, const i
  * dependent launch); activations are still read only after it completes. */
 #define BITLINEAR_WEIGHTS_RESIDENT 1u
 
+/* Flag of bitlinear_quant_forward(_ws): the epilogue writes the squared ReLU
+ * y = fp32(max(y,0) * max(y,0)) of the rescaled product: the FFN activation
+ * that BitNet b1.58 2B4T uses in place of a gated one (yousumm.com transcript,
+ * the paragraph after the poker-chip analogy).  acc, when requested, still
+ * holds the raw integer products. */
+#define BITLINEAR_RELU2 2u
+
 /* Test hook of bitlinear_quant_forward(_ws), not for production use: on the
  * one-kernel path (M <= 4, K <= 32768) the kernel issues no weight copies, so
  * its bounded waits run out (after about two seconds); it then records
@@ -201,7 +232,7 @@ bl_status bitlinear_forward(const uint8_t* W_packed, const float* gamma, const i
  *   x_q, s              out  int8 [M, K] (16-byte aligned) and fp32 [M] (4-byte
  *                            aligned): the quantised activations and scales
  *   acc                 out  optional int32 [M, N] (may be NULL)
- *   flags               in   0 or BITLINEAR_WEIGHTS_RESIDENT
+ *   flags               in   0, or BITLINEAR_WEIGHTS_RESIDENT and/or BITLINEAR_RELU2
  */
 bl_status bitlinear_quant_forward(const uint8_t* W_packed, const float* gamma, const void* X, bl_dtype dtype,
                                   int64_t M, int64_t N, int64_t K, float* y, int8_t* x_q, float* s, int32_t* acc,

@@ -242,8 +242,8 @@ void oracle_quant_act(const float* X, int64_t M, int64_t K, float clamp_eps, int
 
 /* ------------------------------------------------------------------------ */
 /* R9: sub-layer RMS normalisation ahead of the activation quantisation.     */
-/* The transcript names a "sub-layer norm" in the BitNet b1.58 2B4T block    */
-/* (paragraph after the poker-chip analogy); its formula is not on the       */
+/* The transcript says BitNet b1.58 2B4T adds a normalisation inside each    */
+/* sub-layer (paragraph after the poker-chip analogy); its formula is not on */
 /* pages.  Reading: x_n = x * g / sqrt(mean(x^2) + eps) per token, g an       */
 /* optional per-channel gain.  The per-token factor 1/sqrt(...) does not     */
 /* change the absmax codes (absmax quantisation is invariant to a positive   */
@@ -270,8 +270,8 @@ void oracle_rmsnorm_quant_act(const float* X, int64_t M, int64_t K, const float*
   free(xg);
 }
 
-/* R10: squared ReLU on the BitLinear output ("a simpler squared ReLU", the  */
-/* same transcript paragraph): y' = fp32(max(y, 0) * max(y, 0)).             */
+/* R10: squared ReLU on the BitLinear output, the FFN activation that the    */
+/* same transcript paragraph names: y' = fp32(max(y, 0) * max(y, 0)).        */
 void oracle_relu2(float* y, int64_t n) {
   for (int64_t i = 0; i < n; ++i) {
     const float r = y[i] > 0.0f ? y[i] : 0.0f;

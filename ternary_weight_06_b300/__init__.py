@@ -30,6 +30,7 @@ __all__ = [
     "bitlinear_pack_weights",
     "bitlinear_pack_workspace_bytes",
     "bitlinear_quant_act",
+    "bitlinear_rmsnorm_quant_act",
     "bitlinear_forward",
     "bitlinear_quant_forward",
     "bitlinear_forward_workspace_bytes",
@@ -39,6 +40,8 @@ __all__ = [
     "bitlinear_status_string",
     "BITLINEAR_WEIGHTS_RESIDENT",
     "BITLINEAR_TEST_STALL",
+    "BITLINEAR_RELU2",
+    "bitlinear_rmsnorm_quant_act",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -48,6 +51,7 @@ BL_OK, BL_ERR_INVALID_ARG, BL_ERR_UNSUPPORTED_SHAPE, BL_ERR_MISALIGNED, BL_ERR_W
     BL_ERR_TIMEOUT = range(7)
 BL_F32, BL_BF16 = 0, 1
 BITLINEAR_WEIGHTS_RESIDENT = 1
+BITLINEAR_RELU2 = 2  # epilogue writes the squared ReLU of y
 BITLINEAR_TEST_STALL = 0x80000000  # test hook: the one-kernel path's bounded waits run out
 
 EXPORTED_SYMBOLS = (
@@ -83,6 +87,8 @@ def _load() -> ctypes.CDLL:
     L.bitlinear_pack_weights.restype = i32
     L.bitlinear_quant_act.argtypes = [P, i32, i64, i64, P, P, P]
     L.bitlinear_quant_act.restype = i32
+    L.bitlinear_rmsnorm_quant_act.argtypes = [P, i32, i64, i64, P, f32, P, P, P]
+    L.bitlinear_rmsnorm_quant_act.restype = i32
     L.bitlinear_forward.argtypes = [P, P, P, P, i64, i64, i64, P, P, P]
     L.bitlinear_forward.restype = i32
     L.bitlinear_pack_weights_noalloc.argtypes = [P, i64, i64, f32, P, P, P]
@@ -178,6 +184,29 @@ def bitlinear_quant_act(X: torch.Tensor, x_q: torch.Tensor | None = None, s: tor
         s = torch.empty((M,), dtype=torch.float32, device=X.device)
     _check(get_lib().bitlinear_quant_act(_dev(X, "X"), dt, M, K, _dev(x_q, "x_q", torch.int8),
                                    _dev(s, "s", torch.float32), _stream(stream)), "bitlinear_quant_act")
+    return x_q, s
+
+
+def bitlinear_rmsnorm_quant_act(X: torch.Tensor, gain: torch.Tensor | None = None, eps: float = 1e-5,
+                                x_q: torch.Tensor | None = None, s: torch.Tensor | None = None, stream=None):
+    """Sub-layer RMS normalisation folded into the int8 quantisation of X
+    (bf16 or fp32 [M, K]): x_q = quant(X * gain), s = s(X * gain) *
+    sqrt(mean(X^2) + eps).  Returns (x_q int8 [M, K], s fp32 [M])."""
+    M, K = X.shape
+    if X.dtype == torch.bfloat16:
+        dt = BL_BF16
+    elif X.dtype == torch.float32:
+        dt = BL_F32
+    else:
+        raise ValueError(f"X must be bf16 or fp32, got {X.dtype}")
+    if x_q is None:
+        x_q = torch.empty((M, K), dtype=torch.int8, device=X.device)
+    if s is None:
+        s = torch.empty((M,), dtype=torch.float32, device=X.device)
+    g_ptr = _dev(gain, "gain", torch.float32) if gain is not None else None
+    _check(get_lib().bitlinear_rmsnorm_quant_act(_dev(X, "X"), dt, M, K, g_ptr, float(eps),
+                                                 _dev(x_q, "x_q", torch.int8), _dev(s, "s", torch.float32),
+                                                 _stream(stream)), "bitlinear_rmsnorm_quant_act")
     return x_q, s
 
 

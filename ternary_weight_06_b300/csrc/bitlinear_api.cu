@@ -82,6 +82,17 @@ bl_status bitlinear_quant_act(const void* X, bl_dtype dtype, int64_t M, int64_t 
   return from_cuda(bl::launch_quant_act(X, dtype == BL_BF16, M, K, x_q, s, stream));
 }
 
+bl_status bitlinear_rmsnorm_quant_act(const void* X, bl_dtype dtype, int64_t M, int64_t K, const float* gain,
+                                      float eps, int8_t* x_q, float* s, cudaStream_t stream) {
+  if (!X || !x_q || !s) return BL_ERR_INVALID_ARG;
+  if (M < 1 || K < 1) return BL_ERR_INVALID_ARG;
+  if (dtype != BL_F32 && dtype != BL_BF16) return BL_ERR_INVALID_ARG;
+  if (!std::isfinite(eps) || eps < 0.0f) return BL_ERR_INVALID_ARG;
+  if (M > INT32_MAX || K > (int64_t)1 << 24) return BL_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(X, dtype == BL_BF16 ? 2 : 4) || !aligned(s, 4) || (gain && !aligned(gain, 4))) return BL_ERR_MISALIGNED;
+  return from_cuda(bl::launch_rmsnorm_quant_act(X, dtype == BL_BF16, M, K, gain, eps, x_q, s, stream));
+}
+
 bl_status bitlinear_forward(const uint8_t* W_packed, const float* gamma, const int8_t* x_q, const float* s,
                             int64_t M, int64_t N, int64_t K, float* y, int32_t* acc, cudaStream_t stream) {
   if (!W_packed || !gamma || !x_q || !s || !y) return BL_ERR_INVALID_ARG;
@@ -103,14 +114,14 @@ bl_status bitlinear_quant_forward(const uint8_t* W_packed, const float* gamma, c
   if (!W_packed || !gamma || !X || !y || !x_q || !s) return BL_ERR_INVALID_ARG;
   if (M < 1 || N < 1 || K < 1) return BL_ERR_INVALID_ARG;
   if (dtype != BL_F32 && dtype != BL_BF16) return BL_ERR_INVALID_ARG;
-  if (flags & ~(BITLINEAR_WEIGHTS_RESIDENT | BITLINEAR_TEST_STALL)) return BL_ERR_INVALID_ARG;
+  if (flags & ~(BITLINEAR_WEIGHTS_RESIDENT | BITLINEAR_RELU2 | BITLINEAR_TEST_STALL)) return BL_ERR_INVALID_ARG;
   if (K % 64 != 0 || K > BITLINEAR_MAX_K || M > INT32_MAX || N > INT32_MAX) return BL_ERR_UNSUPPORTED_SHAPE;
   if (!aligned(W_packed, 16) || !aligned(X, 16) || !aligned(x_q, 16) || !aligned(y, 16) || !aligned(gamma, 4) ||
       !aligned(s, 4) || (acc && !aligned(acc, 16)))
     return BL_ERR_MISALIGNED;
   DeviceInfo d;
   if (bl_status st = device_info(&d)) return st;
-  bl::ForwardArgs a{W_packed, gamma, x_q, s, M, N, K, y, acc, d.err};
+  bl::ForwardArgs a{W_packed, gamma, x_q, s, M, N, K, y, acc, d.err, (flags & BITLINEAR_RELU2) != 0};
   const bool stall = (flags & BITLINEAR_TEST_STALL) != 0;
   if (M <= bl::kGemvMaxTokens && K <= bl::kGemvMaxK)
     return from_cuda(bl::launch_gemv_fused(a, X, dtype == BL_BF16, x_q, s, (flags & BITLINEAR_WEIGHTS_RESIDENT) != 0,
@@ -164,7 +175,7 @@ bl_status bitlinear_quant_forward_ws(const uint8_t* W_packed, const float* gamma
   if (!W_packed || !gamma || !X || !y || !x_q || !s) return BL_ERR_INVALID_ARG;
   if (M < 1 || N < 1 || K < 1) return BL_ERR_INVALID_ARG;
   if (dtype != BL_F32 && dtype != BL_BF16) return BL_ERR_INVALID_ARG;
-  if (flags & ~(BITLINEAR_WEIGHTS_RESIDENT | BITLINEAR_TEST_STALL)) return BL_ERR_INVALID_ARG;
+  if (flags & ~(BITLINEAR_WEIGHTS_RESIDENT | BITLINEAR_RELU2 | BITLINEAR_TEST_STALL)) return BL_ERR_INVALID_ARG;
   if (K % 64 != 0 || K > BITLINEAR_MAX_K || M > INT32_MAX || N > INT32_MAX) return BL_ERR_UNSUPPORTED_SHAPE;
   if (!aligned(W_packed, 16) || !aligned(X, 16) || !aligned(x_q, 16) || !aligned(y, 16) || !aligned(gamma, 4) ||
       !aligned(s, 4) || (acc && !aligned(acc, 16)))
@@ -172,7 +183,7 @@ bl_status bitlinear_quant_forward_ws(const uint8_t* W_packed, const float* gamma
   if (bl_status st = check_workspace(M, N, K, workspace, workspace_bytes)) return st;
   DeviceInfo d;
   if (bl_status st = device_info(&d)) return st;
-  bl::ForwardArgs a{W_packed, gamma, x_q, s, M, N, K, y, acc, d.err};
+  bl::ForwardArgs a{W_packed, gamma, x_q, s, M, N, K, y, acc, d.err, (flags & BITLINEAR_RELU2) != 0};
   const bool stall = (flags & BITLINEAR_TEST_STALL) != 0;
   if (M <= bl::kGemvMaxTokens && K <= bl::kGemvMaxK)
     return from_cuda(bl::launch_gemv_fused(a, X, dtype == BL_BF16, x_q, s, (flags & BITLINEAR_WEIGHTS_RESIDENT) != 0,

@@ -117,6 +117,15 @@ inline cudaError_t set_smem_attrs(Kernel kern, size_t smem_bytes) {
   return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
 }
 
+// Output activation of the epilogue: y, or the squared ReLU fp32(max(y,0)^2).
+__device__ __forceinline__ float out_act(float y, int relu2) {
+  if (relu2) {
+    const float r = y > 0.0f ? y : 0.0f;
+    return __fmul_rn(r, r);
+  }
+  return y;
+}
+
 // ---- exact int8 -> fp16 operand expansion (shared by the GEMM and the
 // activation quantisation, which can write the GEMM's operand directly)
 

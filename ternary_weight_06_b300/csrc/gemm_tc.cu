@@ -55,6 +55,7 @@ struct GemmCfg {
   int32_t* acc;
   uint32_t* err;
   int M, N, K, BN;
+  int relu2;    // epilogue applies the squared ReLU
   int nstages;  // ring depth (the GEMM on pre-expanded activations)
   int ksplit;   // CTAs of a cluster that split K (1 = no split)
 };
@@ -188,7 +189,7 @@ __device__ __forceinline__ void epilogue_store(const GemmCfg& c, uint32_t tmem, 
         if (m < c.M) {
           const float v = __uint_as_float(r[jj]);
           const int64_t o = (int64_t)m * c.N + n;
-          c.y[o] = __fmul_rn(v, tscale[j0 + jj]);
+          c.y[o] = out_act(__fmul_rn(v, tscale[j0 + jj]), c.relu2);
           if (c.acc) c.acc[o] = __float2int_rn(v);
         }
       }
@@ -595,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int m = m0 + j0 + jj;
             if (m < c.M) {
               const int64_t o = (int64_t)m * c.N + n;
-              c.y[o] = __fmul_rn(v[jj], tscale[j0 + jj]);
+              c.y[o] = out_act(__fmul_rn(v[jj], tscale[j0 + jj]), c.relu2);
               if (c.acc) c.acc[o] = __float2int_rn(v[jj]);
             }
           }
@@ -803,7 +804,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             if (m < c.M) {
               const float v = __uint_as_float(rr[jj]);
               const int64_t o = (int64_t)m * c.N + n;
-              c.y[o] = __fmul_rn(v, ts[j0 + jj]);
+              c.y[o] = out_act(__fmul_rn(v, ts[j0 + jj]), c.relu2);
               if (c.acc) c.acc[o] = __float2int_rn(v);
             }
           }
@@ -969,7 +970,7 @@ cudaError_t launch_gemm_tc_x16(const ForwardArgs& a, const void* x16, int num_sm
     cudaError_t e =
         cudaFuncSetAttribute(gemm_tc_x16_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    GemmCfg c{a.gamma, a.s, a.y, a.acc, a.err, (int)a.M, (int)a.N, (int)a.K, BN, NS, 1};
+    GemmCfg c{a.gamma, a.s, a.y, a.acc, a.err, (int)a.M, (int)a.N, (int)a.K, BN, a.relu2 ? 1 : 0, NS, 1};
     const int grid = (int)(tiles < num_sms ? tiles : num_sms);
     gemm_tc_x16_persistent_kernel<<<grid, kPThreads, smem, stream>>>(tw, tx, c);
     return cudaGetLastError();
@@ -990,7 +991,7 @@ cudaError_t launch_gemm_tc_x16(const ForwardArgs& a, const void* x16, int num_sm
   int S = choose_ksplit((int64_t)ntn * ntiles, nkb, BN, NS, smem, num_sms);
   // the split partials live in the ring memory: 128 x BN fp32
   if ((size_t)kBM * BN * 4 > (size_t)NS * stage) S = 1;
-  GemmCfg c{a.gamma, a.s, a.y, a.acc, a.err, (int)a.M, (int)a.N, (int)a.K, BN, NS, S};
+  GemmCfg c{a.gamma, a.s, a.y, a.acc, a.err, (int)a.M, (int)a.N, (int)a.K, BN, a.relu2 ? 1 : 0, NS, S};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)ntn, (unsigned)ntiles, (unsigned)S);
   cfg.blockDim = dim3(kThreads);
@@ -1013,7 +1014,7 @@ cudaError_t launch_gemm_tc(const ForwardArgs& a, int num_sms, cudaStream_t strea
   CUtensorMap tw, tx;
   if (!encode_u8_2d(&tw, a.Wp, (uint64_t)a.K / 4, (uint64_t)a.N, kBK / 4, kBM)) return cudaErrorInvalidValue;
   if (!encode_u8_2d(&tx, a.xq, (uint64_t)a.K, (uint64_t)a.M, kBK, (uint32_t)BN)) return cudaErrorInvalidValue;
-  GemmCfg c{a.gamma, a.s, a.y, a.acc, a.err, (int)a.M, (int)a.N, (int)a.K, BN, 0, 1};
+  GemmCfg c{a.gamma, a.s, a.y, a.acc, a.err, (int)a.M, (int)a.N, (int)a.K, BN, a.relu2 ? 1 : 0, 0, 1};
   const size_t smem = 1024 + (size_t)kOpStages * (kAOpBytes + BN * kARowBytes) +
                       (size_t)kRawStages * (kWRawBytes + BN * kBK) + (2 * kRawStages + 2 * kOpStages + 1) * 8 + 16 +
                       (size_t)BN * 4;

@@ -72,6 +72,7 @@ struct GemvCfg {
   int rows_per_cta, rows_per_stage, row_bytes, nslots;  // nslots <= kStages ring slots
   int kw, words_per_row, words_per_warp;
   int test_stall;  // test hook: the producer issues no copies, so the bounded waits expire
+  int relu2;       // epilogue applies the squared ReLU
 };
 
 __device__ __forceinline__ void transpose4x4(uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3, uint32_t* o) {
@@ -452,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm + 1) gemv_kernel(const Ge
       const int t = idx / nrows, r = idx - t * nrows;
       const int32_t v = acc_sm[r * MT + t];
       const int64_t o = (int64_t)(c.tok0 + t) * c.N + row0 + r;
-      c.y[o] = __fmul_rn(__int2float_rn(v), tsc_sm[t]);
+      c.y[o] = out_act(__fmul_rn(__int2float_rn(v), tsc_sm[t]), c.relu2);
       if (c.acc) c.acc[o] = v;
     }
   }
@@ -514,6 +515,7 @@ cudaError_t run(const ForwardArgs& a, const void* X, bool x_bf16, int8_t* xq_out
                 bool pdl, bool test_stall, int num_sms, cudaStream_t stream) {
   GemvCfg c{};
   c.test_stall = test_stall ? 1 : 0;
+  c.relu2 = a.relu2 ? 1 : 0;
   c.Wp = a.Wp;
   c.gamma = a.gamma;
   c.xq_in = a.xq;

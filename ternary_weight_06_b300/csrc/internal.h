@@ -26,6 +26,11 @@ cudaError_t launch_quant_act(const void* X, bool bf16, int64_t M, int64_t K, int
 
 // The same quantisation, also writing the GEMM's fp16 activation operand
 // (gemm_x16_workspace_bytes(M, K) bytes at x16, 16-byte aligned); K % 16 == 0.
+// Sub-layer RMS normalisation folded into the quantisation: x_q = quant(X * gain),
+// s = s(X * gain) * sqrt(mean(X^2) + eps).  gain may be null (all ones).
+cudaError_t launch_rmsnorm_quant_act(const void* X, bool bf16, int64_t M, int64_t K, const float* gain, float eps,
+                                     int8_t* xq, float* s, cudaStream_t stream);
+
 cudaError_t launch_quant_act_x16(const void* X, bool bf16, int64_t M, int64_t K, int8_t* xq, float* s, void* x16,
                                  cudaStream_t stream);
 
@@ -38,6 +43,7 @@ struct ForwardArgs {
   float* y;
   int32_t* acc;
   uint32_t* err;  // device error word
+  bool relu2 = false;  // epilogue applies the squared ReLU
 };
 
 // Streaming GEMV for a few tokens (tokens are taken in groups of <= 4; K <= 32768).

@@ -133,7 +133,76 @@ __global__ void __launch_bounds__(1024) quant_act_kernel(const void* __restrict_
   }
 }
 
+// Sub-layer RMS normalisation folded into the quantisation.  The RMS factor
+// 1/sqrt(mean(x^2) + eps) is one positive number per token, to which absmax
+// codes are invariant, so the codes are those of x * gain and only the scale
+// changes: s = s(x * gain) * sqrt(mean(x^2) + eps).  Pass 1 forms max|x * g|
+// (order-free, on bit patterns) and sum x^2 (fp64); pass 2 quantises x * g
+// with the same fp32 product, so x_q is bit-identical to quantising x * g.
+template <bool BF16>
+__global__ void __launch_bounds__(1024) rmsnorm_quant_act_kernel(const void* __restrict__ X, int64_t K,
+                                                                 const float* __restrict__ gain, float eps,
+                                                                 int8_t* __restrict__ xq, float* __restrict__ s) {
+  constexpr int kEsize = BF16 ? 2 : 4;
+  const int64_t m = blockIdx.x;
+  const char* row = static_cast<const char*>(X) + m * K * kEsize;
+  int8_t* out = xq + m * K;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  auto load = [&](int64_t k) -> float {
+    return BF16 ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(row)[k] << 16)
+                : reinterpret_cast<const float*>(row)[k];
+  };
+  uint32_t amax = 0;
+  double ss = 0.0;
+  for (int64_t k = tid; k < K; k += nt) {
+    const float x = load(k);
+    const float xg = gain ? __fmul_rn(x, __ldg(gain + k)) : x;
+    amax = max(amax, __float_as_uint(xg) & 0x7fffffffu);
+    ss = __fma_rn((double)x, (double)x, ss);
+  }
+  __shared__ uint32_t red[32];
+  __shared__ double red_ss[32];
+  amax = __reduce_max_sync(0xffffffffu, amax);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((tid & 31) == 0) {
+    red[tid >> 5] = amax;
+    red_ss[tid >> 5] = ss;
+  }
+  __syncthreads();
+  if (tid < 32) {
+    uint32_t v = tid < (nt >> 5) ? red[tid] : 0u;
+    double w = tid < (nt >> 5) ? red_ss[tid] : 0.0;
+    v = __reduce_max_sync(0xffffffffu, v);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
+    if (tid == 0) {
+      red[0] = v;
+      red_ss[0] = w;
+    }
+  }
+  __syncthreads();
+  float a = __uint_as_float(red[0]);
+  if (a < kActClampEps) a = kActClampEps;
+  const float sg = __fdiv_rn(127.0f, a);
+  if (tid == 0) s[m] = (float)((double)sg * sqrt(red_ss[0] / (double)K + (double)eps));
+  for (int64_t k = tid; k < K; k += nt) {
+    const float x = load(k);
+    const float xg = gain ? __fmul_rn(x, __ldg(gain + k)) : x;
+    out[k] = (int8_t)q8(xg, sg);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_rmsnorm_quant_act(const void* X, bool bf16, int64_t M, int64_t K, const float* gain, float eps,
+                                     int8_t* xq, float* s, cudaStream_t stream) {
+  int threads = (int)((K + 31) / 32 * 32);
+  if (threads > 1024) threads = 1024;
+  if (bf16) rmsnorm_quant_act_kernel<true><<<(unsigned)M, threads, 0, stream>>>(X, K, gain, eps, xq, s);
+  else rmsnorm_quant_act_kernel<false><<<(unsigned)M, threads, 0, stream>>>(X, K, gain, eps, xq, s);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quant_act(const void* X, bool bf16, int64_t M, int64_t K, int8_t* xq, float* s,
                              cudaStream_t stream) {

@@ -137,7 +137,7 @@ def test_quant_forward_validation(bl):
         assert qfwd(bl, **{kw: None}) == bl.BL_ERR_INVALID_ARG, kw
     assert qfwd(bl, M=0) == bl.BL_ERR_INVALID_ARG
     assert qfwd(bl, dt=3) == bl.BL_ERR_INVALID_ARG
-    assert qfwd(bl, flags=2) == bl.BL_ERR_INVALID_ARG
+    assert qfwd(bl, flags=4) == bl.BL_ERR_INVALID_ARG
     assert qfwd(bl, K=96) == bl.BL_ERR_UNSUPPORTED_SHAPE
     assert qfwd(bl, K=131072 + 64) == bl.BL_ERR_UNSUPPORTED_SHAPE
     assert qfwd(bl, X=GOOD + 2) == bl.BL_ERR_MISALIGNED
@@ -181,11 +181,26 @@ def test_forward_ws_validation(bl):
     for kw in ("Wp", "g", "X", "y", "xq", "s"):
         assert qfwd_ws(bl, **{kw: None}) == bl.BL_ERR_INVALID_ARG, kw
     assert qfwd_ws(bl, dt=3) == bl.BL_ERR_INVALID_ARG
-    assert qfwd_ws(bl, flags=2) == bl.BL_ERR_INVALID_ARG
+    assert qfwd_ws(bl, flags=4) == bl.BL_ERR_INVALID_ARG
     assert qfwd_ws(bl, X=GOOD + 2) == bl.BL_ERR_MISALIGNED
     assert qfwd_ws(bl, ws=None) == bl.BL_ERR_WORKSPACE
     assert qfwd_ws(bl, ws_bytes=100) == bl.BL_ERR_WORKSPACE
     assert qfwd_ws(bl, ws=GOOD + 4) == bl.BL_ERR_MISALIGNED
+
+
+def test_rmsnorm_quant_validation(bl):
+    f = bl.get_lib().bitlinear_rmsnorm_quant_act
+    assert f(None, 1, 2, 64, None, 1e-5, GOOD, GOOD, None) == bl.BL_ERR_INVALID_ARG
+    assert f(GOOD, 1, 2, 64, None, 1e-5, None, GOOD, None) == bl.BL_ERR_INVALID_ARG
+    assert f(GOOD, 2, 2, 64, None, 1e-5, GOOD, GOOD, None) == bl.BL_ERR_INVALID_ARG  # dtype
+    assert f(GOOD, 1, 0, 64, None, 1e-5, GOOD, GOOD, None) == bl.BL_ERR_INVALID_ARG
+    assert f(GOOD, 1, 2, 64, None, -1.0, GOOD, GOOD, None) == bl.BL_ERR_INVALID_ARG
+    assert f(GOOD, 1, 2, 64, None, float("nan"), GOOD, GOOD, None) == bl.BL_ERR_INVALID_ARG
+    assert f(GOOD, 1, 2, 2**24 + 1, None, 1e-5, GOOD, GOOD, None) == bl.BL_ERR_UNSUPPORTED_SHAPE
+    assert f(GOOD + 1, 1, 2, 64, None, 1e-5, GOOD, GOOD, None) == bl.BL_ERR_MISALIGNED
+    assert f(GOOD + 2, 0, 2, 64, None, 1e-5, GOOD, GOOD, None) == bl.BL_ERR_MISALIGNED  # fp32 needs 4
+    assert f(GOOD, 1, 2, 64, GOOD + 2, 1e-5, GOOD, GOOD, None) == bl.BL_ERR_MISALIGNED
+    assert qfwd(bl, flags=bl.BITLINEAR_RELU2 | 4) == bl.BL_ERR_INVALID_ARG
 
 
 def test_python_binding_rejects_cpu_tensors(bl):

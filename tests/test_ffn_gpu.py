@@ -1,0 +1,104 @@
+"""The BitNet FFN pieces around the BitLinear, against the oracle: the
+sub-layer RMS norm folded into the activation quantisation (reading R9) and
+the squared-ReLU epilogue (reading R10), on every kernel path."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+S_RTOL = 1e-6  # s carries an fp64 sum of squares whose order is unspecified
+Y_RTOL = 1e-5
+
+
+@pytest.fixture(scope="module")
+def bl():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from ternary_weight_06_b300 import build
+
+    build.build()
+    import ternary_weight_06_b300 as mod
+
+    return mod
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("K", [1, 63, 2560, 6912, 40000])
+@pytest.mark.parametrize("with_gain", [False, True])
+def test_rmsnorm_quant_act(bl, dtype, K, with_gain):
+    g = torch.Generator().manual_seed(K + with_gain)
+    X = torch.randn((7, K), generator=g) * 3.0
+    X[1] = 0.0  # an all-zero token
+    X[2] *= 1e4
+    X = X.to(dtype)
+    gain = (torch.rand((K,), generator=g) * 2.0).to(torch.float32) if with_gain else None
+    xq_ref, s_ref = oracle.rmsnorm_quant_act(X.to(torch.float32).numpy(),
+                                             gain=None if gain is None else gain.numpy())
+    xq, s = bl.bitlinear_rmsnorm_quant_act(X.cuda(), gain=None if gain is None else gain.cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(xq.cpu().numpy(), xq_ref), "codes must be bit-exact"
+    rel = np.abs(s.cpu().numpy() - s_ref) / s_ref
+    assert rel.max() <= S_RTOL, rel.max()
+
+
+def _relu2_case(bl, M, N, K, ws):
+    rng = np.random.default_rng(M * 31 + N)
+    q = rng.integers(-1, 2, size=(N, K)).astype(np.int8)
+    p = oracle.pack(q)
+    X = torch.randn((M, K), generator=torch.Generator().manual_seed(M + N)).to(torch.bfloat16)
+    xq_ref, s_ref = oracle.quant_act(X.to(torch.float32).numpy())
+    y_ref, acc_ref = oracle.forward(p, np.float32(0.05), xq_ref, s_ref, K)
+    y_ref = oracle.relu2(y_ref)
+    call = bl.bitlinear_quant_forward_ws if ws else bl.bitlinear_quant_forward
+    y, xq, s, acc = call(torch.from_numpy(p).cuda(), torch.tensor([0.05]).cuda(), X.cuda(), acc=True,
+                         flags=bl.BITLINEAR_RELU2)
+    torch.cuda.synchronize()
+    assert np.array_equal(acc.cpu().numpy(), acc_ref), "acc keeps the raw integer products"
+    assert np.array_equal(y.cpu().numpy().view(np.uint32), y_ref.view(np.uint32))
+    bl.bitlinear_check_device_error()
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 300, 1024), (4, 999, 2560), (5, 257, 640), (64, 1000, 2560),
+                                   (300, 19000, 128)])
+@pytest.mark.parametrize("ws", [False, True])
+def test_relu2_epilogue_every_path(bl, M, N, K, ws):
+    _relu2_case(bl, M, N, K, ws)
+
+
+@pytest.mark.parametrize("M", [1, 16])
+def test_ffn_chain(bl, M):
+    """up projection with the squared ReLU, sub-layer RMS norm + quantisation,
+    down projection: the BitNet b1.58 FFN, each step on the GPU."""
+    rng = np.random.default_rng(M)
+    D, H = 512, 1536
+    q_up = rng.integers(-1, 2, size=(H, D)).astype(np.int8)
+    q_dn = rng.integers(-1, 2, size=(D, H)).astype(np.int8)
+    p_up, p_dn = oracle.pack(q_up), oracle.pack(q_dn)
+    g_up, g_dn = np.float32(0.03), np.float32(0.02)
+    gain = (rng.uniform(0.5, 1.5, size=H)).astype(np.float32)
+    X = torch.randn((M, D), generator=torch.Generator().manual_seed(7)).to(torch.bfloat16)
+    # oracle chain
+    xq, s = oracle.quant_act(X.to(torch.float32).numpy())
+    h, _ = oracle.forward(p_up, g_up, xq, s, D)
+    h = oracle.relu2(h)
+    hq, hs = oracle.rmsnorm_quant_act(h, gain=gain)
+    y_ref, _ = oracle.forward(p_dn, g_dn, hq, hs, H)
+    # GPU chain
+    dev = "cuda"
+    hd, _, _ = bl.bitlinear_quant_forward_ws(torch.from_numpy(p_up).to(dev), torch.tensor([g_up]).to(dev),
+                                             X.to(dev), flags=bl.BITLINEAR_RELU2)
+    hqd, hsd = bl.bitlinear_rmsnorm_quant_act(hd, gain=torch.from_numpy(gain).to(dev))
+    y = bl.bitlinear_forward_ws(torch.from_numpy(p_dn).to(dev), torch.tensor([g_dn]).to(dev), hqd, hsd)
+    torch.cuda.synchronize()
+    assert np.array_equal(hd.cpu().numpy().view(np.uint32), h.view(np.uint32))
+    assert np.array_equal(hqd.cpu().numpy(), hq)
+    yr = y.cpu().numpy()
+    nz = y_ref != 0
+    assert np.all(yr[~nz] == 0)
+    assert (np.abs(yr[nz] - y_ref[nz]) / np.abs(y_ref[nz])).max() <= Y_RTOL
+    bl.bitlinear_check_device_error()

@@ -436,6 +436,25 @@ def test_rmsnorm_quant_constant_and_zero_rows():
     assert np.all(xq == 0) and np.isfinite(s).all() and s[0] > 0
 
 
+def test_rmsnorm_quant_matches_unfused_definition():
+    # normalise first, in fp64, then absmax-quantise: the folded form must give
+    # the same codes (random data has no exact .5 ties) and x_q / s must
+    # reconstruct x_n to within half a quantisation step
+    rng = np.random.default_rng(11)
+    K = 300
+    X = (rng.standard_normal((6, K)) * rng.uniform(0.01, 50.0, size=(6, 1))).astype(np.float32)
+    g = rng.uniform(0.2, 2.0, size=K).astype(np.float32)
+    eps = 1e-5
+    xq, s = oracle.rmsnorm_quant_act(X, gain=g, eps=np.float32(eps))
+    x64 = X.astype(np.float64)
+    xn = x64 * g.astype(np.float64) / np.sqrt((x64 ** 2).mean(axis=1, keepdims=True) + np.float32(eps))
+    sc = 127.0 / np.abs(xn).max(axis=1, keepdims=True)
+    codes = np.clip(np.rint(xn * sc), -127, 127).astype(np.int8)
+    assert np.array_equal(xq, codes)
+    assert np.allclose(s, sc[:, 0], rtol=1e-6, atol=0)
+    assert np.all(np.abs(xq / s[:, None].astype(np.float64) - xn) <= 0.5 / s[:, None] * (1 + 1e-5))
+
+
 def test_relu2_values():
     y = np.array([-1.5, -0.0, 0.0, 2.5, 3.0e20, np.float32(1e-23)], np.float32)
     out = oracle.relu2(y)
