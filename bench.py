@@ -449,6 +449,40 @@ def run_gpu(args, dist, rank, world, local):
     if fused and kname == "gemv_kernel":
         roof["note"] = "the timed kernel also quantises the activations (fused)"
 
+    # ---- the FFN pieces around each layer, timed the same way (outside the step):
+    # the sub-layer RMS norm folded into the quantisation of the layer's X, and
+    # the fused forward with and without the squared-ReLU epilogue
+    def graph_us(fn):
+        g = capture(fn, kchunk)
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(3):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        del g
+        return a.elapsed_time(b) * 1e3 / (3 * kchunk)
+
+    ffn = {"rmsnorm_quant": [], "forward_us": [], "forward_relu2_us": []}
+    for l, L in enumerate(wl.layers):
+        gain = torch.rand((L.K,), generator=torch.Generator().manual_seed(l), dtype=torch.float32).add_(0.5).to(dev)
+        us = graph_us(lambda j, l=l, gain=gain: bl.bitlinear_rmsnorm_quant_act(
+            Xrot[l][j % Rs[l]], gain=gain, x_q=xqs[l], s=ss[l], stream=stream))
+        nbytes = L.M * L.K * (Xs[l].element_size() + 1) + 4 * L.M + 4 * L.K
+        ffn["rmsnorm_quant"].append({"us": round(us, 3), "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1),
+                                     "frac": round(nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+                                     "algorithmic_bytes": nbytes})
+        for key, fl in (("forward_us", 0), ("forward_relu2_us", bl.BITLINEAR_RELU2)):
+            ffn[key].append(round(graph_us(lambda j, l=l, fl=fl: bl.bitlinear_quant_forward_ws(
+                Wrot[l][j % Rs[l]], gammas[l], Xrot[l][j % Rs[l]], y=ys[l], x_q=xqs[l], s=ss[l],
+                workspace=workspace, flags=fl, stream=stream)), 3))
+    bl.bitlinear_check_device_error(stream)
+    ffn["note"] = ("rmsnorm_quant: bitlinear_rmsnorm_quant_act on each layer's X with a per-channel gain, bytes = "
+                   "X read + x_q write + s + gain, frac of the measured copy bandwidth; forward(_relu2)_us: "
+                   "bitlinear_quant_forward_ws without and with BITLINEAR_RELU2")
+
     e2e = run_e2e(bl, wl, step, Xs_host, y_all, K, Wm, stream, dist, world, unit, step_bytes, step_ops)
 
     return {
@@ -470,6 +504,7 @@ def run_gpu(args, dist, rank, world, local):
         "gpu_launches": launches,
         "verified": verified,
         "clocks": clocks,
+        "ffn": ffn,
         "pack": {"ms": round(pack_ms, 4), "GB/s": round(pack_bytes / (pack_ms * 1e-3) / 1e9, 1),
                  "note": "gamma + ternarise + pack of every layer (one call each), outside the step"},
     }

@@ -79,7 +79,9 @@ bl_status bitlinear_quant_act(const void* X, bl_dtype dtype, int64_t M, int64_t 
   if (dtype != BL_F32 && dtype != BL_BF16) return BL_ERR_INVALID_ARG;
   if (M > INT32_MAX || K > (int64_t)1 << 24) return BL_ERR_UNSUPPORTED_SHAPE;
   if (!aligned(X, 16) || !aligned(x_q, 16) || !aligned(s, 4)) return BL_ERR_MISALIGNED;
-  return from_cuda(bl::launch_quant_act(X, dtype == BL_BF16, M, K, x_q, s, stream));
+  DeviceInfo d;
+  if (bl_status st = device_info(&d)) return st;
+  return from_cuda(bl::launch_quant_act(X, dtype == BL_BF16, M, K, x_q, s, d.num_sms, d.err, stream));
 }
 
 bl_status bitlinear_rmsnorm_quant_act(const void* X, bl_dtype dtype, int64_t M, int64_t K, const float* gain,
@@ -127,7 +129,8 @@ bl_status bitlinear_quant_forward(const uint8_t* W_packed, const float* gamma, c
     return from_cuda(bl::launch_gemv_fused(a, X, dtype == BL_BF16, x_q, s, (flags & BITLINEAR_WEIGHTS_RESIDENT) != 0,
                                            stall, d.num_sms, stream));
   if (stall) return BL_ERR_INVALID_ARG;  // the test hook exists on the one-kernel path only
-  if (cudaError_t e = bl::launch_quant_act(X, dtype == BL_BF16, M, K, x_q, s, stream)) return from_cuda(e);
+  if (cudaError_t e = bl::launch_quant_act(X, dtype == BL_BF16, M, K, x_q, s, d.num_sms, d.err, stream))
+    return from_cuda(e);
   return from_cuda(bl::launch_gemm_tc(a, d.num_sms, stream));
 }
 

@@ -12,6 +12,7 @@ enum : uint32_t {
   kErrGemvFullWait = 1u << 0,
   kErrGemvEmptyWait = 1u << 1,
   kErrGemmWait = 1u << 2,
+  kErrQuantWait = 1u << 3,
 };
 
 // A bounded wait gives up after this many nanoseconds of polling.  Every

@@ -412,7 +412,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm + 1) gemv_kernel(const Ge
           for (int t = 0; t < MT; ++t)
 #pragma unroll
             for (int i = 0; i < 4; ++i) a[rr][t][i] = 0;
-#pragma unroll
         // one pointer per row (rows past the stage's last valid row read that
         // row again; their sums are discarded), words at immediate offsets.
         // Words past this lane's K slice multiply activations held as zero,

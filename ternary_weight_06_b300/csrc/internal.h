@@ -21,8 +21,12 @@ constexpr size_t kPackWorkspaceBytes = 512;
 cudaError_t launch_pack(const float* W, uint64_t n, float eps, uint8_t* Wp, float* gamma, PackWorkspace* ws,
                         int num_sms, cudaStream_t stream);
 
-cudaError_t launch_quant_act(const void* X, bool bf16, int64_t M, int64_t K, int8_t* xq, float* s,
-                             cudaStream_t stream);
+// Per-token quantisation.  From 256 tokens up (K % 16 == 0, 16-byte aligned
+// buffers) a persistent kernel with rows staged in shared memory by bulk
+// copies, one team of warps per row; else one CTA per row.  err: the device
+// error word (the staged kernel's waits are bounded).
+cudaError_t launch_quant_act(const void* X, bool bf16, int64_t M, int64_t K, int8_t* xq, float* s, int num_sms,
+                             uint32_t* err, cudaStream_t stream);
 
 // The same quantisation, also writing the GEMM's fp16 activation operand
 // (gemm_x16_workspace_bytes(M, K) bytes at x16, 16-byte aligned); K % 16 == 0.

@@ -9,6 +9,7 @@
 // loads (as fp32 bit patterns: for non-negative floats the unsigned order is
 // the numeric order, so the reduction is exact and order-free); pass 2 reads
 // the row again (from L1/L2) and writes x_q.
+#include <algorithm>
 #include <cstdint>
 
 #include "common.cuh"
@@ -18,6 +19,7 @@ namespace bl {
 namespace {
 
 constexpr float kActClampEps = 1e-5f;
+constexpr int kRmsCache = 4;
 
 __device__ __forceinline__ uint32_t abs_bits_bf16x2(uint32_t w) {
   return max((w << 16) & 0x7fff0000u, w & 0x7fff0000u);
@@ -136,76 +138,525 @@ __global__ void __launch_bounds__(1024) quant_act_kernel(const void* __restrict_
 // Sub-layer RMS normalisation folded into the quantisation.  The RMS factor
 // 1/sqrt(mean(x^2) + eps) is one positive number per token, to which absmax
 // codes are invariant, so the codes are those of x * gain and only the scale
-// changes: s = s(x * gain) * sqrt(mean(x^2) + eps).  Pass 1 forms max|x * g|
-// (order-free, on bit patterns) and sum x^2 (fp64); pass 2 quantises x * g
-// with the same fp32 product, so x_q is bit-identical to quantising x * g.
+// changes: s = s(x * gain) * sqrt(mean(x^2) + eps).
+//
+// Pass 1 forms max|x| and max|x * g| (order-free, on fp32 bit patterns).
+// Pass 2 quantises x * g with the same fp32 product, so x_q is bit-identical
+// to quantising x * g, and sums the squares.  On the 128-bit path the squares
+// are of x * 2^-e, e the exponent of max|x| (an exact scaling that keeps
+// every square <= 4, so nothing overflows fp32 and a row of tiny values keeps
+// its precision), summed in fp32 within each 16-byte chunk, and the chunk sums
+// are carried as an fp32 pair (hi, lo) with an error-free two-sum, across
+// threads too.  With all terms positive the relative error of the sum is that
+// of one chunk, about 4 fp32 ulps, so s carries about 2 ulps more than an
+// fp64 sum; fp64 is used by one thread, once, at the end (fp64 issues slowly
+// on this part).  Each thread keeps its first kRmsCache chunks of x in
+// registers between the passes, all loaded before the first is used, and the
+// CTA is sized so that a row of up to 1024 * kRmsCache chunks is read once.
+// The scalar path (rows or gain not 16-byte aligned) sums x^2 in fp64
+// element by element.
+
+__device__ __forceinline__ void block_reduce_max2(uint32_t& a, uint32_t& b, uint32_t* red) {
+  const int tid = threadIdx.x, nw = blockDim.x >> 5;
+  a = __reduce_max_sync(0xffffffffu, a);
+  b = __reduce_max_sync(0xffffffffu, b);
+  if ((tid & 31) == 0) {
+    red[tid >> 5] = a;
+    red[32 + (tid >> 5)] = b;
+  }
+  __syncthreads();
+  if (tid < 32) {
+    uint32_t u = tid < nw ? red[tid] : 0u, v = tid < nw ? red[32 + tid] : 0u;
+    u = __reduce_max_sync(0xffffffffu, u);
+    v = __reduce_max_sync(0xffffffffu, v);
+    if (tid == 0) {
+      red[64] = u;
+      red[65] = v;
+    }
+  }
+  __syncthreads();
+  a = red[64];
+  b = red[65];
+}
+
+// (hi, lo) += p with hi + lo kept exactly up to the rounding of lo (Knuth's two-sum)
+__device__ __forceinline__ void two_sum_add(float& hi, float& lo, float p) {
+  const float t = __fadd_rn(hi, p);
+  const float z = __fsub_rn(t, hi);
+  const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(t, z)), __fsub_rn(p, z));
+  hi = t;
+  lo = __fadd_rn(lo, err);
+}
+
+__device__ __forceinline__ double block_reduce_pair(float hi, float lo, float2* red) {
+  const int tid = threadIdx.x, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float h2 = __shfl_xor_sync(0xffffffffu, hi, o), l2 = __shfl_xor_sync(0xffffffffu, lo, o);
+    two_sum_add(hi, lo, h2);
+    lo = __fadd_rn(lo, l2);
+  }
+  if ((tid & 31) == 0) red[tid >> 5] = make_float2(hi, lo);
+  __syncthreads();
+  double r = 0.0;
+  if (tid < 32) {
+    const float2 v = tid < nw ? red[tid] : make_float2(0.0f, 0.0f);
+    hi = v.x;
+    lo = v.y;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float h2 = __shfl_xor_sync(0xffffffffu, hi, o), l2 = __shfl_xor_sync(0xffffffffu, lo, o);
+      two_sum_add(hi, lo, h2);
+      lo = __fadd_rn(lo, l2);
+    }
+    if (tid == 0) r = (double)hi + (double)lo;
+  }
+  return r;  // valid in thread 0
+}
+
+__device__ __forceinline__ float sq_sum4(float a, float b, float c, float d) {
+  return __fadd_rn(__fadd_rn(__fmul_rn(a, a), __fmul_rn(b, b)), __fadd_rn(__fmul_rn(c, c), __fmul_rn(d, d)));
+}
+
 template <bool BF16>
-__global__ void __launch_bounds__(1024) rmsnorm_quant_act_kernel(const void* __restrict__ X, int64_t K,
+__device__ __forceinline__ void unpack_chunk(const uint4 v, float* x) {
+  if (BF16) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = bf16_lo(w[i]);
+      x[2 * i + 1] = bf16_hi(w[i]);
+    }
+  } else {
+    x[0] = __uint_as_float(v.x);
+    x[1] = __uint_as_float(v.y);
+    x[2] = __uint_as_float(v.z);
+    x[3] = __uint_as_float(v.w);
+  }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(1024) rmsnorm_quant_act_kernel(const void* __restrict__ X, int64_t K, bool vec,
                                                                  const float* __restrict__ gain, float eps,
                                                                  int8_t* __restrict__ xq, float* __restrict__ s) {
   constexpr int kEsize = BF16 ? 2 : 4;
+  constexpr int kPer = 16 / kEsize;  // elements per 16-byte chunk
+  constexpr int kCache = kRmsCache;  // chunks per thread held in registers between the passes
   const int64_t m = blockIdx.x;
   const char* row = static_cast<const char*>(X) + m * K * kEsize;
+  const uint4* row4 = reinterpret_cast<const uint4*>(row);
+  const float4* gain4 = reinterpret_cast<const float4*>(gain);
   int8_t* out = xq + m * K;
   const int tid = threadIdx.x, nt = blockDim.x;
+  __shared__ uint32_t red[66];
+  __shared__ float2 red_ss[32];
+
+  auto load_gain = [&](int64_t c, float (&g)[kPer]) {
+    if (gain) {
+#pragma unroll
+      for (int h = 0; h < kPer / 4; ++h) {
+        const float4 q = __ldg(gain4 + c * (kPer / 4) + h);
+        g[4 * h] = q.x;
+        g[4 * h + 1] = q.y;
+        g[4 * h + 2] = q.z;
+        g[4 * h + 3] = q.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) g[i] = 1.0f;
+    }
+  };
   auto load = [&](int64_t k) -> float {
     return BF16 ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(row)[k] << 16)
                 : reinterpret_cast<const float*>(row)[k];
   };
-  uint32_t amax = 0;
-  double ss = 0.0;
-  for (int64_t k = tid; k < K; k += nt) {
-    const float x = load(k);
-    const float xg = gain ? __fmul_rn(x, __ldg(gain + k)) : x;
-    amax = max(amax, __float_as_uint(xg) & 0x7fffffffu);
-    ss = __fma_rn((double)x, (double)x, ss);
-  }
-  __shared__ uint32_t red[32];
-  __shared__ double red_ss[32];
-  amax = __reduce_max_sync(0xffffffffu, amax);
+
+  // pass 1: max|x| and max|x * g|
+  uint32_t amax_x = 0, amax_g = 0;
+  const int64_t nch = vec ? K / kPer : 0;
+  uint4 xc[kCache];
+  auto amax_chunk = [&](const uint4 v, const float (&g)[kPer]) {
+    float x[kPer];
+    unpack_chunk<BF16>(v, x);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if ((tid & 31) == 0) {
-    red[tid >> 5] = amax;
-    red_ss[tid >> 5] = ss;
-  }
-  __syncthreads();
-  if (tid < 32) {
-    uint32_t v = tid < (nt >> 5) ? red[tid] : 0u;
-    double w = tid < (nt >> 5) ? red_ss[tid] : 0.0;
-    v = __reduce_max_sync(0xffffffffu, v);
+    for (int i = 0; i < kPer; ++i) {
+      amax_x = max(amax_x, __float_as_uint(x[i]) & 0x7fffffffu);
+      amax_g = max(amax_g, __float_as_uint(__fmul_rn(x[i], g[i])) & 0x7fffffffu);
+    }
+  };
+  if (vec) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
-    if (tid == 0) {
-      red[0] = v;
-      red_ss[0] = w;
+    for (int i = 0; i < kCache; ++i) {
+      const int64_t c = tid + (int64_t)i * nt;
+      if (c < nch) xc[i] = __ldg(row4 + c);  // every load in flight before the first use
+    }
+#pragma unroll
+    for (int i = 0; i < kCache; ++i) {
+      const int64_t c = tid + (int64_t)i * nt;
+      if (c < nch) {
+        float g[kPer];
+        load_gain(c, g);
+        amax_chunk(xc[i], g);
+      }
+    }
+    for (int64_t c = tid + (int64_t)kCache * nt; c < nch; c += nt) {
+      float g[kPer];
+      load_gain(c, g);
+      amax_chunk(__ldg(row4 + c), g);
+    }
+  } else {
+    for (int64_t k = tid; k < K; k += nt) {
+      const float x = load(k);
+      const float xg = gain ? __fmul_rn(x, __ldg(gain + k)) : x;
+      amax_x = max(amax_x, __float_as_uint(x) & 0x7fffffffu);
+      amax_g = max(amax_g, __float_as_uint(xg) & 0x7fffffffu);
     }
   }
-  __syncthreads();
-  float a = __uint_as_float(red[0]);
+  block_reduce_max2(amax_x, amax_g, red);
+  float a = __uint_as_float(amax_g);
   if (a < kActClampEps) a = kActClampEps;
   const float sg = __fdiv_rn(127.0f, a);
-  if (tid == 0) s[m] = (float)((double)sg * sqrt(red_ss[0] / (double)K + (double)eps));
-  for (int64_t k = tid; k < K; k += nt) {
-    const float x = load(k);
-    const float xg = gain ? __fmul_rn(x, __ldg(gain + k)) : x;
-    out[k] = (int8_t)q8(xg, sg);
+
+  // pass 2: codes of x * g, and the sum of squares
+  double ss = 0.0;
+  if (vec) {
+    // 2^-e with e the unbiased exponent of max|x| (max|x| * 2^-e in [1, 2));
+    // a zero row keeps scale 1; a subnormal maximum takes 2^126
+    int e = 0;
+    if (amax_x >= 0x00800000u) e = (int)(amax_x >> 23) - 127;
+    else if (amax_x != 0) e = -126;
+    const float scale = ldexpf(1.0f, -e);
+    float hi = 0.0f, lo = 0.0f;
+    auto quant_chunk = [&](int64_t c, const uint4 v, const float (&g)[kPer]) {
+      float x[kPer];
+      unpack_chunk<BF16>(v, x);
+      uint32_t q[kPer];
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) q[i] = q8(__fmul_rn(x[i], g[i]), sg);
+      float part = 0.0f;
+#pragma unroll
+      for (int h = 0; h < kPer / 4; ++h)
+        part = __fadd_rn(part, sq_sum4(__fmul_rn(x[4 * h], scale), __fmul_rn(x[4 * h + 1], scale),
+                                       __fmul_rn(x[4 * h + 2], scale), __fmul_rn(x[4 * h + 3], scale)));
+      two_sum_add(hi, lo, part);
+      if (BF16) {
+        uint2 o;
+        o.x = q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24);
+        o.y = q[4] | (q[5] << 8) | (q[6] << 16) | (q[7] << 24);
+        reinterpret_cast<uint2*>(out)[c] = o;
+      } else {
+        reinterpret_cast<uint32_t*>(out)[c] = q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24);
+      }
+    };
+#pragma unroll
+    for (int i = 0; i < kCache; ++i) {
+      const int64_t c = tid + (int64_t)i * nt;
+      if (c < nch) {
+        float g[kPer];
+        load_gain(c, g);  // the gain row is shared by every token: an L1 hit
+        quant_chunk(c, xc[i], g);
+      }
+    }
+    for (int64_t c = tid + (int64_t)kCache * nt; c < nch; c += nt) {
+      float g[kPer];
+      load_gain(c, g);
+      quant_chunk(c, __ldg(row4 + c), g);
+    }
+    ss = block_reduce_pair(hi, lo, red_ss) * ldexp(1.0, 2 * e);
+  } else {
+    for (int64_t k = tid; k < K; k += nt) {
+      const float x = load(k);
+      const float xg = gain ? __fmul_rn(x, __ldg(gain + k)) : x;
+      out[k] = (int8_t)q8(xg, sg);
+      ss = __fma_rn((double)x, (double)x, ss);
+    }
+    // fp64 block sum (this path is off the fast path)
+    __shared__ double red_d[32];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((tid & 31) == 0) red_d[tid >> 5] = ss;
+    __syncthreads();
+    if (tid < 32) {
+      ss = tid < (nt >> 5) ? red_d[tid] : 0.0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    }
   }
+  if (tid == 0) s[m] = (float)((double)sg * sqrt(ss / (double)K + (double)eps));
+}
+
+// ---- many tokens: rows staged in shared memory, one team of warps per row -
+//
+// With one CTA per row, every CTA on an SM loads, reduces and quantises in
+// step, so DRAM idles while rows are being quantised and the last wave runs
+// mostly empty.  Here each team of T warps (T = 1, 2, 4 or 8) of a persistent
+// grid owns rows gt, gt + GT, ... (GT teams in the grid).  The team's leader
+// keeps the next `stages` rows in flight as 1-D bulk copies into the team's
+// shared-memory ring; thread t of the team takes the 16-byte chunks t,
+// t + 32T, ... of the staged row (consecutive lanes read consecutive chunks:
+// no bank conflicts).  The row maximum is a warp reduction, then (T > 1) a
+// named barrier over the team.  x_q and s are those of quant_act_kernel bit
+// for bit (finite inputs).
+
+struct RowQuantArgs {
+  const char* X;  // [M, K] rows, row_bytes = K * element size, 16-byte aligned
+  int64_t M, K;
+  int8_t* xq;  // [M, K], 16-byte aligned
+  float* s;
+  uint32_t* err;  // device error word
+  uint32_t row_bytes;
+  int stages;  // ring depth per team
+  int team;    // warps per row
+};
+
+constexpr int kRowWarpsMax = 16;
+constexpr uint32_t kRowBarBytes = 1024;  // mbarriers and per-team flags at the start of shared memory
+
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// fp32(x * s) rounded half to even by one fp32 add of 1.5 * 2^23: while
+// |x * s| < 2^22 the sum is 1.5 * 2^23 + rint(x * s) exactly (its ulp is 1,
+// and 1.5 * 2^23 is even, so ties go to the even integer), and the low byte
+// of its bits is the integer's two's-complement low byte.  For finite inputs
+// |x * s| <= 127 * (1 + 2^-24)^2, so this is the code of q8 (whose clamp never
+// acts) without the quarter-rate float-to-int conversion.
+__device__ __forceinline__ uint32_t q8_bits(float x, float s) {
+  return __float_as_uint(__fadd_rn(__fmul_rn(x, s), 12582912.0f));
+}
+
+// low bytes of a, b, c, d -> bytes 0..3 of one word
+__device__ __forceinline__ uint32_t pack_low_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  return __byte_perm(__byte_perm(a, b, 0x0040u), __byte_perm(c, d, 0x0040u), 0x5410u);
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kRowWarpsMax * 32) quant_rows_staged_kernel(const RowQuantArgs a) {
+  constexpr int kPer = BF16 ? 8 : 4;  // elements per 16-byte chunk
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ uint32_t red_max[kRowWarpsMax];  // per warp: max|x| bits of the current row
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  const int T = a.team, nteams = nwarps / T;
+  const int team = warp / T, tt = (warp % T) * 32 + lane, TT = T * 32;
+  const bool leader = tt == 0;
+  const int S = a.stages;
+  const int64_t K = a.K, nch = K / kPer;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem) + team * S;
+  volatile int* flag = reinterpret_cast<volatile int*>(smem + kRowBarBytes - 4 * kRowWarpsMax) + team;
+  unsigned char* ring = smem + kRowBarBytes + (size_t)team * S * a.row_bytes;
+  auto team_sync = [&]() {
+    if (T > 1) asm volatile("bar.sync %0, %1;" ::"r"(team + 1), "r"(TT) : "memory");
+    else __syncwarp();
+  };
+
+  if (leader) {
+    for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+
+  const int64_t gt = (int64_t)blockIdx.x * nteams + team, GT = (int64_t)gridDim.x * nteams;
+  const int64_t nrows = gt < a.M ? (a.M - 1 - gt) / GT + 1 : 0;
+  auto issue = [&](int64_t i, int st) {
+    const int64_t m = gt + i * GT;
+    mbar_arrive_expect_tx(&bars[st], a.row_bytes);
+    bulk_g2s(ring + (size_t)st * a.row_bytes, a.X + m * (int64_t)a.row_bytes, a.row_bytes, &bars[st]);
+  };
+  if (leader)
+    for (int i = 0; i < S && i < nrows; ++i) issue(i, i);
+
+  int st = 0, prev_st = 0;
+  uint32_t phase = 0;
+  for (int64_t i = 0; i < nrows; ++i) {
+    // the leader waits for the row (bounded) and posts the outcome; after the
+    // team barrier every thread of the team has also finished row i - 1
+    if (leader) *flag = mbar_wait_bounded(&bars[st], phase, a.err, kErrQuantWait) ? 1 : 0;
+    team_sync();
+    const bool ok = *flag != 0;
+    if (leader && i >= 1 && i - 1 + S < nrows) {
+      fence_proxy_async_smem();  // order the team's generic-proxy reads before the async overwrite
+      issue(i - 1 + S, prev_st);
+    }
+    if (!ok) {
+      // give up: rows i .. i + S - 1 have been issued (the refill above ran);
+      // let every copy still in flight into this team's ring land (each wait
+      // bounded) before the CTA's shared memory is released
+      if (leader) {
+        int sj = st;
+        uint32_t pj = phase;
+        for (int64_t j = i; j < i + S && j < nrows; ++j) {
+          mbar_wait_bounded(&bars[sj], pj, a.err, kErrQuantWait);
+          if (++sj == S) {
+            sj = 0;
+            pj ^= 1u;
+          }
+        }
+      }
+      return;
+    }
+    mbar_try_wait(smem_u32(&bars[st]), phase);  // complete: this thread's acquire of the copied row
+    const int64_t m = gt + i * GT;
+    const uint4* buf = reinterpret_cast<const uint4*>(ring + (size_t)st * a.row_bytes);
+
+    // pass 1: max|x| (bf16: packed maxima of the |x| bit patterns)
+    uint32_t amax;
+    if (BF16) {
+      uint32_t m2 = 0;
+      for (int64_t c = tt; c < nch; c += TT) {
+        const uint4 v = buf[c];
+        m2 = max_u16x2(max_u16x2(m2, v.x & 0x7fff7fffu),
+                       max_u16x2(v.y & 0x7fff7fffu, max_u16x2(v.z & 0x7fff7fffu, v.w & 0x7fff7fffu)));
+      }
+      amax = max(m2 >> 16, m2 & 0xffffu) << 16;
+    } else {
+      float f = 0.0f;
+      for (int64_t c = tt; c < nch; c += TT) {
+        const uint4 v = buf[c];
+        f = fmaxf(fmaxf(f, fabsf(__uint_as_float(v.x))),
+                  fmaxf(fabsf(__uint_as_float(v.y)), fmaxf(fabsf(__uint_as_float(v.z)), fabsf(__uint_as_float(v.w)))));
+      }
+      amax = __float_as_uint(f);
+    }
+    amax = __reduce_max_sync(0xffffffffu, amax);
+    if (T > 1) {
+      if (lane == 0) red_max[warp] = amax;
+      team_sync();
+      for (int w = 0; w < T; ++w) amax = max(amax, red_max[team * T + w]);
+    }
+    float am = __uint_as_float(amax);
+    if (am < kActClampEps) am = kActClampEps;
+    const float sg = __fdiv_rn(127.0f, am);
+
+    // pass 2: codes
+    int8_t* qrow = a.xq + m * K;
+    for (int64_t c = tt; c < nch; c += TT) {
+      float x[kPer];
+      unpack_chunk<BF16>(buf[c], x);
+      uint32_t w[kPer / 4];
+#pragma unroll
+      for (int h = 0; h < kPer / 4; ++h)
+        w[h] = pack_low_bytes(q8_bits(x[4 * h], sg), q8_bits(x[4 * h + 1], sg), q8_bits(x[4 * h + 2], sg),
+                              q8_bits(x[4 * h + 3], sg));
+      if (BF16) reinterpret_cast<uint2*>(qrow)[c] = make_uint2(w[0], w[1]);
+      else reinterpret_cast<uint32_t*>(qrow)[c] = w[0];
+    }
+    if (leader) a.s[m] = sg;
+    prev_st = st;
+    if (++st == S) {
+      st = 0;
+      phase ^= 1u;
+    }
+  }
+}
+
+// Launch shape of the staged kernel, or ok = false where the one-CTA-per-row
+// kernel serves (fewer than kRowStagedMinM rows, K % 16 != 0, or rows too
+// long for a ring that keeps enough warps on each SM).
+struct RowPlan {
+  bool ok = false;
+  int team = 1, warps = 0, stages = 0, grid = 0;
+  size_t smem = 0;
+};
+
+constexpr int64_t kRowStagedMinM = 256;
+constexpr size_t kRowSmemBudget = 200 * 1024;  // dynamic shared memory per CTA (also the kernel's limit)
+constexpr int kRowWarpsPerSmTarget = 32;       // busy warps per SM the team size aims for
+constexpr int kRowWarpsPerSmMin = 4;
+
+template <bool BF16>
+RowPlan plan_rows_staged(int64_t M, int64_t K, int num_sms) {
+  RowPlan p;
+  if (M < kRowStagedMinM || K % 16 != 0 || num_sms < 1) return p;
+  const size_t row = (size_t)K * (BF16 ? 2 : 4);
+  const size_t avail = kRowSmemBudget - kRowBarBytes;
+  int S = row <= 4096 ? 4 : (row <= 8192 ? 3 : 2);
+  // warps per row: several warps share a row (and its ring) when the rows are
+  // too few, or the rings too large for the shared memory of an SM, to keep
+  // about kRowWarpsPerSmTarget warps per SM at work
+  const int64_t teams_per_sm = (int64_t)(228 * 1024) / ((int64_t)S * (int64_t)row + 1024);
+  int T = 1;
+  while (T < 8 && (M * T < (int64_t)kRowWarpsPerSmTarget * num_sms || teams_per_sm * T < kRowWarpsPerSmTarget))
+    T *= 2;
+  auto kern = quant_rows_staged_kernel<BF16>;
+  if (set_smem_attrs(kern, kRowSmemBudget) != cudaSuccess) {
+    (void)cudaGetLastError();  // not sticky: clear it so the fallback's launch check does not see it
+    return p;
+  }
+  int nteams = 0, occ = 0, grid = 0;
+  size_t smem = 0;
+  for (int iter = 0; iter < 4; ++iter) {
+    nteams = (int)std::min<size_t>(kRowWarpsMax / T, avail / ((size_t)S * row));
+    if (nteams < 1) {
+      if (S == 1) return p;
+      --S;
+      continue;
+    }
+    smem = kRowBarBytes + (size_t)nteams * S * row;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, nteams * T * 32, smem) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return p;
+    }
+    if (occ < 1) return p;
+    grid = (int)std::min<int64_t>((int64_t)num_sms * occ, (M + nteams - 1) / nteams);
+    const int64_t rows_per_team = (M + (int64_t)grid * nteams - 1) / ((int64_t)grid * nteams);
+    if (rows_per_team >= S || S == 1) break;
+    S = (int)std::max<int64_t>(1, rows_per_team);  // no deeper ring than the rows a team gets
+  }
+  if (occ * nteams * T < kRowWarpsPerSmMin) return p;
+  p.ok = true;
+  p.team = T;
+  p.warps = nteams * T;
+  p.stages = S;
+  p.grid = grid;
+  p.smem = smem;
+  return p;
+}
+
+template <bool BF16>
+cudaError_t launch_rows_staged(const void* X, int64_t M, int64_t K, int8_t* xq, float* s, int num_sms, uint32_t* err,
+                               cudaStream_t stream, bool* launched) {
+  *launched = false;
+  const RowPlan p = plan_rows_staged<BF16>(M, K, num_sms);
+  if (!p.ok) return cudaSuccess;
+  const RowQuantArgs a{static_cast<const char*>(X), M, K, xq, s, err, (uint32_t)(K * (BF16 ? 2 : 4)), p.stages, p.team};
+  *launched = true;
+  quant_rows_staged_kernel<BF16><<<p.grid, p.warps * 32, p.smem, stream>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_rmsnorm_quant_act(const void* X, bool bf16, int64_t M, int64_t K, const float* gain, float eps,
                                      int8_t* xq, float* s, cudaStream_t stream) {
-  int threads = (int)((K + 31) / 32 * 32);
+  // 128-bit path: every row starts 16-byte aligned, the gain vector too, and
+  // each chunk's codes (8 or 4 bytes) are aligned stores
+  const int esize = bf16 ? 2 : 4;
+  const bool vec = (K * esize) % 16 == 0 && reinterpret_cast<uintptr_t>(X) % 16 == 0 &&
+                   (!gain || reinterpret_cast<uintptr_t>(gain) % 16 == 0) &&
+                   reinterpret_cast<uintptr_t>(xq) % (bf16 ? 8 : 4) == 0;
+  const int64_t work = vec ? (K * esize / 16 + kRmsCache - 1) / kRmsCache : K;
+  int threads = (int)((work + 31) / 32 * 32);
   if (threads > 1024) threads = 1024;
-  if (bf16) rmsnorm_quant_act_kernel<true><<<(unsigned)M, threads, 0, stream>>>(X, K, gain, eps, xq, s);
-  else rmsnorm_quant_act_kernel<false><<<(unsigned)M, threads, 0, stream>>>(X, K, gain, eps, xq, s);
+  if (bf16) rmsnorm_quant_act_kernel<true><<<(unsigned)M, threads, 0, stream>>>(X, K, vec, gain, eps, xq, s);
+  else rmsnorm_quant_act_kernel<false><<<(unsigned)M, threads, 0, stream>>>(X, K, vec, gain, eps, xq, s);
   return cudaGetLastError();
 }
 
-cudaError_t launch_quant_act(const void* X, bool bf16, int64_t M, int64_t K, int8_t* xq, float* s,
-                             cudaStream_t stream) {
+cudaError_t launch_quant_act(const void* X, bool bf16, int64_t M, int64_t K, int8_t* xq, float* s, int num_sms,
+                             uint32_t* err, cudaStream_t stream) {
+  if (reinterpret_cast<uintptr_t>(X) % 16 == 0 && reinterpret_cast<uintptr_t>(xq) % 16 == 0) {
+    bool launched = false;
+    const cudaError_t e = bf16 ? launch_rows_staged<true>(X, M, K, xq, s, num_sms, err, stream, &launched)
+                               : launch_rows_staged<false>(X, M, K, xq, s, num_sms, err, stream, &launched);
+    if (e != cudaSuccess || launched) return e;
+  }
   const int esize = bf16 ? 2 : 4;
   const bool vec = (K * esize) % 16 == 0;
   const int64_t work = vec ? K * esize / 16 : K;

@@ -35,6 +35,8 @@ def test_rmsnorm_quant_act(bl, dtype, K, with_gain):
     X = torch.randn((7, K), generator=g) * 3.0
     X[1] = 0.0  # an all-zero token
     X[2] *= 1e4
+    X[3] *= 1e30  # squares overflow fp32 unless scaled
+    X[4] *= 1e-40  # subnormal in fp32 (and bf16)
     X = X.to(dtype)
     gain = (torch.rand((K,), generator=g) * 2.0).to(torch.float32) if with_gain else None
     xq_ref, s_ref = oracle.rmsnorm_quant_act(X.to(torch.float32).numpy(),
@@ -44,6 +46,44 @@ def test_rmsnorm_quant_act(bl, dtype, K, with_gain):
     assert np.array_equal(xq.cpu().numpy(), xq_ref), "codes must be bit-exact"
     rel = np.abs(s.cpu().numpy() - s_ref) / s_ref
     assert rel.max() <= S_RTOL, rel.max()
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_rmsnorm_quant_act_unaligned(bl, dtype):
+    """gain and X views that are not 16-byte aligned take the element-wise path"""
+    K = 1024
+    g = torch.Generator().manual_seed(5)
+    Xb = (torch.randn((3 * K + 1,), generator=g) * 2.0).to(dtype)
+    gb = torch.rand((K + 1,), generator=g) + 0.5
+    X = Xb[1:].view(3, K)  # starts one element in
+    gain = gb[1:]
+    xq_ref, s_ref = oracle.rmsnorm_quant_act(X.to(torch.float32).numpy(), gain=gain.numpy())
+    xq, s = bl.bitlinear_rmsnorm_quant_act(Xb.cuda()[1:].view(3, K), gain=gb.cuda()[1:])
+    torch.cuda.synchronize()
+    assert np.array_equal(xq.cpu().numpy(), xq_ref)
+    assert (np.abs(s.cpu().numpy() - s_ref) / s_ref).max() <= S_RTOL
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("M", [256, 1000])
+@pytest.mark.parametrize("K", [16, 2560, 6912])
+@pytest.mark.parametrize("with_gain", [False, True])
+def test_rmsnorm_quant_act_many_tokens(bl, dtype, M, K, with_gain):
+    """the warp-per-row staged kernel (M >= 256), special rows on different warps"""
+    g = torch.Generator().manual_seed(M + K + with_gain)
+    X = torch.randn((M, K), generator=g) * 3.0
+    for r, f in ((0, 0.0), (M // 3, 1e30), (M // 2, 1e-40), (M - 1, 1e4)):
+        X[r] = X[r] * f
+    X = X.to(dtype)
+    gain = (torch.rand((K,), generator=g) * 2.0).to(torch.float32) if with_gain else None
+    xq_ref, s_ref = oracle.rmsnorm_quant_act(X.to(torch.float32).numpy(),
+                                             gain=None if gain is None else gain.numpy())
+    xq, s = bl.bitlinear_rmsnorm_quant_act(X.cuda(), gain=None if gain is None else gain.cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(xq.cpu().numpy(), xq_ref), "codes must be bit-exact"
+    rel = np.abs(s.cpu().numpy() - s_ref) / s_ref
+    assert rel.max() <= S_RTOL, rel.max()
+    bl.bitlinear_check_device_error()
 
 
 def _relu2_case(bl, M, N, K, ws):

@@ -171,6 +171,26 @@ def test_quant_edge_cases(bl, dtype, K):
     assert np.array_equal(xq.cpu().numpy(), xq_ref)
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("M", [255, 256, 257, 1000, 3001])
+@pytest.mark.parametrize("K", [16, 48, 2560, 6912])
+def test_quant_many_tokens(bl, dtype, M, K):
+    """From 256 tokens the quantisation runs one warp per row with rows staged
+    in shared memory; special rows sit on different warps and CTAs."""
+    g = torch.Generator().manual_seed(M * 7 + K)
+    X = torch.randn((M, K), generator=g)
+    for r, f in ((0, 0.0), (1, 1e-7), (M // 2, 1e4), (M - 1, 0.0)):
+        X[r] = X[r] * f
+    X[M - 2, :3] = torch.tensor([1.0, 0.5, -0.5])  # a half-way tie after scaling
+    X = X.to(dtype)
+    xq_ref, s_ref = oracle.quant_act(X.to(torch.float32).numpy())
+    xq, s = bl.bitlinear_quant_act(gpu(X))
+    torch.cuda.synchronize()
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(xq.cpu().numpy(), xq_ref)
+    bl.bitlinear_check_device_error()
+
+
 # ---------------------------------------------------------------- forward
 
 def sample_rows(M: int, limit: int, seed: int) -> np.ndarray:
@@ -434,6 +454,19 @@ def test_quant_forward_ws_edge_shapes(bl, dtype, M, N, K):
     X = X.to(dtype)
     fused_case(bl, oracle.pack(q), np.float32(0.031), X, K, sample_rows(M, 16, seed=M),
                f"ws fused M={M} N={N} K={K}", ws=True)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("M", [256, 300])
+@pytest.mark.parametrize("N,K", [(130, 2560), (64, 6912)])
+def test_quant_forward_ws_many_tokens(bl, dtype, M, N, K):
+    """the staged quantisation writing the GEMM's fp16 operand"""
+    rng = np.random.default_rng(M + N)
+    q = rng.integers(-1, 2, size=(N, K)).astype(np.int8)
+    X = torch.randn((M, K), generator=torch.Generator().manual_seed(M * N))
+    X[M - 1] = 0
+    X = X.to(dtype)
+    fused_case(bl, oracle.pack(q), np.float32(0.02), X, K, np.arange(M), f"ws fused M={M} N={N} K={K}", ws=True)
 
 
 @pytest.mark.parametrize("M,N,K", [(333, 19000, 192), (130, 19201, 320), (1000, 9000, 128)])
