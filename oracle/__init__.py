@@ -8,7 +8,7 @@ share no code.
 The arithmetic lives in ``bitlinear_oracle.c`` (plain C loops, one IEEE fp32
 operation per step, exact integer sums); this module compiles it with gcc on
 first use and exposes numpy-level wrappers.  Every function states the reading
-of the method it follows; see the C file's header for the list (R1..R6).
+of the method it follows; see the C file's header for the list.
 """
 from __future__ import annotations
 
@@ -58,6 +58,11 @@ def _load():
         lib.oracle_unpack.argtypes = [P, u64, P]
         lib.oracle_unpack.restype = u64
         lib.oracle_bf16_to_f32.argtypes = [P, u64, P]
+        lib.oracle_tq5_row_bytes.argtypes = [i64]
+        lib.oracle_tq5_row_bytes.restype = i64
+        lib.oracle_pack_tq5.argtypes = [P, i64, i64, P]
+        lib.oracle_unpack_tq5.argtypes = [P, i64, i64, P]
+        lib.oracle_unpack_tq5.restype = u64
         lib.oracle_quant_act.argtypes = [P, i64, i64, ctypes.c_float, P, P]
         lib.oracle_matmul_int.argtypes = [P, P, i64, i64, i64, P]
         lib.oracle_dequant.argtypes = [P, ctypes.c_float, P, i64, i64, P]
@@ -119,6 +124,49 @@ def pack_weights(W: np.ndarray, eps=WEIGHT_EPS) -> tuple[np.ndarray, np.float32]
     """The whole weight path: gamma, ternarise, pack.  Returns (W_packed, gamma)."""
     g = absmean(W)
     return pack(ternarize(W, g, eps)), g
+
+
+def tq5_row_bytes(K: int) -> int:
+    """Bytes per row of the base-3 format (reading R11): ceil(K/5) rounded up to 16."""
+    return int(_load().oracle_tq5_row_bytes(int(K)))
+
+
+def pack_tq5(q: np.ndarray) -> np.ndarray:
+    """Five ternary codes per byte as base-3 digits (reading R11).  q is [N, K];
+    returns uint8 [N, tq5_row_bytes(K)]."""
+    q = _c(q, np.int8)
+    N, K = q.shape
+    out = np.empty((N, tq5_row_bytes(K)), dtype=np.uint8)
+    _load().oracle_pack_tq5(_p(q), N, K, _p(out))
+    return out
+
+
+def unpack_tq5(packed: np.ndarray, K: int) -> tuple[np.ndarray, int]:
+    """Inverse of :func:`pack_tq5`; also returns the count of invalid bytes and
+    of padding digits that are not zero codes."""
+    packed = _c(packed, np.uint8)
+    N, pitch = packed.shape
+    if pitch != tq5_row_bytes(K):
+        raise ValueError("row pitch does not match K")
+    q = np.empty((N, K), dtype=np.int8)
+    bad = _load().oracle_unpack_tq5(_p(packed), N, K, _p(q))
+    return q, int(bad)
+
+
+def pack_weights_tq5(W: np.ndarray, eps=WEIGHT_EPS) -> tuple[np.ndarray, np.float32]:
+    """gamma, ternarise, base-3 pack.  Returns (W_tq5, gamma)."""
+    g = absmean(W)
+    return pack_tq5(ternarize(W, g, eps)), g
+
+
+def forward_tq5(W_tq5: np.ndarray, gamma, x_q: np.ndarray, s: np.ndarray, K: int) -> tuple[np.ndarray, np.ndarray]:
+    """Forward pass from base-3 packed weights: decode (R11), exact integer
+    product, R6 dequantisation.  Returns (y fp32 [M,N], acc int32 [M,N])."""
+    q, bad = unpack_tq5(W_tq5, K)
+    if bad:
+        raise ValueError(f"{bad} invalid base-3 bytes or padding digits")
+    acc = matmul_int(q, x_q)
+    return dequant(acc, gamma, s), acc
 
 
 def bf16_bits_to_f32(x_bits: np.ndarray) -> np.ndarray:

@@ -40,6 +40,9 @@
  *       optional per-channel gain; it leaves x_q = quant(x * g) and scales s
  *       by sqrt(mean(x^2) + eps) (see the function).
  *   R10 squared ReLU on the output is fp32(max(y,0) * max(y,0)).
+ *   R11 base-3 packing: five codes per byte as sum (q+1) * 3^i, least
+ *       significant first, rows of ceil(K/5) bytes padded with 121 (zero
+ *       codes) to a multiple of 16.
  *
  * Build: plain C11, -O2 -ffp-contract=off, no fast-math (so every float
  * operation is a single IEEE-754 binary32 operation with RNE).
@@ -204,6 +207,63 @@ uint64_t oracle_unpack(const uint8_t* packed, uint64_t n, int8_t* q) {
     unsigned code = (packed[i / 4] >> (2 * (i % 4))) & 3u;
     if (code == 3) ++bad;
     q[i] = (int8_t)((int)code - 1);
+  }
+  return bad;
+}
+
+/* ------------------------------------------------------------------------ */
+/* R11: base-3 packing, five weights per byte (1.6 bits per weight).         */
+/* The pages put the information in one ternary weight at log2(3) = 1.58    */
+/* bits and the weights of the 2B model at about 0.4 GB, under 2 bits per    */
+/* weight, without spelling the format out.  Reading: byte j of a row holds  */
+/* the digits d_i = q[5j + i] + 1 (i = 0..4, least significant first) as     */
+/* sum d_i * 3^i, a value in 0..242; positions at or past K take d = 1       */
+/* (q = 0).  A row takes ceil(K / 5) bytes, padded to a multiple of 16 bytes */
+/* with 121 (five zero codes).                                               */
+/* ------------------------------------------------------------------------ */
+
+int64_t oracle_tq5_row_bytes(int64_t K) {
+  const int64_t used = (K + 4) / 5;
+  return (used + 15) / 16 * 16;
+}
+
+void oracle_pack_tq5(const int8_t* q, int64_t N, int64_t K, uint8_t* out) {
+  const int64_t pitch = oracle_tq5_row_bytes(K);
+  for (int64_t n = 0; n < N; ++n) {
+    for (int64_t j = 0; j < pitch; ++j) {
+      unsigned value = 0, weight = 1;
+      for (int i = 0; i < 5; ++i) {
+        const int64_t k = 5 * j + i;
+        const unsigned digit = k < K ? (unsigned)(q[n * K + k] + 1) : 1u;
+        value += digit * weight;
+        weight *= 3u;
+      }
+      out[n * pitch + j] = (uint8_t)value;
+    }
+  }
+}
+
+/* Inverse of oracle_pack_tq5.  Returns the number of bytes above 242 (not a */
+/* five-digit base-3 value; decoded as five zero codes) plus the number of   */
+/* padding digits that are not zero codes.                                   */
+uint64_t oracle_unpack_tq5(const uint8_t* in, int64_t N, int64_t K, int8_t* q) {
+  const int64_t pitch = oracle_tq5_row_bytes(K);
+  uint64_t bad = 0;
+  for (int64_t n = 0; n < N; ++n) {
+    for (int64_t j = 0; j < pitch; ++j) {
+      unsigned value = in[n * pitch + j];
+      if (value > 242u) {
+        ++bad;
+        value = 121u;
+      }
+      for (int i = 0; i < 5; ++i) {
+        const unsigned digit = value % 3u;
+        value /= 3u;
+        const int64_t k = 5 * j + i;
+        if (k < K) q[n * K + k] = (int8_t)((int)digit - 1);
+        else if (digit != 1u) ++bad;
+      }
+    }
   }
   return bad;
 }

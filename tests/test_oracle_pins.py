@@ -461,3 +461,75 @@ def test_relu2_values():
     assert out[:4].tolist() == [0.0, 0.0, 0.0, 6.25]
     assert np.isinf(out[4]) and out[4] > 0          # overflows to +inf in fp32
     assert out[5] == np.float32(np.float32(1e-23) * np.float32(1e-23))  # rounds to the nearest fp32 (a subnormal)
+
+
+# ---------------------------------------------------------------- base-3 packing, five weights per byte (R11)
+
+def test_tq5_hand_computed_bytes():
+    # q = [1, 0, -1, 1, 1] -> digits [2, 1, 0, 2, 2] -> 2 + 1*3 + 0*9 + 2*27 + 2*81 = 221
+    # all -1 -> 0, all 0 -> 1 + 3 + 9 + 27 + 81 = 121, all +1 -> 2 * 121 = 242
+    q = np.array([[1, 0, -1, 1, 1, -1, -1, -1, -1, -1, 0, 0, 0, 0, 0, 1, 1, 1, 1, 1]], np.int8)
+    p = oracle.pack_tq5(q)
+    assert p.shape == (1, 16)
+    assert p[0, :4].tolist() == [221, 0, 121, 242]
+    assert np.all(p[0, 4:] == 121)  # padding: five zero codes
+
+
+def test_tq5_enumerates_every_code_in_order():
+    # row v holds the little-endian base-3 digits of v: the byte must be v itself,
+    # so the 243 patterns map one to one, in order, onto 0..242
+    v = np.arange(243)
+    digits = np.stack([(v // 3 ** i) % 3 for i in range(5)], axis=1)
+    p = oracle.pack_tq5((digits - 1).astype(np.int8))
+    assert p[:, 0].tolist() == v.tolist()
+    q, bad = oracle.unpack_tq5(p, 5)
+    assert bad == 0 and np.array_equal(q, (digits - 1).astype(np.int8))
+
+
+def test_tq5_ragged_row_padding():
+    # K = 7: byte 0 holds k = 0..4, byte 1 holds k = 5, 6 and three zero codes
+    q = np.array([[0, 0, 0, 0, 0, 1, -1]], np.int8)
+    p = oracle.pack_tq5(q)
+    assert p[0, 0] == 121
+    assert p[0, 1] == 2 + 0 * 3 + 1 * 9 + 1 * 27 + 1 * 81  # = 119
+    assert np.all(p[0, 2:] == 121) and p.shape == (1, 16)
+
+
+def test_tq5_round_trip_and_invalid_bytes():
+    rng = np.random.default_rng(12)
+    for K in (1, 5, 80, 6912, 2563):
+        q = rng.integers(-1, 2, size=(9, K)).astype(np.int8)
+        p = oracle.pack_tq5(q)
+        assert p.shape == (9, oracle.tq5_row_bytes(K)) and p.max() <= 242
+        q2, bad = oracle.unpack_tq5(p, K)
+        assert bad == 0 and np.array_equal(q, q2)
+    p = oracle.pack_tq5(np.zeros((1, 5), np.int8))
+    p[0, 0] = 243  # not a five-digit base-3 value
+    p[0, 1] = 120  # a padding byte whose digits are not all zero codes
+    _, bad = oracle.unpack_tq5(p, 5)
+    assert bad == 2
+
+
+def test_tq5_bits_per_weight():
+    # 8 / 5 = 1.6 bits per weight when K is a multiple of 80, above the
+    # information bound log2(3) = 1.58496 (page constant) and below the 2-bit code
+    for K in (80, 2560, 6912):
+        bits = oracle.tq5_row_bytes(K) * 8 / K
+        assert math.isclose(bits, 1.6) if K % 80 == 0 else bits < 2.0
+        assert bits >= math.log2(3)
+    assert oracle.tq5_row_bytes(2560) == 512 and oracle.tq5_row_bytes(6912) == 1392
+
+
+def test_tq5_forward_equals_two_bit_forward():
+    # two independent encodings of the same ternary weights give the same
+    # integer products and outputs
+    rng = np.random.default_rng(13)
+    N, K, M = 33, 320, 3
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    p2, g2 = oracle.pack_weights(W)
+    p5, g5 = oracle.pack_weights_tq5(W)
+    assert g2 == g5
+    xq, s = oracle.quant_act(rng.standard_normal((M, K)).astype(np.float32))
+    y2, a2 = oracle.forward(p2, g2, xq, s, K)
+    y5, a5 = oracle.forward_tq5(p5, g5, xq, s, K)
+    assert np.array_equal(a2, a5) and np.array_equal(y2.view(np.uint32), y5.view(np.uint32))
