@@ -169,17 +169,27 @@ def x_bytes(L) -> int:
     return 2 if L.x_dtype == "bf16" else 4
 
 
-def layer_bytes(L) -> int:
+def tq5_row_bytes(K: int) -> int:
+    """Bytes per row of the base-3 weight format (the library's rule, restated
+    for the byte accounting): ceil(K/5) rounded up to 16."""
+    return ((K + 4) // 5 + 15) // 16 * 16
+
+
+def weight_bytes(L, fmt: str = "2bit") -> int:
+    return L.N * tq5_row_bytes(L.K) if fmt == "tq5" else L.N * L.K // 4
+
+
+def layer_bytes(L, fmt: str = "2bit") -> int:
     """Algorithmic HBM bytes of one layer step: read X, read the packed
     weights, write y (the per-token scales and gamma are counted too)."""
-    return L.M * L.K * x_bytes(L) + L.N * L.K // 4 + 4 * L.M * L.N + 4 * L.M + 4
+    return L.M * L.K * x_bytes(L) + weight_bytes(L, fmt) + 4 * L.M * L.N + 4 * L.M + 4
 
 
-def forward_kernel_bytes(L, fused: bool) -> int:
+def forward_kernel_bytes(L, fused: bool, fmt: str = "2bit") -> int:
     """Algorithmic bytes of the timed forward kernel: packed W and y, plus
     x_q and s read (two-call path) or X read and x_q, s written (fused)."""
     act = L.M * L.K * (x_bytes(L) + 1) if fused else L.M * L.K
-    return L.N * L.K // 4 + act + 4 * L.M + 4 * L.M * L.N + 4
+    return weight_bytes(L, fmt) + act + 4 * L.M + 4 * L.M * L.N + 4
 
 
 def layer_ops(L) -> int:
@@ -194,14 +204,15 @@ def metric_for(wl) -> tuple[str, str]:
 
 # ---------------------------------------------------------------- CPU oracle (baseline and reference arm)
 
-def run_oracle(wl, budget_s: float, steps: int | None = None, warmup: int = 0):
+def run_oracle(wl, budget_s: float, steps: int | None = None, warmup: int = 0, fmt: str = "2bit"):
     """Time the oracle on a bounded sample of the per-token step: a fraction f
     of each layer's output rows (all tokens).  Returns (value, f, s/step, steps)."""
     import oracle
 
     layers = []
     for i, L in enumerate(wl.layers):
-        p, g = oracle.pack_weights(workloads.layer_weights(wl, i).numpy())
+        W = workloads.layer_weights(wl, i).numpy()
+        p, g = oracle.pack_weights_tq5(W) if fmt == "tq5" else oracle.pack_weights(W)
         layers.append((L, p, g, workloads.x_as_f32_numpy(workloads.layer_activations(wl, i))))
     _, unit = metric_for(wl)
 
@@ -210,8 +221,12 @@ def run_oracle(wl, budget_s: float, steps: int | None = None, warmup: int = 0):
         for (L, p, g, X) in layers:
             rows = max(1, int(round(L.N * frac)))
             xq, s = oracle.quant_act(X)
-            oracle.forward(p[:rows], g, xq, s, L.K)
-            work += (L.M * L.K * x_bytes(L) + rows * L.K / 4 + 4 * L.M * rows) if unit == "GB/s" \
+            if fmt == "tq5":
+                oracle.forward_tq5(p[:rows], g, xq, s, L.K)
+            else:
+                oracle.forward(p[:rows], g, xq, s, L.K)
+            wrow = tq5_row_bytes(L.K) if fmt == "tq5" else L.K / 4
+            work += (L.M * L.K * x_bytes(L) + rows * wrow + 4 * L.M * rows) if unit == "GB/s" \
                 else 2.0 * L.M * rows * L.K
         return work
 
@@ -265,7 +280,8 @@ def run_gpu(args, dist, rank, world, local):
     l2 = props.L2_cache_size
     stream = torch.cuda.Stream(device=dev)  # graphs cannot be captured on the legacy default stream
     torch.cuda.set_stream(stream)
-    fused = args.path == "fused"
+    tq5 = args.format == "tq5"
+    fused = args.path == "fused" and not tq5  # the base-3 forward takes quantised activations
     nlayers = len(wl.layers)
 
     # ---- resident inputs: pack each layer's weights once (timed as the "pack" figure)
@@ -273,15 +289,16 @@ def run_gpu(args, dist, rank, world, local):
     pack_ms, pack_bytes = 0.0, 0
     for i, L in enumerate(wl.layers):
         W = workloads.layer_weights(wl, i).to(dev)
-        bl.bitlinear_pack_weights(W)  # warm
+        pack_fn = bl.bitlinear_pack_weights_tq5 if tq5 else bl.bitlinear_pack_weights
+        pack_fn(W)  # warm
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         e0.record(stream)
-        Wp, g = bl.bitlinear_pack_weights(W)
+        Wp, g = pack_fn(W)
         e1.record(stream)
         torch.cuda.synchronize()
         pack_ms += e0.elapsed_time(e1)
-        pack_bytes += 2 * 4 * L.N * L.K + L.N * L.K // 4
+        pack_bytes += 2 * 4 * L.N * L.K + weight_bytes(L, args.format)
         del W
         packed.append(Wp)
         gammas.append(g)
@@ -318,7 +335,10 @@ def run_gpu(args, dist, rank, world, local):
     workspace = torch.empty((max(ws_bytes, 16),), dtype=torch.uint8, device=dev)
 
     def layer_call(l, r, X=None):
-        if fused:
+        if tq5:
+            bl.bitlinear_quant_act(Xrot[l][r] if X is None else X, x_q=xqs[l], s=ss[l], stream=stream)
+            bl.bitlinear_forward_tq5(Wrot[l][r], gammas[l], xqs[l], ss[l], y=ys[l], stream=stream)
+        elif fused:
             bl.bitlinear_quant_forward_ws(Wrot[l][r], gammas[l], Xrot[l][r] if X is None else X, y=ys[l],
                                           x_q=xqs[l], s=ss[l], workspace=workspace, stream=stream)
         else:
@@ -336,6 +356,9 @@ def run_gpu(args, dist, rank, world, local):
         L = wl.layers[l]
         if fused and gemv_fused_layer(L):
             layer_call(l, r)
+        elif tq5:
+            xq, s = XQrot[l][r]
+            bl.bitlinear_forward_tq5(Wrot[l][r], gammas[l], xq, s, y=ys[l], stream=stream)
         else:
             xq, s = XQrot[l][r]
             bl.bitlinear_forward_ws(Wrot[l][r], gammas[l], xq, s, y=ys[l], workspace=workspace, stream=stream)
@@ -352,7 +375,10 @@ def run_gpu(args, dist, rank, world, local):
     torch.cuda.synchronize()
     bl.bitlinear_check_device_error(stream)
     # kernels per layer: fused GEMV 1; quantise + GEMV 2; quantise + fp16 expansion + GEMM 3
-    launches = K * sum((1 if fused else 2) if gemv_fused_layer(L) else 3 for L in wl.layers)
+    if tq5:  # quantise + base-3 forward, one pass per 4 tokens
+        launches = K * sum(1 + -(-L.M // 4) for L in wl.layers)
+    else:
+        launches = K * sum((1 if fused else 2) if gemv_fused_layer(L) else 3 for L in wl.layers)
     peaks, peak_src = load_peaks()
 
     if args.eager:
@@ -399,7 +425,7 @@ def run_gpu(args, dist, rank, world, local):
     torch.cuda.synchronize()
     verified = all(torch.equal(a, b) for a, b in zip(last, ys))
 
-    step_bytes = sum(layer_bytes(L) for L in wl.layers)
+    step_bytes = sum(layer_bytes(L, args.format) for L in wl.layers)
     step_ops = sum(layer_ops(L) for L in wl.layers)
     value = world * (step_bytes / (ms_per_step * 1e-3) / 1e9 if unit == "GB/s"
                      else step_ops / (ms_per_step * 1e-3) / 1e12)
@@ -421,16 +447,21 @@ def run_gpu(args, dist, rank, world, local):
         torch.cuda.synchronize()
         kern_us.append(a.elapsed_time(b) * 1e3 / (3 * kchunk))
         del g
-    kernel_names = ["gemv_kernel" if (L.M <= 4 and L.K <= 32768) else "gemm_tc_x16_kernel" for L in wl.layers]
-    kernel_variant = [gemm_variant(L, props.multi_processor_count) for L in wl.layers]
+    if tq5:
+        kernel_names = ["gemv_tq5_kernel" for L in wl.layers]
+        kernel_variant = ["gemv_tq5_kernel" for L in wl.layers]
+    else:
+        kernel_names = ["gemv_kernel" if (L.M <= 4 and L.K <= 32768) else "gemm_tc_x16_kernel" for L in wl.layers]
+        kernel_variant = [gemm_variant(L, props.multi_processor_count) for L in wl.layers]
     kname = max(set(kernel_names), key=lambda k: sum(t for t, n in zip(kern_us, kernel_names) if n == k))
     sel = [i for i, n in enumerate(kernel_names) if n == kname]
     tot_s = sum(kern_us[i] for i in sel) * 1e-6
-    if kname == "gemv_kernel":
-        kbytes = sum(forward_kernel_bytes(wl.layers[i], fused) for i in sel)
+    if kname in ("gemv_kernel", "gemv_tq5_kernel"):
+        kbytes = sum(forward_kernel_bytes(wl.layers[i], fused, args.format) for i in sel)
         roof = {"bound": "hbm", "achieved": round(kbytes / tot_s / 1e9, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "peak_source": f"{peak_src} hbm_gbs (copy)",
-                "algorithmic_bytes_per_launch": [forward_kernel_bytes(wl.layers[i], fused) for i in sel]}
+                "algorithmic_bytes_per_launch": [forward_kernel_bytes(wl.layers[i], fused, args.format)
+                                                 for i in sel]}
     else:
         kops = sum(layer_ops(wl.layers[i]) for i in sel)
         roof = {"bound": "tensor", "achieved": round(kops / tot_s / 1e12, 1), "peak": peaks["bf16_tflops"],
@@ -475,13 +506,20 @@ def run_gpu(args, dist, rank, world, local):
                                      "frac": round(nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
                                      "algorithmic_bytes": nbytes})
         for key, fl in (("forward_us", 0), ("forward_relu2_us", bl.BITLINEAR_RELU2)):
-            ffn[key].append(round(graph_us(lambda j, l=l, fl=fl: bl.bitlinear_quant_forward_ws(
-                Wrot[l][j % Rs[l]], gammas[l], Xrot[l][j % Rs[l]], y=ys[l], x_q=xqs[l], s=ss[l],
-                workspace=workspace, flags=fl, stream=stream)), 3))
+            if tq5:
+                prepare_kernel_inputs(l)
+                ffn[key].append(round(graph_us(lambda j, l=l, fl=fl: bl.bitlinear_forward_tq5(
+                    Wrot[l][j % Rs[l]], gammas[l], XQrot[l][j % Rs[l]][0], XQrot[l][j % Rs[l]][1], y=ys[l],
+                    flags=fl, stream=stream)), 3))
+            else:
+                ffn[key].append(round(graph_us(lambda j, l=l, fl=fl: bl.bitlinear_quant_forward_ws(
+                    Wrot[l][j % Rs[l]], gammas[l], Xrot[l][j % Rs[l]], y=ys[l], x_q=xqs[l], s=ss[l],
+                    workspace=workspace, flags=fl, stream=stream)), 3))
     bl.bitlinear_check_device_error(stream)
     ffn["note"] = ("rmsnorm_quant: bitlinear_rmsnorm_quant_act on each layer's X with a per-channel gain, bytes = "
                    "X read + x_q write + s + gain, frac of the measured copy bandwidth; forward(_relu2)_us: "
-                   "bitlinear_quant_forward_ws without and with BITLINEAR_RELU2")
+                   + ("bitlinear_forward_tq5 (quantised activations)" if tq5 else "bitlinear_quant_forward_ws")
+                   + " without and with BITLINEAR_RELU2")
 
     e2e = run_e2e(bl, wl, step, Xs_host, y_all, K, Wm, stream, dist, world, unit, step_bytes, step_ops)
 
@@ -495,9 +533,11 @@ def run_gpu(args, dist, rank, world, local):
                        f"{R} copies ({R * (p.numel() + x.numel() * x.element_size()) / 2**20:.0f} MiB)"
                        for R, p, x in zip(Rs, packed, Xs)) + f" > 2x L2 ({l2 / 2**20:.0f} MiB)",
                    "launch": f"CUDA graphs of the C-ABI calls, {chunk} steps per graph",
-                   "path": ("bitlinear_quant_forward_ws (one fused quantise+GEMV kernel for M <= 4; quantise, fp16 "
-                            "expansion of x_q and tcgen05 GEMM otherwise)") if fused
-                   else "bitlinear_quant_act + bitlinear_forward_ws",
+                   "path": ("bitlinear_quant_act + bitlinear_forward_tq5" if tq5 else
+                            ("bitlinear_quant_forward_ws (one fused quantise+GEMV kernel for M <= 4; quantise, fp16 "
+                             "expansion of x_q and tcgen05 GEMM otherwise)") if fused
+                            else "bitlinear_quant_act + bitlinear_forward_ws"),
+                   "weights": ("base-3, five per byte (1.6 bits per weight)" if tq5 else "2-bit, four per byte"),
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,
         "e2e": e2e,
@@ -522,7 +562,7 @@ def run_gpu_eager(args, bl, wl, step, K, stream, dist, world, unit, metric, Rs, 
     torch.cuda.synchronize()
     barrier(dist)
     ms = max_over_ranks(dist, a.elapsed_time(b)) / K
-    step_bytes = sum(layer_bytes(L) for L in wl.layers)
+    step_bytes = sum(layer_bytes(L, args.format) for L in wl.layers)
     step_ops = sum(layer_ops(L) for L in wl.layers)
     value = world * (step_bytes / (ms * 1e-3) / 1e9 if unit == "GB/s" else step_ops / (ms * 1e-3) / 1e12)
     return {"metric": metric, "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": K,
@@ -609,6 +649,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", default="fused", choices=["fused", "separate"],
                     help="fused: bitlinear_quant_forward; separate: bitlinear_quant_act + bitlinear_forward")
+    ap.add_argument("--format", default="2bit", choices=["2bit", "tq5"],
+                    help="weight format: 2-bit (four per byte) or base-3 (five per byte, the forward on x_q)")
     ap.add_argument("--eager", action="store_true",
                     help="launch every step eagerly instead of from CUDA graphs (for profilers)")
     ap.add_argument("--layers", default="", help="comma-separated layer indices of the workload (default: all)")
@@ -633,7 +675,8 @@ def main():
     if args.impl == "reference":
         # this build's reference arm is the CPU oracle on the host cores; rank 0 only
         if rank == 0:
-            value, frac, sec_step, n = run_oracle(wl, budget_s=120.0, steps=args.steps, warmup=args.warmup)
+            value, frac, sec_step, n = run_oracle(wl, budget_s=120.0, steps=args.steps, warmup=args.warmup,
+                                                  fmt=args.format)
             line = {"impl": "reference", "metric": metric, "value": round(value, 4), "unit": unit,
                     "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                     "ms_per_step": round(sec_step * 1e3, 4), "higher_is_better": True, "scaling": "weak",
@@ -654,7 +697,7 @@ def main():
         raise SystemExit("bench.py needs a CUDA device (the BitLinear kernels have no CPU path)")
     line = run_gpu(args, dist, rank, world, local)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        value, frac, sec_step, n = run_oracle(wl, budget_s=args.cpu_seconds)
+        value, frac, sec_step, n = run_oracle(wl, budget_s=args.cpu_seconds, fmt=args.format)
         line["cpu_baseline"] = {"value": round(value, 4), "unit": unit, "cores": 1, "kind": "oracle",
                                 "sample": f"{n} oracle steps on {frac:.2%} of each layer's output rows "
                                           f"(all tokens), single thread, {n * sec_step:.1f} s"}

@@ -76,6 +76,9 @@ typedef enum { BL_F32 = 0, BL_BF16 = 1 } bl_dtype;
  * partial sum of the product is an integer that fp32 holds exactly. */
 #define BITLINEAR_MAX_K 131072
 
+/* Largest K of the base-3 weight format's forward (bitlinear_forward_tq5). */
+#define BITLINEAR_TQ5_MAX_K 40960
+
 /*
  * bitlinear_pack_workspace_bytes -- bytes of device workspace that
  * bitlinear_pack_weights needs for an [N, K] matrix (a small constant).
@@ -129,6 +132,49 @@ bl_status bitlinear_pack_weights(const float* W, int64_t N, int64_t K, float eps
  */
 bl_status bitlinear_pack_weights_noalloc(const float* W, int64_t N, int64_t K, float eps, uint8_t* W_packed,
                                          float* gamma, cudaStream_t stream);
+
+/*
+ * bitlinear_tq5_row_bytes -- bytes per row of the base-3 weight format:
+ * ceil(K / 5) rounded up to a multiple of 16 (0 for K < 1).
+ */
+int64_t bitlinear_tq5_row_bytes(int64_t K);
+
+/*
+ * bitlinear_pack_weights_tq5 -- bitlinear_pack_weights written in the base-3
+ * format: five ternary weights per byte, 1.6 bits per weight, close to the
+ * log2(3) = 1.58 bits of information in one weight (yousumm.com transcript,
+ * the GPU-plumbing paragraph; anthology note-168, "What it does").  Byte j
+ * of row n holds sum_{i<5} (W_q[n, 5j+i] + 1) * 3^i, least significant digit
+ * first, a value in 0..242; positions at or past K count as W_q = 0, and each
+ * row is padded with 121 (five zero codes) to bitlinear_tq5_row_bytes(K)
+ * bytes.  gamma and W_q are those of bitlinear_pack_weights bit for bit.
+ *
+ *   W, N, K, eps, gamma, workspace, workspace_bytes, stream
+ *            as for bitlinear_pack_weights (K % 4 == 0, N * K <= 2^32)
+ *   W_tq5    out  uint8 [N, bitlinear_tq5_row_bytes(K)], 16-byte aligned
+ */
+bl_status bitlinear_pack_weights_tq5(const float* W, int64_t N, int64_t K, float eps, uint8_t* W_tq5, float* gamma,
+                                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * bitlinear_forward_tq5 -- bitlinear_forward from base-3 packed weights:
+ * acc = W_q . x_q exact in int32, y = fp32(fp32(acc) * fp32(gamma / s[m])),
+ * bit-identical to bitlinear_forward on the 2-bit packing of the same W_q.
+ * Tokens are taken up to four at a time and every pass streams the weights
+ * once, so the format serves decode (a few tokens).
+ *
+ *   W_tq5     in   uint8 [N, bitlinear_tq5_row_bytes(K)], 16-byte aligned
+ *   gamma, x_q, s, y, acc   as for bitlinear_forward
+ *   M, N, K   in   M >= 1, 1 <= N <= 2048 * (number of SMs), K % 16 == 0,
+ *                  16 <= K <= BITLINEAR_TQ5_MAX_K
+ *   flags     in   0 or BITLINEAR_RELU2
+ *
+ * Errors: BL_ERR_INVALID_ARG (null pointer, size < 1, unknown flag),
+ * BL_ERR_UNSUPPORTED_SHAPE, BL_ERR_MISALIGNED, BL_ERR_CUDA.
+ */
+bl_status bitlinear_forward_tq5(const uint8_t* W_tq5, const float* gamma, const int8_t* x_q, const float* s,
+                                int64_t M, int64_t N, int64_t K, float* y, int32_t* acc, unsigned flags,
+                                cudaStream_t stream);
 
 /*
  * bitlinear_quant_act -- per-token absmax quantisation of activations to int8

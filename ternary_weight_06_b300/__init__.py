@@ -41,7 +41,9 @@ __all__ = [
     "BITLINEAR_WEIGHTS_RESIDENT",
     "BITLINEAR_TEST_STALL",
     "BITLINEAR_RELU2",
-    "bitlinear_rmsnorm_quant_act",
+    "bitlinear_tq5_row_bytes",
+    "bitlinear_pack_weights_tq5",
+    "bitlinear_forward_tq5",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -59,11 +61,15 @@ EXPORTED_SYMBOLS = (
     "bitlinear_pack_weights",
     "bitlinear_pack_weights_noalloc",
     "bitlinear_quant_act",
+    "bitlinear_rmsnorm_quant_act",
     "bitlinear_forward",
     "bitlinear_quant_forward",
     "bitlinear_forward_workspace_bytes",
     "bitlinear_forward_ws",
     "bitlinear_quant_forward_ws",
+    "bitlinear_tq5_row_bytes",
+    "bitlinear_pack_weights_tq5",
+    "bitlinear_forward_tq5",
     "bitlinear_check_device_error",
     "bitlinear_status_string",
 )
@@ -89,6 +95,12 @@ def _load() -> ctypes.CDLL:
     L.bitlinear_quant_act.restype = i32
     L.bitlinear_rmsnorm_quant_act.argtypes = [P, i32, i64, i64, P, f32, P, P, P]
     L.bitlinear_rmsnorm_quant_act.restype = i32
+    L.bitlinear_tq5_row_bytes.argtypes = [i64]
+    L.bitlinear_tq5_row_bytes.restype = i64
+    L.bitlinear_pack_weights_tq5.argtypes = [P, i64, i64, f32, P, P, P, sz, P]
+    L.bitlinear_pack_weights_tq5.restype = i32
+    L.bitlinear_forward_tq5.argtypes = [P, P, P, P, i64, i64, i64, P, P, ctypes.c_uint, P]
+    L.bitlinear_forward_tq5.restype = i32
     L.bitlinear_forward.argtypes = [P, P, P, P, i64, i64, i64, P, P, P]
     L.bitlinear_forward.restype = i32
     L.bitlinear_pack_weights_noalloc.argtypes = [P, i64, i64, f32, P, P, P]
@@ -165,6 +177,52 @@ def bitlinear_pack_weights(W: torch.Tensor, eps: float = 1e-5, W_packed: torch.T
                                       _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
                                       _stream(stream)), "bitlinear_pack_weights")
     return W_packed, gamma
+
+
+def bitlinear_tq5_row_bytes(K: int) -> int:
+    """Bytes per row of the base-3 weight format (five weights per byte)."""
+    return int(get_lib().bitlinear_tq5_row_bytes(int(K)))
+
+
+def bitlinear_pack_weights_tq5(W: torch.Tensor, eps: float = 1e-5, W_tq5: torch.Tensor | None = None,
+                               gamma: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None):
+    """As :func:`bitlinear_pack_weights`, written five weights per byte in base 3.
+    Returns (W_tq5 uint8 [N, bitlinear_tq5_row_bytes(K)], gamma fp32 [1])."""
+    N, K = W.shape
+    if W_tq5 is None:
+        W_tq5 = torch.empty((N, bitlinear_tq5_row_bytes(K)), dtype=torch.uint8, device=W.device)
+    if gamma is None:
+        gamma = torch.empty((1,), dtype=torch.float32, device=W.device)
+    ws_bytes = bitlinear_pack_workspace_bytes(N, K)
+    if workspace is None:
+        workspace = torch.empty((ws_bytes,), dtype=torch.uint8, device=W.device)
+    _check(get_lib().bitlinear_pack_weights_tq5(_dev(W, "W", torch.float32), N, K, float(eps),
+                                                _dev(W_tq5, "W_tq5", torch.uint8), _dev(gamma, "gamma", torch.float32),
+                                                _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+                                                _stream(stream)), "bitlinear_pack_weights_tq5")
+    return W_tq5, gamma
+
+
+def bitlinear_forward_tq5(W_tq5: torch.Tensor, gamma: torch.Tensor, x_q: torch.Tensor, s: torch.Tensor,
+                          y: torch.Tensor | None = None, acc: torch.Tensor | bool | None = None, flags: int = 0,
+                          stream=None):
+    """:func:`bitlinear_forward` from base-3 packed weights (W_tq5 uint8
+    [N, bitlinear_tq5_row_bytes(K)]).  Returns y, or (y, acc) with ``acc``."""
+    N, pitch = W_tq5.shape
+    M, K = x_q.shape
+    if pitch != bitlinear_tq5_row_bytes(K):
+        raise ValueError(f"W_tq5 rows have {pitch} bytes but K = {K} needs {bitlinear_tq5_row_bytes(K)}")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x_q.device)
+    want_acc = acc is not None and acc is not False
+    if acc is True:
+        acc = torch.empty((M, N), dtype=torch.int32, device=x_q.device)
+    acc_ptr = _dev(acc, "acc", torch.int32) if want_acc else None
+    _check(get_lib().bitlinear_forward_tq5(_dev(W_tq5, "W_tq5", torch.uint8), _dev(gamma, "gamma", torch.float32),
+                                           _dev(x_q, "x_q", torch.int8), _dev(s, "s", torch.float32), M, N, K,
+                                           _dev(y, "y", torch.float32), acc_ptr, int(flags), _stream(stream)),
+           "bitlinear_forward_tq5")
+    return (y, acc) if want_acc else y
 
 
 def bitlinear_quant_act(X: torch.Tensor, x_q: torch.Tensor | None = None, s: torch.Tensor | None = None,

@@ -72,6 +72,44 @@ bl_status bitlinear_pack_weights(const float* W, int64_t N, int64_t K, float eps
                                    static_cast<bl::PackWorkspace*>(workspace), d.num_sms, stream));
 }
 
+int64_t bitlinear_tq5_row_bytes(int64_t K) {
+  if (K < 1) return 0;
+  return ((K + 4) / 5 + 15) / 16 * 16;
+}
+
+bl_status bitlinear_pack_weights_tq5(const float* W, int64_t N, int64_t K, float eps, uint8_t* W_tq5, float* gamma,
+                                     void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!W || !W_tq5 || !gamma || !workspace) return BL_ERR_INVALID_ARG;
+  if (N < 1 || K < 1) return BL_ERR_INVALID_ARG;
+  if (!std::isfinite(eps) || !(eps > 0.0f)) return BL_ERR_INVALID_ARG;
+  if (K % 4 != 0 || K < 4) return BL_ERR_UNSUPPORTED_SHAPE;
+  if (N > (int64_t)(1ull << 32) / K) return BL_ERR_UNSUPPORTED_SHAPE;  // N*K <= 2^32
+  if (!aligned(W, 16) || !aligned(W_tq5, 16) || !aligned(gamma, 4) || !aligned(workspace, 16))
+    return BL_ERR_MISALIGNED;
+  if (workspace_bytes < bl::kPackWorkspaceBytes) return BL_ERR_WORKSPACE;
+  DeviceInfo d;
+  if (bl_status st = device_info(&d)) return st;
+  return from_cuda(bl::launch_pack_tq5(W, N, K, bitlinear_tq5_row_bytes(K), eps, W_tq5, gamma,
+                                       static_cast<bl::PackWorkspace*>(workspace), d.num_sms, stream));
+}
+
+bl_status bitlinear_forward_tq5(const uint8_t* W_tq5, const float* gamma, const int8_t* x_q, const float* s,
+                                int64_t M, int64_t N, int64_t K, float* y, int32_t* acc, unsigned flags,
+                                cudaStream_t stream) {
+  if (!W_tq5 || !gamma || !x_q || !s || !y) return BL_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1) return BL_ERR_INVALID_ARG;
+  if (flags & ~BITLINEAR_RELU2) return BL_ERR_INVALID_ARG;
+  if (K % 16 != 0 || K > bl::kTq5MaxK || M > INT32_MAX) return BL_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(W_tq5, 16) || !aligned(x_q, 16) || !aligned(y, 16) || !aligned(gamma, 4) || !aligned(s, 4) ||
+      (acc && !aligned(acc, 16)))
+    return BL_ERR_MISALIGNED;
+  DeviceInfo d;
+  if (bl_status st = device_info(&d)) return st;
+  if (N > (int64_t)2048 * d.num_sms) return BL_ERR_UNSUPPORTED_SHAPE;  // per-CTA row sums must fit shared memory
+  bl::ForwardArgs a{W_tq5, gamma, x_q, s, M, N, K, y, acc, d.err, (flags & BITLINEAR_RELU2) != 0};
+  return from_cuda(bl::launch_gemv_tq5(a, bitlinear_tq5_row_bytes(K), d.num_sms, stream));
+}
+
 bl_status bitlinear_quant_act(const void* X, bl_dtype dtype, int64_t M, int64_t K, int8_t* x_q, float* s,
                               cudaStream_t stream) {
   if (!X || !x_q || !s) return BL_ERR_INVALID_ARG;

@@ -21,6 +21,11 @@ constexpr size_t kPackWorkspaceBytes = 512;
 cudaError_t launch_pack(const float* W, uint64_t n, float eps, uint8_t* Wp, float* gamma, PackWorkspace* ws,
                         int num_sms, cudaStream_t stream);
 
+// The same gamma and ternarisation, written in the base-3 format (five
+// weights per byte, rows of `pitch` bytes).  K % 4 == 0.
+cudaError_t launch_pack_tq5(const float* W, int64_t N, int64_t K, int64_t pitch, float eps, uint8_t* Wt,
+                            float* gamma, PackWorkspace* ws, int num_sms, cudaStream_t stream);
+
 // Per-token quantisation.  From 256 tokens up (K % 16 == 0, 16-byte aligned
 // buffers) a persistent kernel with rows staged in shared memory by bulk
 // copies, one team of warps per row; else one CTA per row.  err: the device
@@ -50,6 +55,10 @@ struct ForwardArgs {
   bool relu2 = false;  // epilogue applies the squared ReLU
 };
 
+// The forward from base-3 packed weights (five per byte, rows of `pitch`
+// bytes), for any M in passes of up to 4 tokens; K % 16 == 0, K <= 40960.
+cudaError_t launch_gemv_tq5(const ForwardArgs& a, int64_t pitch, int num_sms, cudaStream_t stream);
+
 // Streaming GEMV for a few tokens (tokens are taken in groups of <= 4; K <= 32768).
 cudaError_t launch_gemv(const ForwardArgs& a, int num_sms, cudaStream_t stream);
 
@@ -61,6 +70,7 @@ cudaError_t launch_gemv_fused(const ForwardArgs& a, const void* X, bool x_bf16, 
 
 constexpr int64_t kGemvMaxTokens = 4;
 constexpr int64_t kGemvMaxK = 32768;
+constexpr int64_t kTq5MaxK = 40960;  // 16 K slices x 32 lanes x 4 words x 20 weights
 
 // Tensor-core GEMM (tcgen05) for more tokens than the GEMV handles well.
 cudaError_t launch_gemm_tc(const ForwardArgs& a, int num_sms, cudaStream_t stream);

@@ -228,7 +228,49 @@ __global__ void __launch_bounds__(kPackThreads) ternarize_pack_kernel(const floa
   }
 }
 
+// Base-3 packing, five weights per byte: byte j of row n is the sum over
+// i < 5 of code(W[n, 5j + i]) * 3^i, with the code of the 2-bit format (q + 1,
+// the same zero band); positions at or past K count as code 1 (q = 0), so a
+// padding byte is 121.  One thread per output byte; a warp's five loads fall
+// on the same 640 contiguous bytes of W, so the last four hit L1.
+__global__ void __launch_bounds__(kPackThreads) ternarize_pack_tq5_kernel(const float* __restrict__ W, int64_t N,
+                                                                           int64_t K, int64_t pitch,
+                                                                           const PackWorkspace* __restrict__ ws,
+                                                                           uint8_t* __restrict__ Wt) {
+  const uint32_t T = ws->thresh_bits;
+  const int64_t total = N * pitch;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t n = idx / pitch, j = idx - n * pitch;
+    const float* row = W + n * K;
+    uint32_t v = 0, w = 1;
+#pragma unroll
+    for (int i = 0; i < 5; ++i) {
+      const int64_t k = 5 * j + i;
+      v += (k < K ? ternary_code(__ldg(row + k), T) : 1u) * w;
+      w *= 3u;
+    }
+    Wt[idx] = (uint8_t)v;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_pack_tq5(const float* W, int64_t N, int64_t K, int64_t pitch, float eps, uint8_t* Wt,
+                            float* gamma, PackWorkspace* ws, int num_sms, cudaStream_t stream) {
+  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(PackWorkspace), stream);
+  if (e != cudaSuccess) return e;
+  const uint64_t n = (uint64_t)N * (uint64_t)K, n4 = n / 4;
+  const uint64_t want = (n4 + kPackThreads - 1) / kPackThreads;
+  const int grid = (int)(want < (uint64_t)num_sms * 8 ? (want ? want : 1) : (uint64_t)num_sms * 8);
+  absmean_hist_kernel<<<grid, kPackThreads, 0, stream>>>(reinterpret_cast<const float4*>(W), n4, ws);
+  absmean_finish_kernel<<<1, 32, 0, stream>>>(ws, n, eps, gamma);
+  const uint64_t bytes = (uint64_t)N * (uint64_t)pitch;
+  const uint64_t want2 = (bytes + kPackThreads - 1) / kPackThreads;
+  const int grid2 = (int)(want2 < (uint64_t)num_sms * 16 ? want2 : (uint64_t)num_sms * 16);
+  ternarize_pack_tq5_kernel<<<grid2, kPackThreads, 0, stream>>>(W, N, K, pitch, ws, Wt);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_pack(const float* W, uint64_t n, float eps, uint8_t* Wp, float* gamma, PackWorkspace* ws,
                         int num_sms, cudaStream_t stream) {

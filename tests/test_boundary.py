@@ -35,7 +35,8 @@ def test_header_declares_the_boundary():
     for required in ("bitlinear_pack_weights", "bitlinear_quant_act", "bitlinear_forward",
                      "bitlinear_quant_forward", "bitlinear_check_device_error", "bitlinear_status_string",
                      "bitlinear_pack_workspace_bytes", "bitlinear_forward_workspace_bytes", "bitlinear_forward_ws",
-                     "bitlinear_quant_forward_ws"):
+                     "bitlinear_quant_forward_ws", "bitlinear_rmsnorm_quant_act", "bitlinear_tq5_row_bytes",
+                     "bitlinear_pack_weights_tq5", "bitlinear_forward_tq5"):
         assert required in names
 
 
@@ -43,7 +44,7 @@ def test_library_exports_every_declared_symbol(bl):
     lib = ctypes.CDLL(bl.LIB_PATH)
     for name in declared_functions():
         assert hasattr(lib, name), f"{name} declared in bitlinear.h but not exported"
-    assert set(bl.EXPORTED_SYMBOLS) <= set(declared_functions())
+    assert set(bl.EXPORTED_SYMBOLS) == set(declared_functions())
 
 
 def test_status_strings(bl):
@@ -201,6 +202,48 @@ def test_rmsnorm_quant_validation(bl):
     assert f(GOOD + 2, 0, 2, 64, None, 1e-5, GOOD, GOOD, None) == bl.BL_ERR_MISALIGNED  # fp32 needs 4
     assert f(GOOD, 1, 2, 64, GOOD + 2, 1e-5, GOOD, GOOD, None) == bl.BL_ERR_MISALIGNED
     assert qfwd(bl, flags=bl.BITLINEAR_RELU2 | 4) == bl.BL_ERR_INVALID_ARG
+
+
+def test_tq5_row_bytes(bl):
+    f = bl.bitlinear_tq5_row_bytes
+    assert [f(K) for K in (0, 1, 5, 80, 81, 2560, 6912, 8192, 28672)] == [0, 16, 16, 16, 32, 512, 1392, 1648, 5744]
+
+
+def pack_tq5(bl, W=GOOD, N=8, K=64, eps=1e-5, Wt=GOOD, g=GOOD, ws=GOOD, ws_bytes=4096):
+    return bl.get_lib().bitlinear_pack_weights_tq5(W, N, K, eps, Wt, g, ws, ws_bytes, None)
+
+
+def test_pack_tq5_validation(bl):
+    for kw in ("W", "Wt", "g", "ws"):
+        assert pack_tq5(bl, **{kw: None}) == bl.BL_ERR_INVALID_ARG, kw
+    assert pack_tq5(bl, N=0) == bl.BL_ERR_INVALID_ARG
+    assert pack_tq5(bl, eps=0.0) == bl.BL_ERR_INVALID_ARG
+    assert pack_tq5(bl, eps=float("inf")) == bl.BL_ERR_INVALID_ARG
+    assert pack_tq5(bl, K=66) == bl.BL_ERR_UNSUPPORTED_SHAPE
+    assert pack_tq5(bl, N=2**20, K=2**13) == bl.BL_ERR_UNSUPPORTED_SHAPE  # N*K > 2^32
+    assert pack_tq5(bl, W=GOOD + 4) == bl.BL_ERR_MISALIGNED
+    assert pack_tq5(bl, Wt=GOOD + 8) == bl.BL_ERR_MISALIGNED
+    assert pack_tq5(bl, ws_bytes=16) == bl.BL_ERR_WORKSPACE
+
+
+def fwd_tq5(bl, Wt=GOOD, g=GOOD, xq=GOOD, s=GOOD, M=1, N=16, K=64, y=GOOD, acc=None, flags=0):
+    return bl.get_lib().bitlinear_forward_tq5(Wt, g, xq, s, M, N, K, y, acc, flags, None)
+
+
+def test_forward_tq5_validation(bl):
+    for kw in ("Wt", "g", "xq", "s", "y"):
+        assert fwd_tq5(bl, **{kw: None}) == bl.BL_ERR_INVALID_ARG, kw
+    assert fwd_tq5(bl, M=0) == bl.BL_ERR_INVALID_ARG
+    assert fwd_tq5(bl, N=0) == bl.BL_ERR_INVALID_ARG
+    assert fwd_tq5(bl, flags=bl.BITLINEAR_WEIGHTS_RESIDENT) == bl.BL_ERR_INVALID_ARG
+    assert fwd_tq5(bl, K=8) == bl.BL_ERR_UNSUPPORTED_SHAPE
+    assert fwd_tq5(bl, K=40960 + 16) == bl.BL_ERR_UNSUPPORTED_SHAPE
+    assert fwd_tq5(bl, M=2**31) == bl.BL_ERR_UNSUPPORTED_SHAPE
+    assert fwd_tq5(bl, Wt=GOOD + 8) == bl.BL_ERR_MISALIGNED
+    assert fwd_tq5(bl, xq=GOOD + 4) == bl.BL_ERR_MISALIGNED
+    assert fwd_tq5(bl, y=GOOD + 4) == bl.BL_ERR_MISALIGNED
+    assert fwd_tq5(bl, s=GOOD + 2) == bl.BL_ERR_MISALIGNED
+    assert fwd_tq5(bl, acc=GOOD + 8) == bl.BL_ERR_MISALIGNED
 
 
 def test_python_binding_rejects_cpu_tensors(bl):
