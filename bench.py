@@ -47,6 +47,12 @@ GRAPH_CHUNK = 500  # steps per captured graph
 
 # ---------------------------------------------------------------- helpers
 
+# Rates of the legacy warp-level MMA on this GPU, measured with a register-only
+# mma.sync loop over all SMs (m16n8k32 s8, m16n8k16 f16 with fp32 accumulate):
+# the recompiled-kernel baseline a tcgen05 kernel is meant to beat.
+LEGACY_MMA_SYNC = {"s8_tops": 139.5, "f16_tflops": 446.0}
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -467,6 +473,10 @@ def run_gpu(args, dist, rank, world, local):
         roof = {"bound": "tensor", "achieved": round(kops / tot_s / 1e12, 1), "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "peak_source": f"{peak_src} bf16_tflops burst (kind::f16 runs at the bf16 rate)",
                 "algorithmic_ops_per_launch": [layer_ops(wl.layers[i]) for i in sel]}
+        roof["vs_legacy_mma_sync"] = {
+            "s8": round(roof["achieved"] / LEGACY_MMA_SYNC["s8_tops"], 2),
+            "f16": round(roof["achieved"] / LEGACY_MMA_SYNC["f16_tflops"], 2),
+            "rates": LEGACY_MMA_SYNC}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
     roof["traffic"] = ncu_traffic(kname, args.workload) if not args.layers else None
     roof["kernel"] = kname
@@ -495,6 +505,15 @@ def run_gpu(args, dist, rank, world, local):
         torch.cuda.synchronize()
         del g
         return a.elapsed_time(b) * 1e3 / (3 * kchunk)
+
+    # the per-token quantisation (a3) alone, per layer: X read, x_q and s written
+    quant = []
+    for l, L in enumerate(wl.layers):
+        us = graph_us(lambda j, l=l: bl.bitlinear_quant_act(Xrot[l][j % Rs[l]], x_q=xqs[l], s=ss[l], stream=stream))
+        nbytes = L.M * L.K * (Xs[l].element_size() + 1) + 4 * L.M
+        quant.append({"us": round(us, 3), "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1),
+                      "frac": round(nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4), "algorithmic_bytes": nbytes})
+    bl.bitlinear_check_device_error(stream)
 
     ffn = {"rmsnorm_quant": [], "forward_us": [], "forward_relu2_us": []}
     for l, L in enumerate(wl.layers):
@@ -544,6 +563,9 @@ def run_gpu(args, dist, rank, world, local):
         "gpu_launches": launches,
         "verified": verified,
         "clocks": clocks,
+        "quant": {"per_layer": quant,
+                  "note": "bitlinear_quant_act alone per layer, graph-replayed over the rotating X copies; bytes = "
+                          "X read + x_q written + s, frac of the measured copy bandwidth"},
         "ffn": ffn,
         "pack": {"ms": round(pack_ms, 4), "GB/s": round(pack_bytes / (pack_ms * 1e-3) / 1e9, 1),
                  "note": "gamma + ternarise + pack of every layer (one call each), outside the step"},
