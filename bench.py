@@ -695,7 +695,7 @@ def main():
     metric, unit = metric_for(wl)
 
     if args.impl == "reference":
-        # this build's reference arm is the CPU oracle on the host cores; rank 0 only
+        # the reference arm is the CPU oracle on the host cores; rank 0 only
         if rank == 0:
             value, frac, sec_step, n = run_oracle(wl, budget_s=120.0, steps=args.steps, warmup=args.warmup,
                                                   fmt=args.format)
