@@ -36,7 +36,7 @@ def _init(rank: int, world: int, port: int):
     dist.init_process_group("gloo", rank=rank, world_size=world)
 
 
-def _row_shard_worker(rank: int, world: int, port: int, result_q):
+def _row_shard_worker(rank: int, world: int, port: int, result_q, fmt: str = "2bit"):
     sys.path.insert(0, ROOT)
     import oracle
     import workloads
@@ -47,30 +47,35 @@ def _row_shard_worker(rank: int, world: int, port: int, result_q):
         W, X = workloads.layer_inputs(wl, 0)
         N, K = W.shape
         # gamma is a property of the whole matrix: every rank packs with the global gamma
-        packed, gamma = oracle.pack_weights(W.numpy())
+        pack = oracle.pack_weights_tq5 if fmt == "tq5" else oracle.pack_weights
+        fwd = oracle.forward_tq5 if fmt == "tq5" else oracle.forward
+        packed, gamma = pack(W.numpy())
         xq, s = oracle.quant_act(workloads.x_as_f32_numpy(X))
         # uneven split on purpose (N = 256 -> 100 + 156 rows)
         bounds = [0, 100, N]
         lo, hi = bounds[rank], bounds[rank + 1]
-        y_part, acc_part = oracle.forward(packed[lo:hi], gamma, xq, s, K)
+        y_part, acc_part = fwd(packed[lo:hi], gamma, xq, s, K)
         pieces = [None] * world
         dist.all_gather_object(pieces, (lo, y_part, acc_part))
         if rank == 0:
             pieces.sort(key=lambda p: p[0])
             y_cat = np.concatenate([p[1] for p in pieces], axis=1)
             acc_cat = np.concatenate([p[2] for p in pieces], axis=1)
-            y_ref, acc_ref = oracle.forward(packed, gamma, xq, s, K)
+            y_ref, acc_ref = fwd(packed, gamma, xq, s, K)
             result_q.put((bool(np.array_equal(acc_cat, acc_ref)),
                           bool(np.array_equal(y_cat.view(np.uint32), y_ref.view(np.uint32)))))
     finally:
         dist.destroy_process_group()
 
 
-def test_row_sharded_forward_equals_unsplit_gloo():
+@pytest.mark.parametrize("fmt", ["2bit", "tq5"])
+def test_row_sharded_forward_equals_unsplit_gloo(fmt):
+    """both weight formats shard by output rows: a row block of the packed
+    array is the packing of that row block"""
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_row_shard_worker, args=(r, 2, port, q)) for r in range(2)]
+    procs = [ctx.Process(target=_row_shard_worker, args=(r, 2, port, q, fmt)) for r in range(2)]
     for p in procs:
         p.start()
     for p in procs:
