@@ -610,6 +610,11 @@ RowPlan plan_rows_staged(int64_t M, int64_t K, int num_sms) {
     S = (int)std::max<int64_t>(1, rows_per_team);  // no deeper ring than the rows a team gets
   }
   if (occ * nteams * T < kRowWarpsPerSmMin) return p;
+  // the leader refills a stage at the top of the next row, after the team
+  // barrier: with one stage that refill would come after the wait for the row
+  // it carries, so a one-stage ring serves at most one row per team
+  const int64_t rows_per_team = (M + (int64_t)grid * nteams - 1) / ((int64_t)grid * nteams);
+  if (S == 1 && rows_per_team > 1) return p;
   p.ok = true;
   p.team = T;
   p.warps = nteams * T;

@@ -191,6 +191,23 @@ def test_quant_many_tokens(bl, dtype, M, K):
     bl.bitlinear_check_device_error()
 
 
+@pytest.mark.parametrize("dtype,M,K", [(torch.float32, 512, 28672), (torch.bfloat16, 300, 51200)])
+def test_quant_many_tokens_long_rows(bl, dtype, M, K):
+    """rows too long for a two-stage ring: the quantisation must not take a
+    one-stage ring with several rows per team (each would wait for a copy not
+    yet issued); it takes the one-CTA-per-row kernel instead"""
+    g = torch.Generator().manual_seed(K)
+    X = torch.randn((M, K), generator=g)
+    X[M // 2] = 0.0
+    X = X.to(dtype)
+    xq_ref, s_ref = oracle.quant_act(X.to(torch.float32).numpy())
+    xq, s = bl.bitlinear_quant_act(gpu(X))
+    torch.cuda.synchronize()
+    bl.bitlinear_check_device_error()
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(xq.cpu().numpy(), xq_ref)
+
+
 # ---------------------------------------------------------------- forward
 
 def sample_rows(M: int, limit: int, seed: int) -> np.ndarray:
