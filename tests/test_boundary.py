@@ -47,6 +47,16 @@ def test_library_exports_every_declared_symbol(bl):
     assert set(bl.EXPORTED_SYMBOLS) == set(declared_functions())
 
 
+def test_binding_constants_match_the_header(bl):
+    text = open(HEADER).read()
+    defines = dict(re.findall(r"#define\s+(BITLINEAR_\w+)\s+(\S+)", text))
+    for name in ("BITLINEAR_WEIGHTS_RESIDENT", "BITLINEAR_RELU2", "BITLINEAR_TEST_STALL"):
+        assert int(defines[name].rstrip("uU"), 0) == getattr(bl, name), name
+    enum = dict(re.findall(r"\b(BL_\w+)\s*=\s*(\d+)", text))
+    for name, value in enum.items():
+        assert getattr(bl, name) == int(value), name
+
+
 def test_status_strings(bl):
     for code in range(7):
         s = bl.bitlinear_status_string(code)
