@@ -67,6 +67,8 @@ def _load():
         lib.oracle_matmul_int.argtypes = [P, P, i64, i64, i64, P]
         lib.oracle_dequant.argtypes = [P, ctypes.c_float, P, i64, i64, P]
         lib.oracle_rmsnorm_quant_act.argtypes = [P, i64, i64, P, ctypes.c_float, ctypes.c_float, P, P]
+        lib.oracle_mean_sq.argtypes = [P, i64]
+        lib.oracle_mean_sq.restype = ctypes.c_float
         lib.oracle_relu2.argtypes = [P, i64]
         lib.oracle_forward.argtypes = [P, ctypes.c_float, P, P, i64, i64, i64, P, P]
         lib.oracle_forward.restype = i64
@@ -187,11 +189,23 @@ def quant_act(X: np.ndarray, clamp_eps=ACT_CLAMP_EPS) -> tuple[np.ndarray, np.nd
     return xq, s
 
 
+def mean_sq(x: np.ndarray) -> np.float32:
+    """mean(x^2) of one row: the exact mean of the squares of the fp32 values,
+    rounded once to fp32 (reading R9, in the manner of R1)."""
+    x = _c(x, np.float32).reshape(-1)
+    if x.size == 0:
+        raise ValueError("mean_sq needs at least one value")
+    return np.float32(_load().oracle_mean_sq(_p(x), x.size))
+
+
 def rmsnorm_quant_act(X: np.ndarray, gain=None, eps=np.float32(1e-5), clamp_eps=ACT_CLAMP_EPS):
-    """Sub-layer RMS normalisation folded into the absmax quantisation (reading
-    R9): x_q = quant_act(X * gain), s = s(X * gain) * sqrt(mean(X^2) + eps)."""
+    """Sub-layer RMS normalisation, then the absmax quantisation (reading R9):
+    x_n = fp32(fp32(X * gain) / fp32(sqrt(fp32(mean(X^2) + eps)))), then
+    (x_q, s) = quant_act(x_n).  eps must be > 0."""
     X = _c(X, np.float32)
     M, K = X.shape
+    if not (np.isfinite(eps) and np.float32(eps) > 0):
+        raise ValueError("eps must be finite and > 0")
     g = None if gain is None else _c(gain, np.float32)
     if g is not None and g.shape != (K,):
         raise ValueError("gain must have K entries")

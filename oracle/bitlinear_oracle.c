@@ -37,8 +37,9 @@
  *   R6  dequant is t = fp32(gamma / s[m]) followed by y = fp32(fp32(acc) * t);
  *       fp32(acc) is exact because |acc| <= 127*K < 2^24.
  *   R9  the sub-layer norm ahead of a BitLinear is RMS normalisation with an
- *       optional per-channel gain; it leaves x_q = quant(x * g) and scales s
- *       by sqrt(mean(x^2) + eps) (see the function).
+ *       optional per-channel gain, applied before the quantisation:
+ *       x_n = fp32(fp32(x * g) / fp32(sqrt(fp32(mean(x^2) + eps)))), the
+ *       mean of squares exact and rounded once (see the function).
  *   R10 squared ReLU on the output is fp32(max(y,0) * max(y,0)).
  *   R11 base-3 packing: five codes per byte as sum (q+1) * 3^i, least
  *       significant first, rows of ceil(K/5) bytes padded with 121 (zero
@@ -56,10 +57,12 @@
 /* R1: gamma = mean |W|, exact.                                              */
 /* ------------------------------------------------------------------------ */
 
-/* A fixed-point accumulator that holds any sum of up to 2^32 finite fp32
- * magnitudes exactly.  One unit is 2^-149 (the smallest fp32 subnormal), so
- * every finite |w| is an integer number of units below 2^278. */
-#define ORC_LIMBS 12 /* 384 bits */
+/* A fixed-point accumulator for exact sums of non-negative values.  For the
+ * absmean one unit is 2^-149 (the smallest fp32 subnormal), so every finite
+ * |w| is an integer number of units below 2^278 and 2^32 of them stay below
+ * 2^310.  For the mean of squares (R9) one unit is 2^-298, every finite x^2
+ * is below 2^554 units and 2^24 of them below 2^578.  640 bits hold both. */
+#define ORC_LIMBS 20 /* 640 bits */
 
 typedef struct {
   uint32_t limb[ORC_LIMBS]; /* little-endian limbs */
@@ -109,12 +112,15 @@ static int orc_big_highest_bit(const orc_big* a) {
 
 static uint32_t orc_big_bit(const orc_big* a, int b) { return (a->limb[b / 32] >> (b % 32)) & 1u; }
 
-/* Round (Q + R/n) units of 2^-149 to the nearest fp32, ties to even. */
-static float orc_round_to_f32(const orc_big* Q, uint64_t R, uint64_t n) {
+/* Round (Q + R/n) units of 2^unit_exp to the nearest fp32, ties to even.
+ * The fp32 quantum is 2^(p-23) units for a top set bit p, never finer than
+ * the subnormal quantum 2^-149, which is 2^(-149-unit_exp) units. */
+static float orc_round_to_f32(const orc_big* Q, uint64_t R, uint64_t n, int unit_exp) {
+  const int qmin = -149 - unit_exp; /* subnormal quantum, as a bit index of Q */
   int p = orc_big_highest_bit(Q);
-  int ulp = (p - 23 > 0) ? p - 23 : 0; /* fp32 quantum, as a power of two in units */
+  int ulp = (p - 23 > qmin) ? p - 23 : qmin; /* fp32 quantum, as a power of two in units */
   uint64_t M = 0;                      /* kept significand: bits [ulp, p] of Q */
-  for (int b = (p > 0 ? p : 0); b >= ulp; --b) M = (M << 1) | (p >= 0 ? orc_big_bit(Q, b) : 0);
+  for (int b = p; b >= ulp; --b) M = (M << 1) | orc_big_bit(Q, b);
   /* compare the discarded part (bits below ulp, plus R/n) with half a quantum */
   int cmp; /* -1 below half, 0 exactly half, +1 above half */
   if (ulp == 0) {
@@ -137,15 +143,28 @@ static float orc_round_to_f32(const orc_big* Q, uint64_t R, uint64_t n) {
   }
   uint32_t bits;
   if (M >= (1u << 23)) {
-    uint32_t biased = (uint32_t)ulp + 1; /* value = M * 2^(ulp-149) */
+    /* value = M * 2^(ulp + unit_exp), M in [2^23, 2^24): biased exponent ulp + unit_exp + 150 */
+    int biased = ulp + unit_exp + 150;
     if (biased >= 255) bits = 0x7f800000u;
-    else bits = (biased << 23) | (uint32_t)(M - (1u << 23));
+    else bits = ((uint32_t)biased << 23) | (uint32_t)(M - (1u << 23));
   } else {
-    bits = (uint32_t)M; /* subnormal, ulp == 0 */
+    bits = (uint32_t)M; /* subnormal: ulp == qmin, value = M * 2^-149 */
   }
   float out;
   memcpy(&out, &bits, 4);
   return out;
+}
+
+/* floor(S / n) into Q and the remainder, most significant limb first. */
+static uint64_t orc_big_divide(const orc_big* S, uint64_t n, orc_big* Q) {
+  memset(Q, 0, sizeof *Q);
+  unsigned __int128 rem = 0;
+  for (int i = ORC_LIMBS - 1; i >= 0; --i) {
+    unsigned __int128 cur = (rem << 32) | S->limb[i];
+    Q->limb[i] = (uint32_t)(cur / n);
+    rem = cur % n;
+  }
+  return (uint64_t)rem;
 }
 
 /* gamma = mean(|W|) over n values, exact then rounded once (reading R1).
@@ -159,16 +178,9 @@ float oracle_absmean(const float* W, uint64_t n) {
     if (!orc_decompose(W[i], &sig, &off)) return NAN;
     if (sig) orc_big_add_shifted(&S, sig, off);
   }
-  /* long division of S by n, most significant limb first */
   orc_big Q;
-  memset(&Q, 0, sizeof Q);
-  unsigned __int128 rem = 0;
-  for (int i = ORC_LIMBS - 1; i >= 0; --i) {
-    unsigned __int128 cur = (rem << 32) | S.limb[i];
-    Q.limb[i] = (uint32_t)(cur / n);
-    rem = cur % n;
-  }
-  return orc_round_to_f32(&Q, (uint64_t)rem, n);
+  uint64_t rem = orc_big_divide(&S, n, &Q);
+  return orc_round_to_f32(&Q, rem, n, -149);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -304,30 +316,50 @@ void oracle_quant_act(const float* X, int64_t M, int64_t K, float clamp_eps, int
 /* R9: sub-layer RMS normalisation ahead of the activation quantisation.     */
 /* The transcript says BitNet b1.58 2B4T adds a normalisation inside each    */
 /* sub-layer (paragraph after the poker-chip analogy); its formula is not on */
-/* pages.  Reading: x_n = x * g / sqrt(mean(x^2) + eps) per token, g an       */
-/* optional per-channel gain.  The per-token factor 1/sqrt(...) does not     */
-/* change the absmax codes (absmax quantisation is invariant to a positive   */
-/* per-token scale), so x_q = quant_act(x * g) exactly and only the scale    */
-/* changes: s = s(x * g) * sqrt(mean(x^2) + eps).  mean(x^2) is formed in    */
-/* double, in index order, and s is rounded once to fp32.                    */
+/* the pages.  Reading, per token, in this order:                            */
+/*   ms  = mean_k x[k]^2, the exact real mean of the squares of the fp32     */
+/*         values, rounded once to fp32 (ties to even), as gamma in R1;      */
+/*   r   = fp32 sqrt(fp32(ms + eps))  (IEEE square root), eps > 0;           */
+/*   x_n = fp32(fp32(x[k] * g[k]) / r)  (one IEEE multiply, one division),   */
+/*         g an optional per-channel gain (1 when absent);                   */
+/* then x_n is quantised exactly as any activation row (R4, R5).             */
 /* ------------------------------------------------------------------------ */
+
+/* mean_k x[k]^2, exact then rounded once to fp32.  x = sig * 2^off units of
+ * 2^-149, so x^2 = sig^2 * 2^(2 off) units of 2^-298; sig^2 < 2^48 is added
+ * as two 32-bit halves.  Non-finite input gives NaN. */
+float oracle_mean_sq(const float* x, int64_t K) {
+  orc_big S;
+  memset(&S, 0, sizeof S);
+  for (int64_t k = 0; k < K; ++k) {
+    uint32_t sig;
+    int off;
+    if (!orc_decompose(x[k], &sig, &off)) return NAN;
+    const uint64_t sq = (uint64_t)sig * (uint64_t)sig;
+    if ((uint32_t)sq) orc_big_add_shifted(&S, (uint32_t)sq, 2 * off);
+    if ((uint32_t)(sq >> 32)) orc_big_add_shifted(&S, (uint32_t)(sq >> 32), 2 * off + 32);
+  }
+  orc_big Q;
+  uint64_t rem = orc_big_divide(&S, (uint64_t)K, &Q);
+  return orc_round_to_f32(&Q, rem, (uint64_t)K, -298);
+}
 
 void oracle_rmsnorm_quant_act(const float* X, int64_t M, int64_t K, const float* gain, float eps, float clamp_eps,
                               int8_t* x_q, float* s) {
-  float* xg = (float*)malloc((size_t)K * sizeof(float));
-  if (!xg) return;
+  float* xn = (float*)malloc((size_t)K * sizeof(float));
+  if (!xn) return;
   for (int64_t m = 0; m < M; ++m) {
     const float* row = X + m * K;
-    double ss = 0.0;
+    const float ms = oracle_mean_sq(row, K);
+    const float v = ms + eps;
+    const float r = sqrtf(v);
     for (int64_t k = 0; k < K; ++k) {
-      ss += (double)row[k] * (double)row[k];
-      xg[k] = gain ? row[k] * gain[k] : row[k];
+      const float t = gain ? row[k] * gain[k] : row[k];
+      xn[k] = t / r;
     }
-    float sg;
-    oracle_quant_act(xg, 1, K, clamp_eps, x_q + m * K, &sg);
-    s[m] = (float)((double)sg * sqrt(ss / (double)K + (double)eps));
+    oracle_quant_act(xn, 1, K, clamp_eps, x_q + m * K, &s[m]);
   }
-  free(xg);
+  free(xn);
 }
 
 /* R10: squared ReLU on the BitLinear output, the FFN activation that the    */

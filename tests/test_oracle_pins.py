@@ -387,23 +387,143 @@ def test_forward_end_to_end_tiny():
 
 # ---------------------------------------------------------------- sub-layer RMS norm and squared ReLU (R9, R10)
 
-def test_rmsnorm_quant_worked_example():
-    # x = [3, -4, 0, 0], eps = 0: max|x| = 4, s(x) = 127/4 = 31.75, x_q = [rint(95.25), -127, 0, 0];
-    # mean(x^2) = 25/4, sqrt = 2.5, so s = 31.75 * 2.5 = 79.375 (all exact in fp32)
-    xq, s = oracle.rmsnorm_quant_act(np.array([[3.0, -4.0, 0.0, 0.0]], np.float32), eps=np.float32(0.0))
+def sqrt_f32_rne(v: Fraction) -> np.float32:
+    """The fp32 nearest to sqrt(v), v >= 0 exact: the candidate c whose
+    neighbouring midpoints bracket sqrt(v), compared through squares (exact).
+    sqrt of a rational is never exactly half-way between two fp32 values
+    unless it is itself an fp32 value, so no tie rule is needed."""
+    if v == 0:
+        return np.float32(0.0)
+    c = np.float32(math.sqrt(float(v)))
+    for _ in range(4):
+        lo = np.nextafter(c, np.float32(0))
+        hi = np.nextafter(c, np.float32(np.inf))
+        m_lo = (Fraction(float(lo)) + Fraction(float(c))) / 2
+        m_hi = (Fraction(float(c)) + Fraction(float(hi))) / 2
+        if v < m_lo * m_lo:
+            c = lo
+        elif v > m_hi * m_hi:
+            c = hi
+        else:
+            return c
+    raise AssertionError("sqrt search did not settle")
+
+
+def rint_half_even(x: Fraction) -> int:
+    fl = x.numerator // x.denominator
+    rem = x - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    return fl
+
+
+def rmsnorm_quant_exact(x, g, eps):
+    """Reading R9 evaluated in exact rationals, each fp32 step rounded with
+    the IEEE rules written out above; tiny rows only."""
+    x = [Fraction(float(v)) for v in np.asarray(x, np.float32)]
+    g = [Fraction(1)] * len(x) if g is None else [Fraction(float(v)) for v in np.asarray(g, np.float32)]
+    ms = frac_to_f32_rne(sum((v * v for v in x), Fraction(0)) / len(x))
+    v = frac_to_f32_rne(Fraction(float(ms)) + Fraction(float(np.float32(eps))))
+    r = Fraction(float(sqrt_f32_rne(Fraction(float(v)))))
+    xn = [Fraction(float(frac_to_f32_rne(Fraction(float(frac_to_f32_rne(xi * gi))) / r))) for xi, gi in zip(x, g)]
+    a = max(abs(t) for t in xn)
+    a = max(a, Fraction(float(np.float32(1e-5))))
+    s = frac_to_f32_rne(127 / a)
+    codes = [min(127, max(-128, rint_half_even(Fraction(float(frac_to_f32_rne(t * Fraction(float(s)))))))) for t in xn]
+    return codes, s
+
+
+def exact_mean_sq(x) -> Fraction:
+    vals = [Fraction(float(v)) ** 2 for v in np.asarray(x, dtype=np.float32).reshape(-1)]
+    return sum(vals, Fraction(0)) / len(vals)
+
+
+def test_mean_sq_brute_force_fraction():
+    rng = np.random.default_rng(17)
+    for trial in range(60):
+        n = int(rng.integers(1, 40))
+        x = (rng.standard_normal(n) * 10.0 ** rng.uniform(-25, 18)).astype(np.float32)
+        if trial % 6 == 0:
+            x[rng.integers(0, n)] = np.float32(1e-45)
+        if trial % 7 == 0:
+            x[rng.integers(0, n)] = np.float32(3e18)  # square near the top of fp32
+        assert oracle.mean_sq(x) == frac_to_f32_rne(exact_mean_sq(x)), (trial, n)
+    # values spread over the whole range, where an fp32 or fp64 sum drops bits
+    x = np.array([1.8e19, 1.0, 1e-20, -2.5e-38, 1e-45, 7.0, -1e10, 5e-3] * 3, np.float32)
+    assert oracle.mean_sq(x) == frac_to_f32_rne(exact_mean_sq(x))
+
+
+def test_mean_sq_closed_forms_and_ties():
+    assert oracle.mean_sq(np.array([3.0, -4.0, 0.0, 0.0], np.float32)) == np.float32(6.25)
+    assert oracle.mean_sq(np.full(1000, -0.5, np.float32)) == np.float32(0.25)
+    # squares above the fp32 range: the mean rounds to +inf; far below it: to 0
+    assert oracle.mean_sq(np.array([2.0**70, 0.0], np.float32)) == np.float32(np.inf)
+    assert oracle.mean_sq(np.array([2.0**-80], np.float32)) == np.float32(0.0)
+    # 2^-75 squared is 2^-150, half the smallest subnormal: a tie, to even (0);
+    # with a second, larger term the mean goes above the midpoint
+    assert oracle.mean_sq(np.array([2.0**-75], np.float32)) == np.float32(0.0)
+    assert oracle.mean_sq(np.array([2.0**-74, 2.0**-74], np.float32)) == np.float32(2.0**-148)
+    # 297^2 + 5785^2 = 2 * (2^24 + 1): the mean 2^24 + 1 lies half-way between
+    # the fp32 neighbours 2^24 and 2^24 + 2, and rounds to the even one, 2^24;
+    # a third, tiny square pushes it above the midpoint (to 2^24 + 2 for
+    # K = 2 terms scaled to K = 3: checked against the exact fraction)
+    assert oracle.mean_sq(np.array([297.0, 5785.0], np.float32)) == np.float32(2.0**24)
+    x = np.array([297.0, 5785.0, 1e-30], np.float32)
+    assert oracle.mean_sq(x) == frac_to_f32_rne(exact_mean_sq(x))
+    assert oracle.mean_sq(np.array([1.0, 1.0, 0.0, 0.0], np.float32)) == np.float32(0.5)
+
+
+def test_rmsnorm_quant_worked_example_exact_sqrt():
+    # x = [3, -4, 0, 0], eps = 2.75: mean(x^2) = 25/4, v = 9, r = 3 exactly;
+    # x_n = [1, fp32(-4/3)], max|x_n| = fp32(4/3) = 11184811 * 2^-23,
+    # s = fp32(127 / that) = fp32(95.2499972...) = 95.25 (fp32 spacing 2^-17 there);
+    # codes: rint(1 * 95.25) = 95, rint(-127.0000...) = -127
+    xq, s = oracle.rmsnorm_quant_act(np.array([[3.0, -4.0, 0.0, 0.0]], np.float32), eps=np.float32(2.75))
     assert xq.tolist() == [[95, -127, 0, 0]]
-    assert s.tolist() == [79.375]
+    assert s.tolist() == [95.25]
+
+
+def test_rmsnorm_quant_near_tie_normalise_then_quantise():
+    # x = [2, 1], eps = 2^-9.  mean(x^2) = 2.5, v = 2.501953125 (exact),
+    # r = fp32(sqrt(v)) = 0x1.94edfcp+0, x_n = [0x1.43b0dap+0, 0x1.43b0dap-1]
+    # (1/r and 2/r round to the same significand), s = fp32(127 / x_n[0]) =
+    # 0x1.91c41ep+6, and x_n[1] * s = 63.4999977... rounds to 0x1.fbfffep+5 =
+    # 63.49999619, so the code is 63.  Quantising x itself and moving the RMS
+    # factor into s instead would give 1 * 63.5 = 63.5, which rounds (half to
+    # even) to 64: this case tells the two orders apart.
+    xq, s = oracle.rmsnorm_quant_act(np.array([[2.0, 1.0]], np.float32), eps=np.float32(2.0**-9))
+    assert xq.tolist() == [[127, 63]]
+    assert float(s[0]) == float.fromhex("0x1.91c41ep+6")
+    xq_fold, _ = oracle.quant_act(np.array([[2.0, 1.0]], np.float32))
+    assert xq_fold.tolist() == [[127, 64]]
+
+
+def test_rmsnorm_quant_brute_force_exact_rationals():
+    rng = np.random.default_rng(23)
+    for trial in range(80):
+        K = int(rng.integers(1, 7))
+        x = (rng.standard_normal(K) * 10.0 ** rng.uniform(-6, 6)).astype(np.float32)
+        if trial % 5 == 0:
+            x[0] = x[-1] * np.float32(0.5)  # ratios that land near half-way codes
+        g = None if trial % 3 == 0 else rng.uniform(0.1, 3.0, size=K).astype(np.float32)
+        eps = np.float32(10.0 ** rng.uniform(-8, 0))
+        codes, s_ref = rmsnorm_quant_exact(x, g, eps)
+        xq, s = oracle.rmsnorm_quant_act(x[None, :], gain=g, eps=eps)
+        assert xq[0].tolist() == codes, (trial, x, g, eps)
+        assert s[0] == s_ref, (trial, s[0], s_ref)
 
 
 def test_rmsnorm_quant_is_invariant_to_token_scale():
-    # RMS normalisation makes the BitLinear input independent of a per-token scale:
-    # x_q and s must not change when a row is multiplied by 2^k (plain absmax
-    # quantisation would divide s by 2^k)
+    # RMS normalisation makes the BitLinear input independent of a per-token
+    # scale: with eps far below mean(x^2), multiplying a row by 2^k scales the
+    # exact mean of squares by 4^k and r by 2^k exactly, so x_n, x_q and s stay
+    # the same bit for bit (plain absmax quantisation would divide s by 2^k)
     rng = np.random.default_rng(9)
     X = rng.standard_normal((5, 96)).astype(np.float32)
-    xq0, s0 = oracle.rmsnorm_quant_act(X, eps=np.float32(0.0))
+    eps = np.float32(2.0**-100)
+    xq0, s0 = oracle.rmsnorm_quant_act(X, eps=eps)
     for k in (-3, 1, 6):
-        xq1, s1 = oracle.rmsnorm_quant_act(X * np.float32(2.0 ** k), eps=np.float32(0.0))
+        xq1, s1 = oracle.rmsnorm_quant_act(X * np.float32(2.0 ** k), eps=eps)
         assert np.array_equal(xq0, xq1)
         assert np.array_equal(s0, s1)
     _, sp0 = oracle.quant_act(X)
@@ -415,7 +535,7 @@ def test_rmsnorm_quant_gain():
     rng = np.random.default_rng(10)
     X = rng.standard_normal((3, 64)).astype(np.float32)
     xq0, s0 = oracle.rmsnorm_quant_act(X)
-    # a uniform gain of 2 doubles every normalised value: same codes, half the scale
+    # a uniform gain of 2 doubles every normalised value exactly: same codes, half the scale
     xq2, s2 = oracle.rmsnorm_quant_act(X, gain=np.full(64, 2.0, np.float32))
     assert np.array_equal(xq0, xq2) and np.array_equal(s2 * np.float32(2.0), s0)
     # channels with zero gain quantise to zero; the others keep their sign
@@ -428,18 +548,20 @@ def test_rmsnorm_quant_gain():
 
 
 def test_rmsnorm_quant_constant_and_zero_rows():
-    # constant row c: mean(x^2) = c^2, s = (127/|c|) * |c| = 127 with eps = 0
-    xq, s = oracle.rmsnorm_quant_act(np.full((2, 40), -0.5, np.float32), eps=np.float32(0.0))
+    # constant row c = -0.5: mean(x^2) = 0.25, r = 0.5 (eps far below), x_n = -1,
+    # so every code is -127 and s = 127
+    xq, s = oracle.rmsnorm_quant_act(np.full((2, 40), -0.5, np.float32), eps=np.float32(2.0**-100))
     assert np.all(xq == -127) and np.all(s == 127.0)
-    # an all-zero token stays finite (the absmax clamp) and quantises to zeros
+    # an all-zero token normalises to zeros, and the absmax clamp keeps s finite
     xq, s = oracle.rmsnorm_quant_act(np.zeros((1, 16), np.float32))
-    assert np.all(xq == 0) and np.isfinite(s).all() and s[0] > 0
+    assert np.all(xq == 0) and s[0] == np.float32(127.0) / np.float32(1e-5)
+    with pytest.raises(ValueError):
+        oracle.rmsnorm_quant_act(np.ones((1, 4), np.float32), eps=np.float32(0.0))
 
 
-def test_rmsnorm_quant_matches_unfused_definition():
-    # normalise first, in fp64, then absmax-quantise: the folded form must give
-    # the same codes (random data has no exact .5 ties) and x_q / s must
-    # reconstruct x_n to within half a quantisation step
+def test_rmsnorm_quant_close_to_fp64_normalisation():
+    # normalising in fp64 and quantising must land on the same codes away from
+    # half-way points, and x_q / s must reconstruct x_n to half a step
     rng = np.random.default_rng(11)
     K = 300
     X = (rng.standard_normal((6, K)) * rng.uniform(0.01, 50.0, size=(6, 1))).astype(np.float32)
@@ -449,8 +571,10 @@ def test_rmsnorm_quant_matches_unfused_definition():
     x64 = X.astype(np.float64)
     xn = x64 * g.astype(np.float64) / np.sqrt((x64 ** 2).mean(axis=1, keepdims=True) + np.float32(eps))
     sc = 127.0 / np.abs(xn).max(axis=1, keepdims=True)
-    codes = np.clip(np.rint(xn * sc), -127, 127).astype(np.int8)
-    assert np.array_equal(xq, codes)
+    t = xn * sc
+    far = np.abs(np.abs(t - np.floor(t)) - 0.5) > 1e-3
+    codes = np.clip(np.rint(t), -127, 127).astype(np.int8)
+    assert np.array_equal(xq[far], codes[far])
     assert np.allclose(s, sc[:, 0], rtol=1e-6, atol=0)
     assert np.all(np.abs(xq / s[:, None].astype(np.float64) - xn) <= 0.5 / s[:, None] * (1 + 1e-5))
 
