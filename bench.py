@@ -1,7 +1,7 @@
 #!/usr/bin/env python3
 """Benchmark of the BitNet b1.58 BitLinear forward on B300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|...] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload llama70b|...] [--impl ours|reference]
 
 One step is one pass of the per-token hot path over every layer of the
 workload: per-token int8 activation quantisation, then the ternary x int8
@@ -9,13 +9,20 @@ product with the fused gamma/s rescale, through the C ABI of libbitlinear.so.
 Weights are packed once beforehand (the pages' "inference-ready pack"); the
 packing kernels are timed in the same run and reported under "pack".
 
-Timing: W warm-up steps, then exactly K steps replayed from CUDA graphs of the
-public C-ABI calls, bracketed by a barrier and cuda.synchronize() on both
-sides and timed with CUDA events; max over ranks.  L2 (126 MB) is defeated by
-rotating over R copies of the packed weights and activations whose total is
-more than twice L2.  After the timed region the last step is re-run eagerly
-and its outputs must match bit for bit ("verified").  Rank 0 prints one JSON
-line.
+The default workload is the 70B-class layer pair at M = 1, 16 and 176 tokens
+(the largest configuration that fits one GPU), so one line covers both halves
+of the metric: the few-token layers are judged in GB/s against HBM, the
+176-token layers in TOPS against the tensor pipe ("roofline.per_layer").
+
+Timing: W warm-up steps, then the K steps, captured as one CUDA graph of the
+public C-ABI calls, are replayed R times; each replay is bracketed by a
+barrier and cuda.synchronize() on both sides and timed with CUDA events on the
+launching stream, and ms_per_step is the median replay time / K (max over
+ranks).  L2 (126 MB) is defeated by rotating every layer over copies of its
+packed weights and activations whose total is more than twice L2.  After the
+timed region the last step is re-run eagerly and its outputs must match bit
+for bit ("verified").  The same K steps launched one call at a time (no
+graph) give the "per_launch" figure.  Rank 0 prints one JSON line.
 
 Under torchrun (N > 1) every rank runs its own replica of the workload (weak
 scaling; the path has no data-path exchange) and value is the sum over ranks.
@@ -41,8 +48,11 @@ import torch  # noqa: E402
 import workloads  # noqa: E402
 
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
-DEFAULT_STEPS = {"decode": 100000, "tiny": 20000, "skinny": 20000, "prefill": 400, "llama70b": 2000}
+DEFAULT_WORKLOAD = "llama70b"
+DEFAULT_STEPS = {"decode": 2000, "tiny": 2000, "skinny": 500, "prefill": 100, "llama70b": 50}
 GRAPH_CHUNK = 500  # steps per captured graph
+MIN_TIMED_S = 1.0  # replays of the K-step graph are repeated until about this long
+MAX_REPLAYS = 200
 
 
 # ---------------------------------------------------------------- helpers
@@ -69,7 +79,7 @@ def kernel_source_digest(files):
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str, workload: str):
+def ncu_traffic(kernel: str, shape: str):
     """DRAM bytes per launch from the committed ncu summary, or None if absent
     or if the kernel's source changed since the counters were taken."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
@@ -78,7 +88,7 @@ def ncu_traffic(kernel: str, workload: str):
     with open(p) as f:
         table = json.load(f)
     for e in table.get("entries", []):
-        if e.get("kernel") == kernel and e.get("workload") == workload:
+        if e.get("kernel") == kernel and e.get("shape") == shape:
             if e.get("source_digest") != kernel_source_digest(e.get("source_files", [])):
                 return None
             return e.get("dram_bytes_per_launch")
@@ -205,20 +215,72 @@ def layer_ops(L) -> int:
 def metric_for(wl) -> tuple[str, str]:
     if max(L.M for L in wl.layers) <= 4:
         return "BitLinear GEMV GB/s (HBM roofline)", "GB/s"
+    if min(L.M for L in wl.layers) <= 4:
+        return ("BitLinear GEMV GB/s & GEMM int8 TOPS: step TOPS (2MNK over all layers); per-layer GB/s or TOPS "
+                "against the roofline each layer's intensity implies"), "TOPS"
     return "BitLinear GEMM int8 TOPS (tensor roofline)", "TOPS"
+
+
+def layer_bound(ops: float, nbytes: float, peaks) -> str:
+    """'hbm' where the layer's intensity (ops per algorithmic byte) lies below
+    the ridge of the measured peaks, else 'tensor'."""
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    return "hbm" if ops / nbytes < ridge else "tensor"
+
+
+def layer_roofline(L, us: float, fused: bool, fmt: str, peaks, peak_src: str) -> dict:
+    """One layer's forward kernel against the bound its intensity implies."""
+    nbytes = forward_kernel_bytes(L, fused and gemv_fused_layer(L), fmt)
+    ops = layer_ops(L)
+    bound = layer_bound(ops, nbytes, peaks)
+    if bound == "hbm":
+        achieved, peak, unit = nbytes / (us * 1e-6) / 1e9, peaks["hbm_gbs"], "GB/s"
+        src = f"{peak_src} hbm_gbs (copy)"
+    else:
+        achieved, peak, unit = ops / (us * 1e-6) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+        src = f"{peak_src} bf16_tflops burst (kind::f16 runs at the bf16 rate)"
+    return {"layer": f"M={L.M} K={L.K} N={L.N}", "bound": bound, "achieved": round(achieved, 1),
+            "peak": peak, "unit": unit, "frac": round(achieved / peak, 4), "us": round(us, 3),
+            "algorithmic_bytes": nbytes, "algorithmic_ops": ops, "intensity_op_per_byte": round(ops / nbytes, 2),
+            "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1), "TOPS": round(ops / (us * 1e-6) / 1e12, 2),
+            "peak_source": src}
+
+
+def common_config(args, wl) -> dict:
+    """The workload description shared by both arms' JSON lines."""
+    return {"workload": args.workload,
+            "layers": [f"M={L.M} K={L.K} N={L.N} X={L.x_dtype}" for L in wl.layers],
+            "weights": ("base-3, five per byte (1.6 bits per weight)" if args.format == "tq5"
+                        else "2-bit, four per byte"),
+            "path": ("bitlinear_quant_act + bitlinear_forward_tq5" if args.format == "tq5" else
+                     ("bitlinear_quant_forward_ws (one fused quantise+GEMV kernel for M <= 4; quantisation "
+                      "writing the fp16 operand, then the tcgen05 GEMM otherwise)") if args.path == "fused"
+                     else "bitlinear_quant_act + bitlinear_forward_ws"),
+            "l2": "every layer rotates over copies of its packed weights and activations totalling more than "
+                  "2x L2 (126 MiB); no L2 flush",
+            "launch": "K steps captured as one CUDA graph of the C-ABI calls, replayed R times (median)",
+            "parallelism": f"replicas x{args.gpus}"}
 
 
 # ---------------------------------------------------------------- CPU oracle (baseline and reference arm)
 
-def run_oracle(wl, budget_s: float, steps: int | None = None, warmup: int = 0, fmt: str = "2bit"):
+_ORACLE_PACKED: dict = {}  # oracle-packed weights by (workload, weight seed, format)
+
+
+def run_oracle(wl, budget_s: float, steps: int | None = None, warmup: int = 0, fmt: str = "2bit",
+               omp: bool = False):
     """Time the oracle on a bounded sample of the per-token step: a fraction f
-    of each layer's output rows (all tokens).  Returns (value, f, s/step, steps)."""
+    of each layer's output rows (all tokens).  Returns (value, f, s/step,
+    steps, threads)."""
     import oracle
 
     layers = []
     for i, L in enumerate(wl.layers):
-        W = workloads.layer_weights(wl, i).numpy()
-        p, g = oracle.pack_weights_tq5(W) if fmt == "tq5" else oracle.pack_weights(W)
+        key = (wl.name, workloads.weight_seed(wl, i), fmt)
+        if key not in _ORACLE_PACKED:
+            W = workloads.layer_weights(wl, i).numpy()
+            _ORACLE_PACKED[key] = oracle.pack_weights_tq5(W) if fmt == "tq5" else oracle.pack_weights(W)
+        p, g = _ORACLE_PACKED[key]
         layers.append((L, p, g, workloads.x_as_f32_numpy(workloads.layer_activations(wl, i))))
     _, unit = metric_for(wl)
 
@@ -226,11 +288,11 @@ def run_oracle(wl, budget_s: float, steps: int | None = None, warmup: int = 0, f
         work = 0.0
         for (L, p, g, X) in layers:
             rows = max(1, int(round(L.N * frac)))
-            xq, s = oracle.quant_act(X)
+            xq, s = oracle.quant_act(X, omp=omp)
             if fmt == "tq5":
                 oracle.forward_tq5(p[:rows], g, xq, s, L.K)
             else:
-                oracle.forward(p[:rows], g, xq, s, L.K)
+                oracle.forward(p[:rows], g, xq, s, L.K, omp=omp)
             wrow = tq5_row_bytes(L.K) if fmt == "tq5" else L.K / 4
             work += (L.M * L.K * x_bytes(L) + rows * wrow + 4 * L.M * rows) if unit == "GB/s" \
                 else 2.0 * L.M * rows * L.K
@@ -244,7 +306,11 @@ def run_oracle(wl, budget_s: float, steps: int | None = None, warmup: int = 0, f
         n_total = steps
         frac = max(1.0 / max(L.N for L in wl.layers), min(1.0, budget_s / (steps * t_small / 0.02)))
     else:
-        n_total = max(1, int(budget_s / max(t_small, 1e-4)))
+        frac = min(1.0, max(0.02, 0.02 * budget_s / (20 * max(t_small, 1e-4))))
+        t0 = time.perf_counter()
+        one(frac)
+        t_one = time.perf_counter() - t0
+        n_total = max(1, int(budget_s / max(t_one, 1e-4)))
     for _ in range(warmup):
         one(frac)
     t0 = time.perf_counter()
@@ -252,7 +318,27 @@ def run_oracle(wl, budget_s: float, steps: int | None = None, warmup: int = 0, f
     for _ in range(n_total):
         work += one(frac)
     dt = time.perf_counter() - t0
-    return work / dt / (1e9 if unit == "GB/s" else 1e12), frac, dt / n_total, n_total
+    return (work / dt / (1e9 if unit == "GB/s" else 1e12), frac, dt / n_total, n_total,
+            oracle.num_threads(omp) if omp else 1)
+
+
+def cpu_baseline(wl, fmt: str, budget_s: float) -> dict:
+    """The oracle on the host: single-threaded, and its OpenMP build on every
+    host thread (the same code; identical results)."""
+    _, unit = metric_for(wl)
+    v1, f1, s1, n1, _ = run_oracle(wl, budget_s=budget_s / 2, fmt=fmt)
+    out = {"unit": unit, "kind": "oracle", "nproc": os.cpu_count()}
+    single = {"value": round(v1, 4), "cores": 1,
+              "sample": f"{n1} oracle steps on {f1:.2%} of each layer's output rows (all tokens), {n1 * s1:.1f} s"}
+    if fmt == "tq5":  # the base-3 decode has no threaded loops
+        out.update(single)
+        return out
+    vN, fN, sN, nN, thr = run_oracle(wl, budget_s=budget_s / 2, fmt=fmt, omp=True)
+    out.update({"value": round(vN, 4), "cores": thr,
+                "sample": f"{nN} oracle steps on {fN:.2%} of each layer's output rows (all tokens), "
+                          f"OpenMP build on {thr} threads, {nN * sN:.1f} s",
+                "single_thread": single})
+    return out
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -276,6 +362,53 @@ def gemv_fused_layer(L) -> bool:
     return L.M <= 4 and L.K <= 32768
 
 
+def graph_kernel_nodes(g) -> int | None:
+    """Kernel nodes of a captured CUDA graph (the launches one replay makes),
+    or None where the graph cannot be inspected."""
+    try:
+        import cuda.bindings.runtime as rt
+
+        graph = rt.cudaGraph_t(init_value=g.raw_cuda_graph())
+        err, _, n = rt.cudaGraphGetNodes(graph, numNodes=0)
+        if err != rt.cudaError_t.cudaSuccess:
+            return None
+        err, nodes, n = rt.cudaGraphGetNodes(graph, numNodes=n)
+        if err != rt.cudaError_t.cudaSuccess:
+            return None
+        count = 0
+        for node in nodes[:n]:
+            err, typ = rt.cudaGraphNodeGetType(node)
+            if err != rt.cudaError_t.cudaSuccess:
+                return None
+            count += int(typ == rt.cudaGraphNodeType.cudaGraphNodeTypeKernel)
+        return count
+    except Exception:  # noqa: BLE001 -- an inspection aid only
+        return None
+
+
+def timed_replays(graphs, K, stream, dist, sampler=None):
+    """Replays the K-step graph(s) R times, each replay bracketed by a barrier
+    and synchronize; returns (median ms per step over ranks, R, per-replay ms)."""
+    def once():
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(dist)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for g in graphs:
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+        return a.elapsed_time(b)
+
+    first = once()
+    R = int(min(MAX_REPLAYS, max(5, math.ceil(MIN_TIMED_S * 1e3 / max(first, 1e-3)))))
+    R = int(max_over_ranks(dist, R))  # every rank replays the same number of times
+    times = [once() for _ in range(R)]
+    med = statistics.median(times)
+    return max_over_ranks(dist, med) / K, R, times
+
+
 def run_gpu(args, dist, rank, world, local):
     import ternary_weight_06_b300 as bl
 
@@ -289,23 +422,29 @@ def run_gpu(args, dist, rank, world, local):
     tq5 = args.format == "tq5"
     fused = args.path == "fused" and not tq5  # the base-3 forward takes quantised activations
     nlayers = len(wl.layers)
+    peaks, peak_src = load_peaks()
 
-    # ---- resident inputs: pack each layer's weights once (timed as the "pack" figure)
+    # ---- resident inputs: pack each distinct weight matrix once (timed as the "pack" figure)
     packed, gammas, Xs, Xs_host, ys, xqs, ss = [], [], [], [], [], [], []
     pack_ms, pack_bytes = 0.0, 0
+    by_seed = {}
     for i, L in enumerate(wl.layers):
-        W = workloads.layer_weights(wl, i).to(dev)
-        pack_fn = bl.bitlinear_pack_weights_tq5 if tq5 else bl.bitlinear_pack_weights
-        pack_fn(W)  # warm
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        e0.record(stream)
-        Wp, g = pack_fn(W)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        pack_ms += e0.elapsed_time(e1)
-        pack_bytes += 2 * 4 * L.N * L.K + weight_bytes(L, args.format)
-        del W
+        seed = workloads.weight_seed(wl, i)
+        if seed not in by_seed:
+            W = workloads.layer_weights(wl, i).to(dev)
+            pack_fn = bl.bitlinear_pack_weights_tq5 if tq5 else bl.bitlinear_pack_weights
+            pack_fn(W)  # warm
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            Wp, g = pack_fn(W)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            pack_ms += e0.elapsed_time(e1)
+            pack_bytes += 2 * 4 * L.N * L.K + weight_bytes(L, args.format)
+            del W
+            by_seed[seed] = (Wp, g)
+        Wp, g = by_seed[seed]
         packed.append(Wp)
         gammas.append(g)
         X = workloads.layer_activations(wl, i)
@@ -324,12 +463,18 @@ def run_gpu(args, dist, rank, world, local):
     for l, L in enumerate(wl.layers):
         ys[l] = y_all[y_offs[l]:y_offs[l] + 4 * L.M * L.N].view(torch.float32).view(L.M, L.N)
     # every layer rotates over enough copies of its packed weights and
-    # activations that one pass over them is more than twice L2
-    Rs = []
-    for p, x in zip(packed, Xs):
+    # activations that one pass over them is more than twice L2; layers that
+    # share a weight matrix share its copies
+    Rs, Wrot, rot_by_seed = [], [], {}
+    for i, (p, x) in enumerate(zip(packed, Xs)):
         nbytes = p.numel() + x.numel() * x.element_size()
-        Rs.append(min(512, max(2, math.ceil(2 * l2 / nbytes) + 1)))
-    Wrot = [[p] + [p.clone() for _ in range(R - 1)] for p, R in zip(packed, Rs)]
+        R = min(512, max(2, math.ceil(2 * l2 / nbytes) + 1))
+        Rs.append(R)
+        seed = workloads.weight_seed(wl, i)
+        have = rot_by_seed.setdefault(seed, [p])
+        while len(have) < R:
+            have.append(p.clone())
+        Wrot.append(have)
     Xrot = [[x] + [x.clone() for _ in range(R - 1)] for x, R in zip(Xs, Rs)]
     # quantised activations of every copy, made on first use, for timing the
     # forward kernel alone on layers whose step runs quantise + forward
@@ -356,8 +501,8 @@ def run_gpu(args, dist, rank, world, local):
             layer_call(l, i % Rs[l], None if X_override is None else X_override[l])
 
     def kernel_call(l, r):
-        """The layer's dominant kernel alone: the fused quantise+GEMV where the
-        layer runs as one kernel, else the forward product (GEMV or GEMM) on
+        """The layer's forward alone: the fused quantise+GEMV where the layer
+        runs as one kernel, else the forward product (GEMV or GEMM) on
         activations quantised beforehand."""
         L = wl.layers[l]
         if fused and gemv_fused_layer(L):
@@ -380,49 +525,37 @@ def run_gpu(args, dist, rank, world, local):
         step(i)
     torch.cuda.synchronize()
     bl.bitlinear_check_device_error(stream)
-    # kernels per layer: fused GEMV 1; quantise + GEMV 2; quantise + fp16 expansion + GEMM 3
-    if tq5:  # quantise + base-3 forward, one pass per 4 tokens
-        launches = K * sum(1 + -(-L.M // 4) for L in wl.layers)
-    else:
-        launches = K * sum((1 if fused else 2) if gemv_fused_layer(L) else 3 for L in wl.layers)
-    peaks, peak_src = load_peaks()
 
     if args.eager:
-        return run_gpu_eager(args, bl, wl, step, K, stream, dist, world, unit, metric, Rs, launches)
+        return run_gpu_eager(args, wl, step, K, stream, dist, world, unit, metric)
 
-    # ---- capture: chunks of GRAPH_CHUNK steps
-    chunk = min(GRAPH_CHUNK, K)
-    nfull, rem = divmod(K, chunk)
-
-    def capture(fn, n):
-        g = torch.cuda.CUDAGraph()
+    # ---- capture: the K steps as graphs of at most GRAPH_CHUNK steps
+    def capture(fn, n, keep=False):
+        g = torch.cuda.CUDAGraph(keep_graph=keep)
         with torch.cuda.graph(g, stream=stream):
             for j in range(n):
                 fn(j)
         return g
 
-    g_full = capture(step, chunk)
+    chunk = min(GRAPH_CHUNK, K)
+    nfull, rem = divmod(K, chunk)
+    g_full = capture(step, chunk, keep=True)
     g_rem = capture(step, rem) if rem else None
-    for _ in range(2):
-        g_full.replay()
+    g_full.replay()
     torch.cuda.synchronize()
+    nodes = graph_kernel_nodes(g_full)
+    if tq5:  # quantise + base-3 forward, one pass per 4 tokens
+        rule = sum(1 + -(-L.M // 4) for L in wl.layers)
+    else:  # fused GEMV 1; quantise + GEMV 2; quantise (writing the fp16 operand) + GEMM 2
+        rule = sum((1 if fused else 2) if gemv_fused_layer(L) else (2 if fused else 3) for L in wl.layers)
+    launches_per_step = nodes / chunk if nodes is not None else rule
+    graphs = [g_full] * nfull + ([g_rem] if g_rem is not None else [])
 
     # ---- timed region
-    t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
     with sampler:
-        barrier(dist)
-        torch.cuda.synchronize()
-        t0e.record(stream)
-        for _ in range(nfull):
-            g_full.replay()
-        if g_rem is not None:
-            g_rem.replay()
-        t1e.record(stream)
-        torch.cuda.synchronize()
-        barrier(dist)
+        ms_per_step, R, rep_ms = timed_replays(graphs, K, stream, dist)
     clocks = sampler.summary()
-    ms_per_step = max_over_ranks(dist, t0e.elapsed_time(t1e)) / K
     bl.bitlinear_check_device_error(stream)
 
     # ---- the graph-replayed outputs must equal an eager re-run of the last step
@@ -433,66 +566,31 @@ def run_gpu(args, dist, rank, world, local):
 
     step_bytes = sum(layer_bytes(L, args.format) for L in wl.layers)
     step_ops = sum(layer_ops(L) for L in wl.layers)
-    value = world * (step_bytes / (ms_per_step * 1e-3) / 1e9 if unit == "GB/s"
-                     else step_ops / (ms_per_step * 1e-3) / 1e12)
 
-    # ---- dominant kernel: each layer's forward kernel timed alone, back to back
-    # from a CUDA graph on the launching stream (CUDA events around the replay)
-    kchunk = 200
-    kern_us = []
-    for l in range(nlayers):
-        prepare_kernel_inputs(l)
-        g = capture(lambda j, l=l: kernel_call(l, j % Rs[l]), kchunk)
-        g.replay()
-        torch.cuda.synchronize()
+    def rate(ms):
+        return world * (step_bytes / (ms * 1e-3) / 1e9 if unit == "GB/s" else step_ops / (ms * 1e-3) / 1e12)
+
+    value = rate(ms_per_step)
+
+    # ---- the same K steps launched call by call (no graph)
+    per_launch_ms = []
+    for _ in range(3):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(dist)
+        torch.cuda.synchronize()
         a.record(stream)
-        for _ in range(3):
-            g.replay()
+        for i in range(K):
+            step(i)
         b.record(stream)
         torch.cuda.synchronize()
-        kern_us.append(a.elapsed_time(b) * 1e3 / (3 * kchunk))
-        del g
-    if tq5:
-        kernel_names = ["gemv_tq5_kernel" for L in wl.layers]
-        kernel_variant = ["gemv_tq5_kernel" for L in wl.layers]
-    else:
-        kernel_names = ["gemv_kernel" if (L.M <= 4 and L.K <= 32768) else "gemm_tc_x16_kernel" for L in wl.layers]
-        kernel_variant = [gemm_variant(L, props.multi_processor_count) for L in wl.layers]
-    kname = max(set(kernel_names), key=lambda k: sum(t for t, n in zip(kern_us, kernel_names) if n == k))
-    sel = [i for i, n in enumerate(kernel_names) if n == kname]
-    tot_s = sum(kern_us[i] for i in sel) * 1e-6
-    if kname in ("gemv_kernel", "gemv_tq5_kernel"):
-        kbytes = sum(forward_kernel_bytes(wl.layers[i], fused, args.format) for i in sel)
-        roof = {"bound": "hbm", "achieved": round(kbytes / tot_s / 1e9, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "peak_source": f"{peak_src} hbm_gbs (copy)",
-                "algorithmic_bytes_per_launch": [forward_kernel_bytes(wl.layers[i], fused, args.format)
-                                                 for i in sel]}
-    else:
-        kops = sum(layer_ops(wl.layers[i]) for i in sel)
-        roof = {"bound": "tensor", "achieved": round(kops / tot_s / 1e12, 1), "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "peak_source": f"{peak_src} bf16_tflops burst (kind::f16 runs at the bf16 rate)",
-                "algorithmic_ops_per_launch": [layer_ops(wl.layers[i]) for i in sel]}
-        roof["vs_legacy_mma_sync"] = {
-            "s8": round(roof["achieved"] / LEGACY_MMA_SYNC["s8_tops"], 2),
-            "f16": round(roof["achieved"] / LEGACY_MMA_SYNC["f16_tflops"], 2),
-            "rates": LEGACY_MMA_SYNC}
-    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    roof["traffic"] = ncu_traffic(kname, args.workload) if not args.layers else None
-    roof["kernel"] = kname
-    roof["kernel_us"] = [round(kern_us[i], 3) for i in sel]
-    roof["variants"] = [kernel_variant[i] for i in sel]
-    roof["how"] = (f"each layer's kernel replayed {3 * kchunk} times back to back from a CUDA graph over its rotating "
-                   "buffers; CUDA events on the launching stream")
-    if kname == "gemm_tc_x16_kernel":
-        roof["note"] = ("time of the bitlinear_forward_ws call: the fp16 expansion of x_q (x16_prepass_kernel) "
-                        "plus the GEMM")
-    if fused and kname == "gemv_kernel":
-        roof["note"] = "the timed kernel also quantises the activations (fused)"
+        barrier(dist)
+        per_launch_ms.append(a.elapsed_time(b) / K)
+    pl_ms = max_over_ranks(dist, statistics.median(per_launch_ms))
 
-    # ---- the FFN pieces around each layer, timed the same way (outside the step):
-    # the sub-layer RMS norm folded into the quantisation of the layer's X, and
-    # the fused forward with and without the squared-ReLU epilogue
+    # ---- each layer's forward alone, back to back from a CUDA graph on the
+    # launching stream (CUDA events around the replays)
+    kchunk = 200
+
     def graph_us(fn):
         g = capture(fn, kchunk)
         g.replay()
@@ -506,6 +604,36 @@ def run_gpu(args, dist, rank, world, local):
         del g
         return a.elapsed_time(b) * 1e3 / (3 * kchunk)
 
+    kern_us = []
+    for l in range(nlayers):
+        prepare_kernel_inputs(l)
+        kern_us.append(graph_us(lambda j, l=l: kernel_call(l, j % Rs[l])))
+    per_layer = []
+    for l, L in enumerate(wl.layers):
+        e = layer_roofline(L, kern_us[l], fused, args.format, peaks, peak_src)
+        e["kernel"] = "gemv_tq5_kernel" if tq5 else gemm_variant(L, props.multi_processor_count)
+        if fused and gemv_fused_layer(L) and not tq5:
+            e["note"] = "the timed kernel also quantises the activations (fused)"
+        elif not gemv_fused_layer(L) and not tq5:
+            e["note"] = "bitlinear_forward_ws on quantised activations: the fp16 expansion of x_q plus the GEMM"
+        per_layer.append(e)
+    dom = max(range(nlayers), key=lambda l: kern_us[l])
+    roof = {k: per_layer[dom][k] for k in ("bound", "achieved", "peak", "unit", "frac")}
+    roof["traffic"] = (ncu_traffic(per_layer[dom]["kernel"].split(" ")[0], per_layer[dom]["layer"])
+                       if not args.layers else None)
+    roof["layer"] = per_layer[dom]["layer"]
+    roof["kernel"] = per_layer[dom]["kernel"]
+    roof["peak_source"] = per_layer[dom]["peak_source"]
+    roof["dominant"] = "the layer with the largest forward time in the step"
+    roof["per_layer"] = per_layer
+    roof["how"] = (f"each layer's forward replayed {3 * kchunk} times back to back from a CUDA graph over its "
+                   "rotating buffers; CUDA events on the launching stream; bound from the layer's intensity "
+                   "(2MNK per algorithmic byte) against the ridge of the measured peaks")
+    if roof["bound"] == "tensor":
+        roof["vs_legacy_mma_sync"] = {"s8": round(roof["achieved"] / LEGACY_MMA_SYNC["s8_tops"], 2),
+                                      "f16": round(roof["achieved"] / LEGACY_MMA_SYNC["f16_tflops"], 2),
+                                      "rates": LEGACY_MMA_SYNC}
+
     # the per-token quantisation (a3) alone, per layer: X read, x_q and s written
     quant = []
     for l, L in enumerate(wl.layers):
@@ -515,6 +643,9 @@ def run_gpu(args, dist, rank, world, local):
                       "frac": round(nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4), "algorithmic_bytes": nbytes})
     bl.bitlinear_check_device_error(stream)
 
+    # ---- the FFN pieces around each layer, timed the same way (outside the step):
+    # the sub-layer RMS norm then the quantisation of the layer's X, and the
+    # fused forward with and without the squared-ReLU epilogue
     ffn = {"rmsnorm_quant": [], "forward_us": [], "forward_relu2_us": []}
     for l, L in enumerate(wl.layers):
         gain = torch.rand((L.K,), generator=torch.Generator().manual_seed(l), dtype=torch.float32).add_(0.5).to(dev)
@@ -542,25 +673,26 @@ def run_gpu(args, dist, rank, world, local):
 
     e2e = run_e2e(bl, wl, step, Xs_host, y_all, K, Wm, stream, dist, world, unit, step_bytes, step_ops)
 
+    config = common_config(args, wl)
     return {
         "metric": metric, "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": K, "warmup": Wm,
         "ms_per_step": round(ms_per_step, 6), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int8", "data": "synthetic",
-        "config": {"workload": args.workload,
-                   "layers": [f"M={L.M} K={L.K} N={L.N} X={L.x_dtype}" for L in wl.layers],
-                   "l2": "inputs rotate per layer over " + ", ".join(
-                       f"{R} copies ({R * (p.numel() + x.numel() * x.element_size()) / 2**20:.0f} MiB)"
-                       for R, p, x in zip(Rs, packed, Xs)) + f" > 2x L2 ({l2 / 2**20:.0f} MiB)",
-                   "launch": f"CUDA graphs of the C-ABI calls, {chunk} steps per graph",
-                   "path": ("bitlinear_quant_act + bitlinear_forward_tq5" if tq5 else
-                            ("bitlinear_quant_forward_ws (one fused quantise+GEMV kernel for M <= 4; quantise, fp16 "
-                             "expansion of x_q and tcgen05 GEMM otherwise)") if fused
-                            else "bitlinear_quant_act + bitlinear_forward_ws"),
-                   "weights": ("base-3, five per byte (1.6 bits per weight)" if tq5 else "2-bit, four per byte"),
-                   "parallelism": f"replicas x{world}"},
+        "config": config,
+        "timing": {"replays": R, "graph_steps": K, "replay_ms": [round(t, 4) for t in rep_ms],
+                   "rotation": {"copies_per_layer": Rs,
+                                "MiB_per_layer": [round(R * (p.numel() + x.numel() * x.element_size()) / 2**20)
+                                                  for R, p, x in zip(Rs, packed, Xs)],
+                                "l2_MiB": round(l2 / 2**20)},
+                   "kernel_sum_us": round(sum(kern_us), 3),
+                   "how": "median over R replays of the K-step graph, each bracketed by barrier + synchronize"},
+        "per_launch": {"value": round(rate(pl_ms), 2), "unit": unit, "ms_per_step": round(pl_ms, 6),
+                       "how": "the K steps launched call by call without a graph, median of 3 runs"},
         "roofline": roof,
         "e2e": e2e,
-        "gpu_launches": launches,
+        "gpu_launches": int(round(launches_per_step * K)),
+        "gpu_launches_how": ("kernel nodes counted in the captured step graph" if nodes is not None
+                             else "counted by the library's routing rule"),
         "verified": verified,
         "clocks": clocks,
         "quant": {"per_layer": quant,
@@ -568,12 +700,13 @@ def run_gpu(args, dist, rank, world, local):
                           "X read + x_q written + s, frac of the measured copy bandwidth"},
         "ffn": ffn,
         "pack": {"ms": round(pack_ms, 4), "GB/s": round(pack_bytes / (pack_ms * 1e-3) / 1e9, 1),
-                 "note": "gamma + ternarise + pack of every layer (one call each), outside the step"},
+                 "matrices": len(by_seed),
+                 "note": "gamma + ternarise + pack of every distinct weight matrix (one call each), outside the step"},
     }
 
 
-def run_gpu_eager(args, bl, wl, step, K, stream, dist, world, unit, metric, Rs, launches):
-    """Timed region with eager launches (for profilers; includes launch gaps)."""
+def run_gpu_eager(args, wl, step, K, stream, dist, world, unit, metric):
+    """Timed region with eager launches only (for profilers; includes launch gaps)."""
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist)
     torch.cuda.synchronize()
@@ -587,12 +720,11 @@ def run_gpu_eager(args, bl, wl, step, K, stream, dist, world, unit, metric, Rs, 
     step_bytes = sum(layer_bytes(L, args.format) for L in wl.layers)
     step_ops = sum(layer_ops(L) for L in wl.layers)
     value = world * (step_bytes / (ms * 1e-3) / 1e9 if unit == "GB/s" else step_ops / (ms * 1e-3) / 1e12)
+    cfg = common_config(args, wl)
+    cfg["launch"] = "eager (profiling mode)"
     return {"metric": metric, "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "int8", "data": "synthetic",
-            "config": {"workload": args.workload, "launch": "eager (profiling mode)", "path": args.path,
-                       "l2": f"inputs rotate per layer over {Rs} copies"},
-            "gpu_launches": launches}
+            "vs_baseline": None, "dtype": "int8", "data": "synthetic", "config": cfg}
 
 
 def run_e2e(bl, wl, step, Xs_host, y_all, K, Wm, stream, dist, world, unit, step_bytes, step_ops):
@@ -603,6 +735,7 @@ def run_e2e(bl, wl, step, Xs_host, y_all, K, Wm, stream, dist, world, unit, step
     dev = y_all.device
     in_bytes = [x.numel() * x.element_size() for x in Xs_host]
     out_bytes = [4 * L.M * L.N for L in wl.layers]
+
     # 256-byte aligned slices of one staging buffer per direction
     def offsets(sizes):
         offs, o = [], 0
@@ -642,22 +775,12 @@ def run_e2e(bl, wl, step, Xs_host, y_all, K, Wm, stream, dist, world, unit, step
     g2 = capture(rem) if rem else None
     g1.replay()
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(dist)
-    torch.cuda.synchronize()
-    a.record(stream)
-    for _ in range(nfull):
-        g1.replay()
-    if g2 is not None:
-        g2.replay()
-    b.record(stream)
-    torch.cuda.synchronize()
-    barrier(dist)
-    ms = max_over_ranks(dist, a.elapsed_time(b)) / K
+    ms, R, _ = timed_replays([g1] * nfull + ([g2] if g2 is not None else []), K, stream, dist)
     val = world * (step_bytes / (ms * 1e-3) / 1e9 if unit == "GB/s" else step_ops / (ms * 1e-3) / 1e12)
     return {"value": round(val, 2), "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": round(ms, 6),
-            "how": "CUDA graphs of one pinned H2D copy of every layer's X + C-ABI calls + one D2H copy of every y"}
+            "ms_per_step": round(ms, 6), "replays": R,
+            "how": "CUDA graphs of one pinned H2D copy of every layer's X + C-ABI calls + one D2H copy of every y; "
+                   "median over R replays"}
 
 
 # ---------------------------------------------------------------- main
@@ -667,7 +790,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="decode", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", default="fused", choices=["fused", "separate"],
                     help="fused: bitlinear_quant_forward; separate: bitlinear_quant_act + bitlinear_forward")
@@ -676,7 +799,7 @@ def main():
     ap.add_argument("--eager", action="store_true",
                     help="launch every step eagerly instead of from CUDA graphs (for profilers)")
     ap.add_argument("--layers", default="", help="comma-separated layer indices of the workload (default: all)")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the oracle CPU baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -695,19 +818,19 @@ def main():
     metric, unit = metric_for(wl)
 
     if args.impl == "reference":
-        # the reference arm is the CPU oracle on the host cores; rank 0 only
+        # the reference arm is the CPU oracle (OpenMP build) on the host cores; rank 0 only
         if rank == 0:
-            value, frac, sec_step, n = run_oracle(wl, budget_s=120.0, steps=args.steps, warmup=args.warmup,
-                                                  fmt=args.format)
+            value, frac, sec_step, n, thr = run_oracle(wl, budget_s=120.0, steps=args.steps, warmup=args.warmup,
+                                                       fmt=args.format, omp=args.format != "tq5")
             line = {"impl": "reference", "metric": metric, "value": round(value, 4), "unit": unit,
                     "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                     "ms_per_step": round(sec_step * 1e3, 4), "higher_is_better": True, "scaling": "weak",
                     "vs_baseline": None, "dtype": "int8 x ternary -> int64 sums (fp32 rescale)",
-                    "data": "synthetic",
-                    "config": {"workload": args.workload,
-                               "layers": [f"M={L.M} K={L.K} N={L.N} X={L.x_dtype}" for L in wl.layers]},
-                    "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": 1, "kind": "oracle",
-                                     "sample": f"{frac:.4%} of each layer's output rows, all tokens, per step"},
+                    "data": "synthetic", "config": common_config(args, wl),
+                    "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": thr, "kind": "oracle",
+                                     "nproc": os.cpu_count(),
+                                     "sample": f"{frac:.4%} of each layer's output rows, all tokens, per step; "
+                                               f"{'OpenMP build, ' if thr > 1 else ''}{thr} host threads"},
                     "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0,
                             "d2h_bytes_per_step": 0}}
             print(json.dumps(line), flush=True)
@@ -718,11 +841,8 @@ def main():
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA device (the BitLinear kernels have no CPU path)")
     line = run_gpu(args, dist, rank, world, local)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        value, frac, sec_step, n = run_oracle(wl, budget_s=args.cpu_seconds, fmt=args.format)
-        line["cpu_baseline"] = {"value": round(value, 4), "unit": unit, "cores": 1, "kind": "oracle",
-                                "sample": f"{n} oracle steps on {frac:.2%} of each layer's output rows "
-                                          f"(all tokens), single thread, {n * sec_step:.1f} s"}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.eager:
+        line["cpu_baseline"] = cpu_baseline(wl, args.format, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -111,10 +111,10 @@ bl_status bitlinear_pack_weights(const float* W, int64_t N, int64_t K, float eps
  * bitlinear_pack_weights_noalloc -- the same packing as bitlinear_pack_weights
  * (identical W_packed and gamma), for callers that cannot supply device
  * workspace: applications whose device memory belongs to their own pool
- * allocator, code running during CUDA stream capture (where cudaMalloc is not
- * allowed), or plug-in hosts that only pass pointers to memory they own.  The
- * BitNet b1.58 pages have no counterpart of this call; it only changes where
- * the workspace lives.
+ * allocator (an extra cudaMalloc would fail or fragment it), and plug-in
+ * hosts that only pass pointers to memory they own.  The BitNet b1.58 pages
+ * have no counterpart of this call; it only changes where the workspace
+ * lives.
  *
  * The workspace is a fixed 512-byte array inside the library's device image
  * (held by every GPU that loads the library until the process exits), so the
@@ -123,12 +123,15 @@ bl_status bitlinear_pack_weights(const float* W, int64_t N, int64_t K, float eps
  * workspace than the array holds returns BL_ERR_WORKSPACE (the packing
  * workspace is a constant 272 bytes, so no valid shape does).
  *
- * The first call on a device, made with that device current, looks up the
- * array's device address (cudaGetSymbolAddress); make that first call before
- * any stream capture.  Every call on a device shares the one array, whose
- * contents persist between calls and are cleared on `stream` at the start of
- * each call: calls that may overlap on the GPU (different streams without
- * ordering between them) race on it and must be serialised by the caller.
+ * The first call in a CUDA context (with that context current: normally the
+ * device's primary context) looks up the array's device address with
+ * cudaGetSymbolAddress and caches it for that context; make that first call
+ * before any stream capture.  A device reset, or another context made
+ * current, is a new context and gets its own lookup.  Every call in a
+ * context shares the one array, whose contents persist between calls and are
+ * cleared on `stream` at the start of each call: calls that may overlap on
+ * the GPU (different streams without ordering between them) race on it and
+ * must be serialised by the caller.
  */
 bl_status bitlinear_pack_weights_noalloc(const float* W, int64_t N, int64_t K, float eps, uint8_t* W_packed,
                                          float* gamma, cudaStream_t stream);
@@ -194,23 +197,28 @@ bl_status bitlinear_quant_act(const void* X, bl_dtype dtype, int64_t M, int64_t 
 /*
  * bitlinear_rmsnorm_quant_act -- the normalisation that BitNet b1.58 2B4T adds
  * inside each sub-layer, ahead of a BitLinear (yousumm.com transcript, the
- * paragraph after the poker-chip analogy), folded into the per-token absmax
- * quantisation.  The pages give no
- * formula; this is RMS normalisation with an optional per-channel gain,
- * x_n = X * gain / sqrt(mean(X^2) + eps).  The RMS factor is one positive
- * number per token and absmax codes are invariant to it, so
- *   x_q = quantisation of X * gain   (bit-identical to bitlinear_quant_act of
- *                                     the fp32 products X * gain)
- *   s[m] = s(X * gain) * sqrt(mean(X[m,:]^2) + eps)
- * and bitlinear_forward(..., x_q, s, ...) then yields W_q applied to x_n.
+ * paragraph after the poker-chip analogy), followed by the per-token absmax
+ * quantisation of the normalised row.  The pages give no formula; this is
+ * RMS normalisation with an optional per-channel gain, per token m:
+ *
+ *   ms   = mean_k X[m,k]^2: the exact real mean of the squares, rounded once
+ *          to fp32 (ties to even), so it does not depend on summation order
+ *   r    = fp32(sqrt(fp32(ms + eps)))            (IEEE square root)
+ *   x_n  = fp32(fp32(X[m,k] * gain[k]) / r)      (one multiply, one division)
+ *   x_q, s = bitlinear_quant_act of x_n           (bit for bit)
+ *
+ * so bitlinear_forward(..., x_q, s, ...) then yields W_q applied to x_n.
  *
  *   X       in   [M, K] row-major, BL_BF16 or BL_F32, element-aligned
+ *   M, K    in   M >= 1, 1 <= K <= 2^24
  *   gain    in   fp32 [K] (4-byte aligned) or NULL for all ones
- *   eps     in   finite, >= 0
+ *   eps     in   finite, > 0
  *   x_q, s  out  as for bitlinear_quant_act (x_q needs no alignment here)
  *
- * mean(X^2) is summed in fp64 in an unspecified order, so s may differ from
- * an fp64 sequential sum in its last bit; x_q does not depend on it.
+ * Results are unspecified where X holds a non-finite value or X * gain
+ * overflows fp32.  A row whose mean square overflows fp32 gives r = inf and
+ * x_q = 0.  One CTA per token; rows and gains that are 16-byte aligned take a
+ * vectorised path with the same arithmetic.
  */
 bl_status bitlinear_rmsnorm_quant_act(const void* X, bl_dtype dtype, int64_t M, int64_t K, const float* gain,
                                       float eps, int8_t* x_q, float* s, cudaStream_t stream);

@@ -23,8 +23,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "bitlinear_oracle.c")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_LIB_OMP_PATH = os.path.join(_BUILD_DIR, "liboracle_omp.so")
 _lock = threading.Lock()
-_lib = None
+_libs = {}
 
 # The activation clamp of reading R4 and the eps of the configurations.
 ACT_CLAMP_EPS = np.float32(1e-5)
@@ -33,22 +34,25 @@ WEIGHT_EPS = np.float32(1e-5)
 _CFLAGS = ["-O2", "-std=gnu11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math", "-fno-builtin-rintf"]
 
 
-def build(force: bool = False) -> str:
-    """Compile the oracle shared library (idempotent).  Returns its path."""
+def build(force: bool = False, omp: bool = False) -> str:
+    """Compile the oracle shared library (idempotent).  Returns its path.
+    omp=True builds the same source with -fopenmp (loops over independent
+    outputs on several host threads; identical results)."""
+    path = _LIB_OMP_PATH if omp else _LIB_PATH
     with _lock:
-        stale = (not os.path.exists(_LIB_PATH)) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)
+        stale = (not os.path.exists(path)) or os.path.getmtime(path) < os.path.getmtime(_SRC)
         if force or stale:
             os.makedirs(_BUILD_DIR, exist_ok=True)
-            tmp = _LIB_PATH + f".tmp{os.getpid()}"
-            subprocess.run(["gcc", *_CFLAGS, _SRC, "-o", tmp, "-lm"], check=True)
-            os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+            tmp = path + f".tmp{os.getpid()}"
+            extra = ["-fopenmp"] if omp else []
+            subprocess.run(["gcc", *_CFLAGS, *extra, _SRC, "-o", tmp, "-lm"], check=True)
+            os.replace(tmp, path)
+    return path
 
 
-def _load():
-    global _lib
-    if _lib is None:
-        lib = ctypes.CDLL(build())
+def _load(omp: bool = False):
+    if omp not in _libs:
+        lib = ctypes.CDLL(build(omp=omp))
         P = ctypes.c_void_p
         u64, i64 = ctypes.c_uint64, ctypes.c_int64
         lib.oracle_absmean.argtypes = [P, u64]
@@ -72,8 +76,15 @@ def _load():
         lib.oracle_relu2.argtypes = [P, i64]
         lib.oracle_forward.argtypes = [P, ctypes.c_float, P, P, i64, i64, i64, P, P]
         lib.oracle_forward.restype = i64
-        _lib = lib
-    return _lib
+        lib.oracle_num_threads.argtypes = []
+        lib.oracle_num_threads.restype = ctypes.c_int
+        _libs[omp] = lib
+    return _libs[omp]
+
+
+def num_threads(omp: bool = True) -> int:
+    """Host threads the oracle's loops use in the OpenMP build (1 otherwise)."""
+    return int(_load(omp).oracle_num_threads())
 
 
 def _c(a: np.ndarray, dtype) -> np.ndarray:
@@ -179,13 +190,14 @@ def bf16_bits_to_f32(x_bits: np.ndarray) -> np.ndarray:
     return out
 
 
-def quant_act(X: np.ndarray, clamp_eps=ACT_CLAMP_EPS) -> tuple[np.ndarray, np.ndarray]:
-    """Per-token absmax int8 quantisation (readings R4, R5).  X is fp32 [M, K]."""
+def quant_act(X: np.ndarray, clamp_eps=ACT_CLAMP_EPS, omp: bool = False) -> tuple[np.ndarray, np.ndarray]:
+    """Per-token absmax int8 quantisation (readings R4, R5).  X is fp32 [M, K].
+    omp=True runs the tokens on several host threads (same results)."""
     X = _c(X, np.float32)
     M, K = X.shape
     xq = np.empty((M, K), dtype=np.int8)
     s = np.empty((M,), dtype=np.float32)
-    _load().oracle_quant_act(_p(X), M, K, float(np.float32(clamp_eps)), _p(xq), _p(s))
+    _load(omp).oracle_quant_act(_p(X), M, K, float(np.float32(clamp_eps)), _p(xq), _p(s))
     return xq, s
 
 
@@ -223,7 +235,7 @@ def relu2(y: np.ndarray) -> np.ndarray:
     return out
 
 
-def matmul_int(q: np.ndarray, x_q: np.ndarray) -> np.ndarray:
+def matmul_int(q: np.ndarray, x_q: np.ndarray, omp: bool = False) -> np.ndarray:
     """acc[m, n] = sum_k q[n, k] * x_q[m, k] in exact integer arithmetic."""
     q = _c(q, np.int8)
     x_q = _c(x_q, np.int8)
@@ -232,7 +244,7 @@ def matmul_int(q: np.ndarray, x_q: np.ndarray) -> np.ndarray:
     if K != K2:
         raise ValueError("K mismatch")
     acc = np.empty((M, N), dtype=np.int32)
-    _load().oracle_matmul_int(_p(q), _p(x_q), M, N, K, _p(acc))
+    _load(omp).oracle_matmul_int(_p(q), _p(x_q), M, N, K, _p(acc))
     return acc
 
 
@@ -246,8 +258,10 @@ def dequant(acc: np.ndarray, gamma, s: np.ndarray) -> np.ndarray:
     return y
 
 
-def forward(W_packed: np.ndarray, gamma, x_q: np.ndarray, s: np.ndarray, K: int) -> tuple[np.ndarray, np.ndarray]:
-    """Forward pass from packed weights.  Returns (y fp32 [M,N], acc int32 [M,N])."""
+def forward(W_packed: np.ndarray, gamma, x_q: np.ndarray, s: np.ndarray, K: int,
+            omp: bool = False) -> tuple[np.ndarray, np.ndarray]:
+    """Forward pass from packed weights.  Returns (y fp32 [M,N], acc int32 [M,N]).
+    omp=True runs the independent outputs on several host threads (same results)."""
     W_packed = _c(W_packed, np.uint8)
     x_q = _c(x_q, np.int8)
     s = _c(s, np.float32)
@@ -257,7 +271,7 @@ def forward(W_packed: np.ndarray, gamma, x_q: np.ndarray, s: np.ndarray, K: int)
         raise ValueError("shape mismatch")
     y = np.empty((M, N), dtype=np.float32)
     acc = np.empty((M, N), dtype=np.int32)
-    rc = _load().oracle_forward(_p(W_packed), float(np.float32(gamma)), _p(x_q), _p(s), M, N, K, _p(y), _p(acc))
+    rc = _load(omp).oracle_forward(_p(W_packed), float(np.float32(gamma)), _p(x_q), _p(s), M, N, K, _p(y), _p(acc))
     if rc < 0:
         raise MemoryError("oracle_forward allocation failed")
     if rc > 0:

@@ -46,10 +46,17 @@
  *       codes) to a multiple of 16.
  *
  * Build: plain C11, -O2 -ffp-contract=off, no fast-math (so every float
- * operation is a single IEEE-754 binary32 operation with RNE).
+ * operation is a single IEEE-754 binary32 operation with RNE).  The same
+ * source is also built with -fopenmp: the loops over independent outputs
+ * (rows of the product, tokens, packed bytes) then run on several host
+ * threads.  Every output is still computed by the same sequential code, so
+ * both builds give identical results.
  */
 #include <math.h>
 #include <stdint.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 #include <stdlib.h>
 #include <string.h>
 
@@ -215,6 +222,7 @@ void oracle_pack(const int8_t* q, uint64_t n, uint8_t* packed) {
  * oracle_pack never writes); those decode to +2. */
 uint64_t oracle_unpack(const uint8_t* packed, uint64_t n, int8_t* q) {
   uint64_t bad = 0;
+#pragma omp parallel for reduction(+ : bad) schedule(static)
   for (uint64_t i = 0; i < n; ++i) {
     unsigned code = (packed[i / 4] >> (2 * (i % 4))) & 3u;
     if (code == 3) ++bad;
@@ -293,6 +301,7 @@ void oracle_bf16_to_f32(const uint16_t* x, uint64_t n, float* out) {
 }
 
 void oracle_quant_act(const float* X, int64_t M, int64_t K, float clamp_eps, int8_t* x_q, float* s) {
+#pragma omp parallel for schedule(static)
   for (int64_t m = 0; m < M; ++m) {
     const float* row = X + m * K;
     float a = 0.0f;
@@ -377,6 +386,7 @@ void oracle_relu2(float* y, int64_t n) {
 
 /* acc[m,n] = sum_k q[n,k] * x_q[m,k]; q is [N,K] ternary, x_q is [M,K]. */
 void oracle_matmul_int(const int8_t* q, const int8_t* x_q, int64_t M, int64_t N, int64_t K, int32_t* acc) {
+#pragma omp parallel for collapse(2) schedule(static)
   for (int64_t m = 0; m < M; ++m)
     for (int64_t n = 0; n < N; ++n) {
       int64_t sum = 0;
@@ -386,6 +396,7 @@ void oracle_matmul_int(const int8_t* q, const int8_t* x_q, int64_t M, int64_t N,
 }
 
 void oracle_dequant(const int32_t* acc, float gamma, const float* s, int64_t M, int64_t N, float* y) {
+#pragma omp parallel for schedule(static)
   for (int64_t m = 0; m < M; ++m) {
     float t = gamma / s[m];
     for (int64_t n = 0; n < N; ++n) y[m * N + n] = (float)acc[m * N + n] * t;
@@ -410,4 +421,13 @@ int64_t oracle_forward(const uint8_t* packed, float gamma, const int8_t* x_q, co
   free(q);
   if (!acc) free(a);
   return (int64_t)bad;
+}
+
+/* Host threads the loops above run on: 1 in the plain build. */
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
 }

@@ -247,9 +247,11 @@ def bitlinear_quant_act(X: torch.Tensor, x_q: torch.Tensor | None = None, s: tor
 
 def bitlinear_rmsnorm_quant_act(X: torch.Tensor, gain: torch.Tensor | None = None, eps: float = 1e-5,
                                 x_q: torch.Tensor | None = None, s: torch.Tensor | None = None, stream=None):
-    """Sub-layer RMS normalisation folded into the int8 quantisation of X
-    (bf16 or fp32 [M, K]): x_q = quant(X * gain), s = s(X * gain) *
-    sqrt(mean(X^2) + eps).  Returns (x_q int8 [M, K], s fp32 [M])."""
+    """Sub-layer RMS normalisation of X (bf16 or fp32 [M, K]) followed by the
+    int8 quantisation of the normalised rows: x_n = fp32(X * gain) /
+    fp32(sqrt(mean(X^2) + eps)) with the exact mean of squares, then
+    (x_q, s) = bitlinear_quant_act(x_n).  eps > 0.  Returns (x_q int8 [M, K],
+    s fp32 [M])."""
     M, K = X.shape
     if X.dtype == torch.bfloat16:
         dt = BL_BF16

@@ -3,7 +3,6 @@
 // Contracts are documented in include/bitlinear.h.
 #include <cmath>
 #include <cstdint>
-#include <mutex>
 
 #include "bitlinear.h"
 #include "internal.h"
@@ -14,31 +13,18 @@ static __device__ uint32_t g_bl_error_word;
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-
 struct DeviceInfo {
-  bool ready = false;
   int num_sms = 0;
   uint32_t* err = nullptr;
 };
 
-std::mutex g_mu;
-DeviceInfo g_dev[kMaxDevices];
+cudaError_t lookup_error_word(void** p) { return cudaGetSymbolAddress(p, g_bl_error_word); }
 
-// Per-device facts, filled on first use with that device current.
+// Facts of the current context: SM count and the error word's address.
 bl_status device_info(DeviceInfo* out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BL_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_mu);
-  DeviceInfo& d = g_dev[dev];
-  if (!d.ready) {
-    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return BL_ERR_CUDA;
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_bl_error_word) != cudaSuccess) return BL_ERR_CUDA;
-    d.err = static_cast<uint32_t*>(p);
-    d.ready = true;
-  }
-  *out = d;
+  void* p = nullptr;
+  if (bl_status st = bl::context_facts(bl::kSlotErrorWord, lookup_error_word, &out->num_sms, &p)) return st;
+  out->err = static_cast<uint32_t*>(p);
   return BL_OK;
 }
 
@@ -127,7 +113,7 @@ bl_status bitlinear_rmsnorm_quant_act(const void* X, bl_dtype dtype, int64_t M, 
   if (!X || !x_q || !s) return BL_ERR_INVALID_ARG;
   if (M < 1 || K < 1) return BL_ERR_INVALID_ARG;
   if (dtype != BL_F32 && dtype != BL_BF16) return BL_ERR_INVALID_ARG;
-  if (!std::isfinite(eps) || eps < 0.0f) return BL_ERR_INVALID_ARG;
+  if (!std::isfinite(eps) || !(eps > 0.0f)) return BL_ERR_INVALID_ARG;
   if (M > INT32_MAX || K > (int64_t)1 << 24) return BL_ERR_UNSUPPORTED_SHAPE;
   if (!aligned(X, dtype == BL_BF16 ? 2 : 4) || !aligned(s, 4) || (gain && !aligned(gain, 4))) return BL_ERR_MISALIGNED;
   return from_cuda(bl::launch_rmsnorm_quant_act(X, dtype == BL_BF16, M, K, gain, eps, x_q, s, stream));

@@ -5,7 +5,20 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "bitlinear.h"
+
 namespace bl {
+
+// Per-context facts (context_cache.cu).  `lookup` returns the device address
+// of one of the library's __device__ arrays in the current context (it must
+// call cudaGetSymbolAddress in the translation unit that defines the array);
+// its result is cached per context id and slot, with the current device's SM
+// count.  Slots: kSlotErrorWord, kSlotPackScratch.
+using SymbolLookup = cudaError_t (*)(void**);
+constexpr int kSlotErrorWord = 0;
+constexpr int kSlotPackScratch = 1;
+constexpr int kCtxSlots = 2;
+bl_status context_facts(int slot, SymbolLookup lookup, int* num_sms, void** addr);
 
 // Device workspace of bitlinear_pack_weights.
 struct PackWorkspace {

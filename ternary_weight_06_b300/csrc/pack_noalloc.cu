@@ -4,19 +4,19 @@
 // bitlinear_pack_weights needs a small device workspace (the exact |W| sums
 // and the zero-band threshold).  Some callers cannot provide one: a host
 // application whose device memory is owned by its own pool allocator (an
-// extra cudaMalloc would fail or fragment that pool), code running while a
-// CUDA stream is being captured (cudaMalloc is not a legal call there), and
-// plug-in hosts that only pass pointers to memory somebody else owns.  This
+// extra cudaMalloc would fail or fragment that pool), and plug-in hosts that
+// only pass pointers to memory somebody else owns.  This
 // entry point therefore keeps the workspace in a fixed array inside the
 // library's device image instead, so it allocates nothing.
 //
 // The array lives in every GPU that loads the library until the process
-// exits.  Host code cannot use its name as a device address, so the first
-// call on each device (with that device current) looks its address up once
-// with cudaGetSymbolAddress and caches it.
+// exits.  Host code cannot use its name as a device address: the address is
+// looked up with cudaGetSymbolAddress, in this file, with the device's
+// context current, and cached per CUDA context (context_cache.cu), because
+// each context has its own copy of the array and a reset device's context is
+// a new one.
 #include <cmath>
 #include <cstdint>
-#include <mutex>
 
 #include "bitlinear.h"
 #include "internal.h"
@@ -30,32 +30,7 @@ static_assert(sizeof(bl::PackWorkspace) <= kScratchBytes, "scratch too small for
 
 static __device__ __align__(256) unsigned char g_pack_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-
-struct ScratchInfo {
-  bool ready = false;
-  int num_sms = 0;
-  void* scratch = nullptr;  // device address of g_pack_scratch on this device
-};
-
-std::mutex g_mu;
-ScratchInfo g_info[kMaxDevices];
-
-bl_status scratch_for_current_device(ScratchInfo* out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BL_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_mu);
-  ScratchInfo& s = g_info[dev];
-  if (!s.ready) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_pack_scratch) != cudaSuccess || p == nullptr) return BL_ERR_CUDA;
-    if (cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return BL_ERR_CUDA;
-    s.scratch = p;
-    s.ready = true;
-  }
-  *out = s;
-  return BL_OK;
-}
+cudaError_t lookup_scratch(void** p) { return cudaGetSymbolAddress(p, g_pack_scratch); }
 
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -71,10 +46,11 @@ extern "C" bl_status bitlinear_pack_weights_noalloc(const float* W, int64_t N, i
   if (!aligned(W, 16) || !aligned(W_packed, 16) || !aligned(gamma, 4)) return BL_ERR_MISALIGNED;
   // The scratch cannot grow: refuse any request that would need more than it holds.
   if (bitlinear_pack_workspace_bytes(N, K) > kScratchBytes) return BL_ERR_WORKSPACE;
-  ScratchInfo s;
-  if (bl_status st = scratch_for_current_device(&s)) return st;
+  int num_sms = 0;
+  void* scratch = nullptr;
+  if (bl_status st = bl::context_facts(bl::kSlotPackScratch, lookup_scratch, &num_sms, &scratch)) return st;
   // launch_pack clears the workspace on `stream` before its kernels use it.
   const cudaError_t e = bl::launch_pack(W, (uint64_t)N * (uint64_t)K, eps, W_packed, gamma,
-                                        static_cast<bl::PackWorkspace*>(s.scratch), s.num_sms, stream);
+                                        static_cast<bl::PackWorkspace*>(scratch), num_sms, stream);
   return e == cudaSuccess ? BL_OK : BL_ERR_CUDA;
 }

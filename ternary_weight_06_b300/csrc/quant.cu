@@ -14,6 +14,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "sumsq_exact.cuh"
 
 namespace bl {
 namespace {
@@ -135,87 +136,35 @@ __global__ void __launch_bounds__(1024) quant_act_kernel(const void* __restrict_
   }
 }
 
-// Sub-layer RMS normalisation folded into the quantisation.  The RMS factor
-// 1/sqrt(mean(x^2) + eps) is one positive number per token, to which absmax
-// codes are invariant, so the codes are those of x * gain and only the scale
-// changes: s = s(x * gain) * sqrt(mean(x^2) + eps).
-//
-// Pass 1 forms max|x| and max|x * g| (order-free, on fp32 bit patterns).
-// Pass 2 quantises x * g with the same fp32 product, so x_q is bit-identical
-// to quantising x * g, and sums the squares.  On the 128-bit path the squares
-// are of x * 2^-e, e the exponent of max|x| (an exact scaling that keeps
-// every square <= 4, so nothing overflows fp32 and a row of tiny values keeps
-// its precision), summed in fp32 within each 16-byte chunk, and the chunk sums
-// are carried as an fp32 pair (hi, lo) with an error-free two-sum, across
-// threads too.  With all terms positive the relative error of the sum is that
-// of one chunk, about 4 fp32 ulps, so s carries about 2 ulps more than an
-// fp64 sum; fp64 is used by one thread, once, at the end (fp64 issues slowly
-// on this part).  Each thread keeps its first kRmsCache chunks of x in
-// registers between the passes, all loaded before the first is used, and the
+// Sub-layer RMS normalisation, then the quantisation of the normalised row
+// (the normalisation BitNet b1.58 2B4T adds inside each sub-layer: yousumm.com
+// transcript, the paragraph after the poker-chip analogy).  Per token:
+//   ms  = mean(x^2), exact, rounded once to fp32 (sumsq_exact.cuh)
+//   r   = fp32 sqrt(fp32(ms + eps))
+//   x_n = fp32(fp32(x * g) / r)
+//   s   = 127 / max(max|x_n|, 1e-5),  x_q = clip(rint(fp32(x_n * s)), -128, 127)
+// Division by r > 0 rounds monotonically, so max|x_n| = fp32(max|x * g| / r):
+// pass 1 forms max|x * g| (order-free, on fp32 bit patterns) and the exact
+// sum of squares; one thread finishes ms, r and s; pass 2 divides and
+// quantises.  The CTA has at least one full warp (the finish is warp-wide).
+// Each thread keeps its first kRmsCache 16-byte chunks of x in
+// registers between the passes (all loaded before the first is used); the
 // CTA is sized so that a row of up to 1024 * kRmsCache chunks is read once.
-// The scalar path (rows or gain not 16-byte aligned) sums x^2 in fp64
-// element by element.
+// Rows or gains that are not 16-byte aligned take an element-wise path with
+// the same arithmetic.
 
-__device__ __forceinline__ void block_reduce_max2(uint32_t& a, uint32_t& b, uint32_t* red) {
+__device__ __forceinline__ uint32_t block_reduce_max(uint32_t a, uint32_t* red) {
   const int tid = threadIdx.x, nw = blockDim.x >> 5;
   a = __reduce_max_sync(0xffffffffu, a);
-  b = __reduce_max_sync(0xffffffffu, b);
-  if ((tid & 31) == 0) {
-    red[tid >> 5] = a;
-    red[32 + (tid >> 5)] = b;
-  }
+  if ((tid & 31) == 0) red[tid >> 5] = a;
   __syncthreads();
   if (tid < 32) {
-    uint32_t u = tid < nw ? red[tid] : 0u, v = tid < nw ? red[32 + tid] : 0u;
-    u = __reduce_max_sync(0xffffffffu, u);
+    uint32_t v = tid < nw ? red[tid] : 0u;
     v = __reduce_max_sync(0xffffffffu, v);
-    if (tid == 0) {
-      red[64] = u;
-      red[65] = v;
-    }
+    if (tid == 0) red[32] = v;
   }
   __syncthreads();
-  a = red[64];
-  b = red[65];
-}
-
-// (hi, lo) += p with hi + lo kept exactly up to the rounding of lo (Knuth's two-sum)
-__device__ __forceinline__ void two_sum_add(float& hi, float& lo, float p) {
-  const float t = __fadd_rn(hi, p);
-  const float z = __fsub_rn(t, hi);
-  const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(t, z)), __fsub_rn(p, z));
-  hi = t;
-  lo = __fadd_rn(lo, err);
-}
-
-__device__ __forceinline__ double block_reduce_pair(float hi, float lo, float2* red) {
-  const int tid = threadIdx.x, nw = blockDim.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float h2 = __shfl_xor_sync(0xffffffffu, hi, o), l2 = __shfl_xor_sync(0xffffffffu, lo, o);
-    two_sum_add(hi, lo, h2);
-    lo = __fadd_rn(lo, l2);
-  }
-  if ((tid & 31) == 0) red[tid >> 5] = make_float2(hi, lo);
-  __syncthreads();
-  double r = 0.0;
-  if (tid < 32) {
-    const float2 v = tid < nw ? red[tid] : make_float2(0.0f, 0.0f);
-    hi = v.x;
-    lo = v.y;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float h2 = __shfl_xor_sync(0xffffffffu, hi, o), l2 = __shfl_xor_sync(0xffffffffu, lo, o);
-      two_sum_add(hi, lo, h2);
-      lo = __fadd_rn(lo, l2);
-    }
-    if (tid == 0) r = (double)hi + (double)lo;
-  }
-  return r;  // valid in thread 0
-}
-
-__device__ __forceinline__ float sq_sum4(float a, float b, float c, float d) {
-  return __fadd_rn(__fadd_rn(__fmul_rn(a, a), __fmul_rn(b, b)), __fadd_rn(__fmul_rn(c, c), __fmul_rn(d, d)));
+  return red[32];
 }
 
 template <bool BF16>
@@ -238,7 +187,8 @@ __device__ __forceinline__ void unpack_chunk(const uint4 v, float* x) {
 template <bool BF16>
 __global__ void __launch_bounds__(1024) rmsnorm_quant_act_kernel(const void* __restrict__ X, int64_t K, bool vec,
                                                                  const float* __restrict__ gain, float eps,
-                                                                 int8_t* __restrict__ xq, float* __restrict__ s) {
+                                                                 unsigned long long recip_k, int8_t* __restrict__ xq,
+                                                                 float* __restrict__ s) {
   constexpr int kEsize = BF16 ? 2 : 4;
   constexpr int kPer = 16 / kEsize;  // elements per 16-byte chunk
   constexpr int kCache = kRmsCache;  // chunks per thread held in registers between the passes
@@ -248,8 +198,11 @@ __global__ void __launch_bounds__(1024) rmsnorm_quant_act_kernel(const void* __r
   const float4* gain4 = reinterpret_cast<const float4*>(gain);
   int8_t* out = xq + m * K;
   const int tid = threadIdx.x, nt = blockDim.x;
-  __shared__ uint32_t red[66];
-  __shared__ float2 red_ss[32];
+  __shared__ uint32_t red[33];
+  __shared__ SqBuckets sb;
+  __shared__ float fin[2];  // r, s
+  sq_clear(&sb);
+  __syncthreads();
 
   auto load_gain = [&](int64_t c, float (&g)[kPer]) {
     if (gain) {
@@ -271,17 +224,18 @@ __global__ void __launch_bounds__(1024) rmsnorm_quant_act_kernel(const void* __r
                 : reinterpret_cast<const float*>(row)[k];
   };
 
-  // pass 1: max|x| and max|x * g|
-  uint32_t amax_x = 0, amax_g = 0;
+  // pass 1: max|x * g| and the exact sum of x^2
+  uint32_t amax_t = 0;
+  SqAcc sq;
   const int64_t nch = vec ? K / kPer : 0;
   uint4 xc[kCache];
-  auto amax_chunk = [&](const uint4 v, const float (&g)[kPer]) {
+  auto pass1_chunk = [&](const uint4 v, const float (&g)[kPer]) {
     float x[kPer];
     unpack_chunk<BF16>(v, x);
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
-      amax_x = max(amax_x, __float_as_uint(x[i]) & 0x7fffffffu);
-      amax_g = max(amax_g, __float_as_uint(__fmul_rn(x[i], g[i])) & 0x7fffffffu);
+      amax_t = max(amax_t, __float_as_uint(__fmul_rn(x[i], g[i])) & 0x7fffffffu);
+      sq.add(x[i], &sb);
     }
   };
   if (vec) {
@@ -296,49 +250,47 @@ __global__ void __launch_bounds__(1024) rmsnorm_quant_act_kernel(const void* __r
       if (c < nch) {
         float g[kPer];
         load_gain(c, g);
-        amax_chunk(xc[i], g);
+        pass1_chunk(xc[i], g);
       }
     }
     for (int64_t c = tid + (int64_t)kCache * nt; c < nch; c += nt) {
       float g[kPer];
       load_gain(c, g);
-      amax_chunk(__ldg(row4 + c), g);
+      pass1_chunk(__ldg(row4 + c), g);
     }
   } else {
     for (int64_t k = tid; k < K; k += nt) {
       const float x = load(k);
-      const float xg = gain ? __fmul_rn(x, __ldg(gain + k)) : x;
-      amax_x = max(amax_x, __float_as_uint(x) & 0x7fffffffu);
-      amax_g = max(amax_g, __float_as_uint(xg) & 0x7fffffffu);
+      const float t = gain ? __fmul_rn(x, __ldg(gain + k)) : x;
+      amax_t = max(amax_t, __float_as_uint(t) & 0x7fffffffu);
+      sq.add(x, &sb);
     }
   }
-  block_reduce_max2(amax_x, amax_g, red);
-  float a = __uint_as_float(amax_g);
-  if (a < kActClampEps) a = kActClampEps;
-  const float sg = __fdiv_rn(127.0f, a);
+  sq.flush_warp(&sb);
+  amax_t = block_reduce_max(amax_t, red);  // its barriers also order the bucket adds before the finish
+  if (tid < 32) {
+    const float ms = sq_mean_f32(&sb, (uint32_t)K, recip_k);  // the whole warp
+    const float r = __fsqrt_rn(__fadd_rn(ms, eps));
+    float a = __fdiv_rn(__uint_as_float(amax_t), r);
+    if (a < kActClampEps) a = kActClampEps;
+    const float sg = __fdiv_rn(127.0f, a);
+    if (tid == 0) {
+      fin[0] = r;
+      fin[1] = sg;
+      s[m] = sg;
+    }
+  }
+  __syncthreads();
+  const float r = fin[0], sg = fin[1];
 
-  // pass 2: codes of x * g, and the sum of squares
-  double ss = 0.0;
+  // pass 2: codes of x_n = fp32(x * g) / r
   if (vec) {
-    // 2^-e with e the unbiased exponent of max|x| (max|x| * 2^-e in [1, 2));
-    // a zero row keeps scale 1; a subnormal maximum takes 2^126
-    int e = 0;
-    if (amax_x >= 0x00800000u) e = (int)(amax_x >> 23) - 127;
-    else if (amax_x != 0) e = -126;
-    const float scale = ldexpf(1.0f, -e);
-    float hi = 0.0f, lo = 0.0f;
     auto quant_chunk = [&](int64_t c, const uint4 v, const float (&g)[kPer]) {
       float x[kPer];
       unpack_chunk<BF16>(v, x);
       uint32_t q[kPer];
 #pragma unroll
-      for (int i = 0; i < kPer; ++i) q[i] = q8(__fmul_rn(x[i], g[i]), sg);
-      float part = 0.0f;
-#pragma unroll
-      for (int h = 0; h < kPer / 4; ++h)
-        part = __fadd_rn(part, sq_sum4(__fmul_rn(x[4 * h], scale), __fmul_rn(x[4 * h + 1], scale),
-                                       __fmul_rn(x[4 * h + 2], scale), __fmul_rn(x[4 * h + 3], scale)));
-      two_sum_add(hi, lo, part);
+      for (int i = 0; i < kPer; ++i) q[i] = q8(__fdiv_rn(__fmul_rn(x[i], g[i]), r), sg);
       if (BF16) {
         uint2 o;
         o.x = q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24);
@@ -362,27 +314,13 @@ __global__ void __launch_bounds__(1024) rmsnorm_quant_act_kernel(const void* __r
       load_gain(c, g);
       quant_chunk(c, __ldg(row4 + c), g);
     }
-    ss = block_reduce_pair(hi, lo, red_ss) * ldexp(1.0, 2 * e);
   } else {
     for (int64_t k = tid; k < K; k += nt) {
       const float x = load(k);
-      const float xg = gain ? __fmul_rn(x, __ldg(gain + k)) : x;
-      out[k] = (int8_t)q8(xg, sg);
-      ss = __fma_rn((double)x, (double)x, ss);
-    }
-    // fp64 block sum (this path is off the fast path)
-    __shared__ double red_d[32];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if ((tid & 31) == 0) red_d[tid >> 5] = ss;
-    __syncthreads();
-    if (tid < 32) {
-      ss = tid < (nt >> 5) ? red_d[tid] : 0.0;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      const float t = gain ? __fmul_rn(x, __ldg(gain + k)) : x;
+      out[k] = (int8_t)q8(__fdiv_rn(t, r), sg);
     }
   }
-  if (tid == 0) s[m] = (float)((double)sg * sqrt(ss / (double)K + (double)eps));
 }
 
 // ---- many tokens: rows staged in shared memory, one team of warps per row -
@@ -649,8 +587,9 @@ cudaError_t launch_rmsnorm_quant_act(const void* X, bool bf16, int64_t M, int64_
   const int64_t work = vec ? (K * esize / 16 + kRmsCache - 1) / kRmsCache : K;
   int threads = (int)((work + 31) / 32 * 32);
   if (threads > 1024) threads = 1024;
-  if (bf16) rmsnorm_quant_act_kernel<true><<<(unsigned)M, threads, 0, stream>>>(X, K, vec, gain, eps, xq, s);
-  else rmsnorm_quant_act_kernel<false><<<(unsigned)M, threads, 0, stream>>>(X, K, vec, gain, eps, xq, s);
+  const unsigned long long rk = sq_recip((uint32_t)K);
+  if (bf16) rmsnorm_quant_act_kernel<true><<<(unsigned)M, threads, 0, stream>>>(X, K, vec, gain, eps, rk, xq, s);
+  else rmsnorm_quant_act_kernel<false><<<(unsigned)M, threads, 0, stream>>>(X, K, vec, gain, eps, rk, xq, s);
   return cudaGetLastError();
 }
 

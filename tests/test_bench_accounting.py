@@ -60,3 +60,41 @@ def test_restated_routing_labels():
     assert not bench.gemv_fused_layer(layer(1, 32768 + 64, 100))
     assert bench.gemm_variant(layer(2048, 2560, 6912), 148) == "gemm_tc_x16_persistent_kernel"
     assert bench.gemm_variant(layer(16, 3200, 8640), 148).startswith("gemm_tc_x16_kernel")
+
+
+PEAKS = {"hbm_gbs": 6484.9, "bf16_tflops": 1755.4}  # ridge about 270.7 op/B
+
+
+@pytest.mark.parametrize("M,bound", [(1, "hbm"), (16, "hbm"), (176, "tensor")])
+def test_llama70b_layer_bounds_from_intensity(M, bound):
+    # 2MNK over about N*K/4 bytes of packed weights: 8 op/B per token, so 1 and
+    # 16 tokens (8, 128 op/B) sit below the ridge, 176 tokens (~1400) above it
+    for K, N in ((8192, 28672), (28672, 8192)):
+        L = layer(M, K, N)
+        nbytes = bench.forward_kernel_bytes(L, fused=bench.gemv_fused_layer(L))
+        assert bench.layer_bound(bench.layer_ops(L), nbytes, PEAKS) == bound
+
+
+def test_layer_roofline_hbm_fraction_by_hand():
+    L = layer(16, 8192, 28672)
+    # 58,720,256 B of packed weights + 16*8192 B of x_q + 64 B of s + 16*28672*4 B of y + 4 B of gamma
+    nbytes = 58_720_256 + 131_072 + 64 + 1_835_008 + 4
+    e = bench.layer_roofline(L, 20.0, True, "2bit", PEAKS, "measured")
+    assert e["algorithmic_bytes"] == nbytes and e["bound"] == "hbm" and e["unit"] == "GB/s"
+    assert abs(e["achieved"] - nbytes / 20e-6 / 1e9) < 0.1
+    assert abs(e["frac"] - nbytes / 20e-6 / 1e9 / 6484.9) < 1e-4
+
+
+def test_layer_roofline_tensor_fraction_by_hand():
+    L = layer(176, 8192, 28672)
+    e = bench.layer_roofline(L, 100.0, True, "2bit", PEAKS, "measured")
+    ops = 2 * 176 * 8192 * 28672
+    assert e["bound"] == "tensor" and e["unit"] == "TFLOP/s" and e["algorithmic_ops"] == ops
+    assert abs(e["achieved"] - ops / 100e-6 / 1e12) < 0.1
+
+
+def test_default_workload_is_the_largest_single_gpu_config():
+    assert bench.DEFAULT_WORKLOAD == "llama70b"
+    wl = workloads.WORKLOADS[bench.DEFAULT_WORKLOAD]
+    assert {L.M for L in wl.layers} == {1, 16, 176}
+    assert bench.metric_for(wl)[1] == "TOPS"

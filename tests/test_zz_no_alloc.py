@@ -1,12 +1,15 @@
 """The allocation-free packing entry point, through the C ABI.
 
 bitlinear_pack_weights_noalloc serves callers that cannot give the library
-device memory (an application-owned memory pool, code inside stream capture,
-plug-in hosts): it keeps its workspace in a fixed array in the library's
-device image.  Its output must equal bitlinear_pack_weights' output exactly
-(the tolerance of every packing test here: bit-exact bytes and gamma), on two
-calls in a row, because the shared array keeps the previous call's contents
-and must be cleared by each call.  This file is collected last on purpose.
+device memory (an application whose device memory belongs to its own pool
+allocator, plug-in hosts that only pass pointers): it keeps its workspace in
+a fixed array in the library's device image.  Its output must equal
+bitlinear_pack_weights' output exactly (the tolerance of every packing test
+here: bit-exact bytes and gamma), on two calls in a row, because the shared
+array keeps the previous call's contents and must be cleared by each call;
+the small matrix is also checked against the CPU oracle.  This file is
+collected last on purpose: if it fails, a run that stops at the first failure
+has already run every other test.
 """
 from __future__ import annotations
 
@@ -15,6 +18,8 @@ import ctypes
 import numpy as np
 import pytest
 import torch
+
+import oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -55,6 +60,9 @@ def test_noalloc_pack_matches_pack_twice_in_a_row(bl):
         torch.cuda.synchronize()
         assert torch.equal(got_p, ref_p)
         assert np.float32(got_g.item()).view(np.uint32) == np.float32(ref_g.item()).view(np.uint32)
+    p_or, g_or = oracle.pack_weights(mats[1].numpy())
+    assert np.array_equal(got_p.cpu().numpy(), p_or)
+    assert np.float32(got_g.item()).view(np.uint32) == np.float32(g_or).view(np.uint32)
     bl.bitlinear_check_device_error()
 
 
@@ -65,3 +73,10 @@ def test_noalloc_pack_rejects_bad_arguments(bl):
     assert lib.bitlinear_pack_weights_noalloc(good, 4, 66, 1e-5, good, good, None) == bl.BL_ERR_UNSUPPORTED_SHAPE
     assert lib.bitlinear_pack_weights_noalloc(good, 2**20, 2**13, 1e-5, good, good, None) == \
         bl.BL_ERR_UNSUPPORTED_SHAPE
+    # W and W_packed need 16-byte alignment, gamma 4-byte: checked before anything is launched
+    odd = ctypes.c_void_p(0x10008)
+    assert lib.bitlinear_pack_weights_noalloc(odd, 4, 64, 1e-5, good, good, None) == bl.BL_ERR_MISALIGNED
+    assert lib.bitlinear_pack_weights_noalloc(good, 4, 64, 1e-5, odd, good, None) == bl.BL_ERR_MISALIGNED
+    assert lib.bitlinear_pack_weights_noalloc(good, 4, 64, 1e-5, good, ctypes.c_void_p(0x10002), None) == \
+        bl.BL_ERR_MISALIGNED
+    assert lib.bitlinear_pack_weights_noalloc(good, 4, 64, 0.0, good, good, None) == bl.BL_ERR_INVALID_ARG
