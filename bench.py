@@ -348,6 +348,8 @@ def gemm_variant(L, num_sms: int) -> str:
     rule, restated here only to label the bench line)."""
     if L.M <= 4 and L.K <= 32768:
         return "gemv_kernel"
+    if L.M <= 64:
+        return "gemm_f8_kernel"
     ntiles_m = -(-L.M // 256)
     bn = -(-(-(-L.M // ntiles_m)) // 16) * 16
     tiles = -(-L.N // 128) * ntiles_m

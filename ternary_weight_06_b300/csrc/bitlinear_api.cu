@@ -159,9 +159,15 @@ bl_status bitlinear_quant_forward(const uint8_t* W_packed, const float* gamma, c
 }
 
 size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  (void)N;
   if (M < 1 || K < 1) return 0;
   if (M <= bl::kGemvMaxTokens && K <= bl::kGemvMaxK) return 0;  // the GEMV needs none
+  if (bl::gemm_f8_serves(M, N, K)) {
+    // the fp8 GEMM keeps partial-sum slots per CTA (one CTA per SM); without a
+    // usable device the bound assumes 256 SMs
+    DeviceInfo d;
+    const int sms = device_info(&d) == BL_OK ? d.num_sms : 256;
+    return bl::gemm_f8_workspace_bytes(M, K, sms);
+  }
   return bl::gemm_x16_workspace_bytes(M, K);
 }
 
@@ -192,6 +198,10 @@ bl_status bitlinear_forward_ws(const uint8_t* W_packed, const float* gamma, cons
   if (bl_status st = device_info(&d)) return st;
   bl::ForwardArgs a{W_packed, gamma, x_q, s, M, N, K, y, acc, d.err};
   if (M <= bl::kGemvMaxTokens && K <= bl::kGemvMaxK) return from_cuda(bl::launch_gemv(a, d.num_sms, stream));
+  if (bl::gemm_f8_serves(M, N, K)) {
+    if (cudaError_t e = bl::launch_x8_prepass(x_q, M, K, workspace, d.num_sms, stream)) return from_cuda(e);
+    return from_cuda(bl::launch_gemm_f8(a, workspace, d.num_sms, stream));
+  }
   if (cudaError_t e = bl::launch_x16_prepass(x_q, M, K, workspace, d.num_sms, stream)) return from_cuda(e);
   return from_cuda(bl::launch_gemm_tc_x16(a, workspace, d.num_sms, stream));
 }
@@ -216,6 +226,11 @@ bl_status bitlinear_quant_forward_ws(const uint8_t* W_packed, const float* gamma
     return from_cuda(bl::launch_gemv_fused(a, X, dtype == BL_BF16, x_q, s, (flags & BITLINEAR_WEIGHTS_RESIDENT) != 0,
                                            stall, d.num_sms, stream));
   if (stall) return BL_ERR_INVALID_ARG;  // the test hook exists on the one-kernel path only
+  if (bl::gemm_f8_serves(M, N, K)) {
+    if (cudaError_t e = bl::launch_quant_act_x8(X, dtype == BL_BF16, M, K, x_q, s, workspace, d.num_sms, stream))
+      return from_cuda(e);
+    return from_cuda(bl::launch_gemm_f8(a, workspace, d.num_sms, stream));
+  }
   if (cudaError_t e = bl::launch_quant_act_x16(X, dtype == BL_BF16, M, K, x_q, s, workspace, stream))
     return from_cuda(e);
   return from_cuda(bl::launch_gemm_tc_x16(a, workspace, d.num_sms, stream));

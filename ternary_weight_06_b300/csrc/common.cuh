@@ -154,5 +154,54 @@ __device__ __forceinline__ void convert_x16_f16(uint4 v, uint32_t* h /* 8 words 
   }
 }
 
+// ---- e4m3 activation operand of the fp8 GEMM (shared by the GEMM's prepass
+// and the activation quantisation, which can write the operand directly)
+
+// e4m3 bits of an integer v with |v| <= 128 and at most four significant bits
+// (l in [0, 15], or 16 h with |h| <= 8): exponent from the top bit, the three
+// bits below it as the mantissa.
+__device__ __forceinline__ uint32_t e4m3_small(int v) {
+  if (v == 0) return 0u;
+  const uint32_t s = v < 0 ? 0x80u : 0u;
+  const uint32_t a = (uint32_t)(v < 0 ? -v : v);
+  const uint32_t e = 31u - __clz(a);
+  return s | ((e + 7u) << 3) | (((a << 3) >> e) & 7u);
+}
+
+// 16 int8 activations (natural k order, 4 words) -> the token's two e4m3
+// operand rows of the fp8 GEMM, 16 h and l (x = 16 h + l, h = x >> 4,
+// l = x & 15), 16 bytes each, in the k order [0, 2, ..., 14, 1, ..., 15].
+__device__ __forceinline__ void x8_rows16(uint4 v, uint4* hi, uint4* lo) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t H[4] = {0u, 0u, 0u, 0u}, L[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const int x = (int)(int8_t)((w[k >> 2] >> (8 * (k & 3))) & 0xffu);
+    const int p = (k & 1) ? 8 + (k >> 1) : (k >> 1);  // position of k in the operand order
+    H[p >> 2] |= e4m3_small(16 * (x >> 4)) << (8 * (p & 3));
+    L[p >> 2] |= e4m3_small(x & 15) << (8 * (p & 3));
+  }
+  *hi = make_uint4(H[0], H[1], H[2], H[3]);
+  *lo = make_uint4(L[0], L[1], L[2], L[3]);
+}
+
+// Tiled layout of that operand: blocks of BN tokens x kX8Block k, each block
+// NB = 2 BN rows (16 h and l of every token) of kX8Block bytes stored as four
+// 128-byte-wide boxes [NB rows][128 B] one after another, with the 128-byte
+// swizzle of the MMA's shared-memory operands applied (16-byte chunk c of row
+// j at chunk c ^ (j & 7)); block (token tile mt, k-block kb) starts at byte
+// (mt * nkb + kb) * NB * kX8Block.  One contiguous copy of a block gives the
+// shared-memory image the MMA reads.  Rows of tokens past M and bytes of k
+// past K are zero.
+constexpr int kX8Block = 512;
+
+// Byte offset of the 16-byte group of k = k16 .. k16 + 15 (k16 % 16 == 0) in
+// row hl (0: 16 h, 1: l) of token m.
+__device__ __forceinline__ size_t x8_group_offset(int64_t m, int64_t k16, int hl, int BN, int64_t nkb) {
+  const int64_t mt = m / BN, kb = k16 / kX8Block;
+  const int t = (int)(m - mt * BN), kk = (int)(k16 - kb * kX8Block);
+  const int NB = 2 * BN, j = 2 * t + hl, c = (kk & 127) >> 4;
+  return (size_t)(mt * nkb + kb) * (size_t)(NB * kX8Block) + (size_t)((kk >> 7) * NB * 128 + j * 128 + ((c ^ (j & 7)) << 4));
+}
 
 }  // namespace bl

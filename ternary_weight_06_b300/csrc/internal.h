@@ -2,6 +2,7 @@
 // kernel translation units of libbitlinear.so.  Not part of the public ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -19,6 +20,13 @@ constexpr int kSlotErrorWord = 0;
 constexpr int kSlotPackScratch = 1;
 constexpr int kCtxSlots = 2;
 bl_status context_facts(int slot, SymbolLookup lookup, int* num_sms, void** addr);
+
+// TMA tensor maps (tensor_map.cu).  u8 [outer, inner] row-major, box
+// {box_inner bytes, box_outer rows}, swizzle 0 (none), 32, 64 or 128 bytes;
+// fp16 [outer, inner] row-major, box {64 elements, box_outer}, 128-byte swizzle.
+bool encode_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                  uint32_t box_outer, int swizzle_bytes);
+bool encode_f16_2d_sw128(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer);
 
 // Device workspace of bitlinear_pack_weights.
 struct PackWorkspace {
@@ -84,6 +92,28 @@ cudaError_t launch_gemv_fused(const ForwardArgs& a, const void* X, bool x_bf16, 
 constexpr int64_t kGemvMaxTokens = 4;
 constexpr int64_t kGemvMaxK = 32768;
 constexpr int64_t kTq5MaxK = 40960;  // 16 K slices x 32 lanes x 4 words x 20 weights
+
+// fp8 tensor-core GEMM (gemm_f8.cu) for up to kF8MaxTokens tokens (in tiles
+// of at most kF8MaxTile), through a
+// workspace of gemm_f8_workspace_bytes(M, K, num_sms) bytes (16-byte aligned)
+// that holds the e4m3 activation operand (2 rows per token), partial-sum
+// slots and arrival counters.  The operand and the zeroed counters come from
+// launch_x8_prepass (from x_q) or launch_quant_act_x8 (from X), in stream
+// order before launch_gemm_f8.
+constexpr int64_t kF8MaxTokens = 64;  // the kernel handles up to 2 tiles of 96; past 64 tokens the f16 GEMM is faster
+constexpr int kF8MaxTile = 96;
+bool gemm_f8_serves(int64_t M, int64_t N, int64_t K);
+int gemm_f8_token_tile(int64_t M);   // tokens per tile: M split into tiles of <= 96, rounded up to 16
+int64_t gemm_f8_kblocks(int64_t K);  // 512-k blocks of the operand: ceil(K / 512)
+size_t gemm_f8_workspace_bytes(int64_t M, int64_t K, int num_sms);
+cudaError_t launch_x8_prepass(const int8_t* xq, int64_t M, int64_t K, void* ws, int num_sms, cudaStream_t stream);
+cudaError_t launch_gemm_f8(const ForwardArgs& a, void* ws, int num_sms, cudaStream_t stream);
+uint32_t* f8_counters(void* ws, int64_t M, int64_t K, int num_sms);
+uint8_t* f8_operand(void* ws);
+// The per-token quantisation, also writing the fp8 operand (and zeroing the
+// counters) of the workspace; K % 16 == 0.
+cudaError_t launch_quant_act_x8(const void* X, bool bf16, int64_t M, int64_t K, int8_t* xq, float* s, void* ws,
+                                int num_sms, cudaStream_t stream);
 
 // Tensor-core GEMM (tcgen05) for more tokens than the GEMV handles well.
 cudaError_t launch_gemm_tc(const ForwardArgs& a, int num_sms, cudaStream_t stream);

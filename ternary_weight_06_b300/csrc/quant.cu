@@ -20,7 +20,6 @@ namespace bl {
 namespace {
 
 constexpr float kActClampEps = 1e-5f;
-constexpr int kRmsCache = 4;
 
 __device__ __forceinline__ uint32_t abs_bits_bf16x2(uint32_t w) {
   return max((w << 16) & 0x7fff0000u, w & 0x7fff0000u);
@@ -35,12 +34,37 @@ __device__ __forceinline__ uint32_t q8(float x, float s) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-template <bool BF16, bool X16>
+// Where the fp8 GEMM's operand goes (OUT == 2): the tiled layout of
+// x8_group_offset, tokens in tiles of BN, nkb 512-k blocks, M real tokens.
+struct X8Out {
+  uint8_t* x8;
+  uint32_t* cnt;  // arrival counters, zeroed by block 0
+  int ncnt;
+  int64_t M, nkb;
+  int BN;
+};
+
+// OUT: 0 x_q and s only; 1 also the fp16 operand of the f16 GEMM (x16,
+// M x K halves); 2 also the e4m3 operand of the fp8 GEMM: the grid then has a
+// CTA for every token of the last tile, and the CTAs of tokens past M (and
+// every CTA for k past K in the last block) write zeros.
+template <bool BF16, int OUT>
 __global__ void __launch_bounds__(1024) quant_act_kernel(const void* __restrict__ X, int64_t K, bool vec,
                                                          int8_t* __restrict__ xq, float* __restrict__ s,
-                                                         uint4* __restrict__ x16) {
+                                                         uint4* __restrict__ xop, const X8Out o8) {
   constexpr int kEsize = BF16 ? 2 : 4;
   const int64_t m = blockIdx.x;
+  if (OUT == 2) {
+    if (blockIdx.x == 0)
+      for (int i = threadIdx.x; i < o8.ncnt; i += blockDim.x) o8.cnt[i] = 0u;
+    const int64_t kpad = o8.nkb * kX8Block;
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    for (int64_t k16 = (m < o8.M ? K : 0) + 16 * (int64_t)threadIdx.x; k16 < kpad; k16 += 16 * (int64_t)blockDim.x) {
+      *reinterpret_cast<uint4*>(o8.x8 + x8_group_offset(m, k16, 0, o8.BN, o8.nkb)) = z;
+      *reinterpret_cast<uint4*>(o8.x8 + x8_group_offset(m, k16, 1, o8.BN, o8.nkb)) = z;
+    }
+    if (m >= o8.M) return;  // a padding token of the last tile: zeros only (whole CTA, before any barrier)
+  }
   const char* row = static_cast<const char*>(X) + m * K * kEsize;
   int8_t* out = xq + m * K;
   const int tid = threadIdx.x, nt = blockDim.x;
@@ -80,11 +104,11 @@ __global__ void __launch_bounds__(1024) quant_act_kernel(const void* __restrict_
   const float sm = __fdiv_rn(127.0f, a);
   if (tid == 0) s[m] = sm;
 
-  if (X16) {
-    // groups of 16 activations: x_q (natural order) and the GEMM's fp16 operand
-    // (order p = 4i + j within the group); K % 16 == 0
+  if (OUT != 0) {
+    // groups of 16 activations: x_q (natural order) and the GEMM's operand:
+    // fp16 in the order p = 4i + j within the group, or the two e4m3 rows;
+    // K % 16 == 0
     const uint4* r4 = reinterpret_cast<const uint4*>(row);
-    uint4* xo = x16 + m * (K / 8);
     for (int64_t g = tid; g < K / 16; g += nt) {
       uint32_t nat[4];
       if (BF16) {
@@ -104,10 +128,18 @@ __global__ void __launch_bounds__(1024) quant_act_kernel(const void* __restrict_
       }
       const uint4 q4 = make_uint4(nat[0], nat[1], nat[2], nat[3]);
       reinterpret_cast<uint4*>(out)[g] = q4;
-      uint32_t h[8];
-      convert_x16_f16(q4, h);
-      xo[2 * g] = make_uint4(h[0], h[1], h[2], h[3]);
-      xo[2 * g + 1] = make_uint4(h[4], h[5], h[6], h[7]);
+      if (OUT == 1) {
+        uint32_t h[8];
+        convert_x16_f16(q4, h);
+        uint4* xo = xop + m * (K / 8);
+        xo[2 * g] = make_uint4(h[0], h[1], h[2], h[3]);
+        xo[2 * g + 1] = make_uint4(h[4], h[5], h[6], h[7]);
+      } else {
+        uint4 hi, lo;
+        x8_rows16(q4, &hi, &lo);
+        *reinterpret_cast<uint4*>(o8.x8 + x8_group_offset(m, 16 * g, 0, o8.BN, o8.nkb)) = hi;
+        *reinterpret_cast<uint4*>(o8.x8 + x8_group_offset(m, 16 * g, 1, o8.BN, o8.nkb)) = lo;
+      }
     }
   } else if (vec) {
     const uint4* r4 = reinterpret_cast<const uint4*>(row);
@@ -143,28 +175,40 @@ __global__ void __launch_bounds__(1024) quant_act_kernel(const void* __restrict_
 //   r   = fp32 sqrt(fp32(ms + eps))
 //   x_n = fp32(fp32(x * g) / r)
 //   s   = 127 / max(max|x_n|, 1e-5),  x_q = clip(rint(fp32(x_n * s)), -128, 127)
-// Division by r > 0 rounds monotonically, so max|x_n| = fp32(max|x * g| / r):
-// pass 1 forms max|x * g| (order-free, on fp32 bit patterns) and the exact
-// sum of squares; one thread finishes ms, r and s; pass 2 divides and
-// quantises.  The CTA has at least one full warp (the finish is warp-wide).
-// Each thread keeps its first kRmsCache 16-byte chunks of x in
-// registers between the passes (all loaded before the first is used); the
-// CTA is sized so that a row of up to 1024 * kRmsCache chunks is read once.
+// Division by r > 0 rounds monotonically, so max|x_n| = fp32(max|x * g| / r).
+// One CTA per token (at least one full warp: the finish is warp-wide), three
+// passes over the row, each a rolled loop over 16-byte chunks (the row is
+// read from DRAM once, then from L1):
+//   1. max|x * g| and max|x| (order-free, on fp32 bit patterns); max|x| fixes
+//      the top exponent group of the squares;
+//   2. the exact sum of x^2;
+//   3. after one warp has finished ms, r and s: the codes of x_n.
+// The code stays small on purpose: each CTA runs it once, on whichever SM it
+// lands, so instruction fetch, not arithmetic, sets a short row's time.
 // Rows or gains that are not 16-byte aligned take an element-wise path with
 // the same arithmetic.
 
-__device__ __forceinline__ uint32_t block_reduce_max(uint32_t a, uint32_t* red) {
+__device__ __forceinline__ void block_reduce_max2(uint32_t& a, uint32_t& b, uint32_t* red) {
   const int tid = threadIdx.x, nw = blockDim.x >> 5;
   a = __reduce_max_sync(0xffffffffu, a);
-  if ((tid & 31) == 0) red[tid >> 5] = a;
-  __syncthreads();
-  if (tid < 32) {
-    uint32_t v = tid < nw ? red[tid] : 0u;
-    v = __reduce_max_sync(0xffffffffu, v);
-    if (tid == 0) red[32] = v;
+  b = __reduce_max_sync(0xffffffffu, b);
+  if ((tid & 31) == 0) {
+    red[tid >> 5] = a;
+    red[32 + (tid >> 5)] = b;
   }
   __syncthreads();
-  return red[32];
+  if (tid < 32) {
+    uint32_t u = tid < nw ? red[tid] : 0u, v = tid < nw ? red[32 + tid] : 0u;
+    u = __reduce_max_sync(0xffffffffu, u);
+    v = __reduce_max_sync(0xffffffffu, v);
+    if (tid == 0) {
+      red[64] = u;
+      red[65] = v;
+    }
+  }
+  __syncthreads();
+  a = red[64];
+  b = red[65];
 }
 
 template <bool BF16>
@@ -191,18 +235,16 @@ __global__ void __launch_bounds__(1024) rmsnorm_quant_act_kernel(const void* __r
                                                                  float* __restrict__ s) {
   constexpr int kEsize = BF16 ? 2 : 4;
   constexpr int kPer = 16 / kEsize;  // elements per 16-byte chunk
-  constexpr int kCache = kRmsCache;  // chunks per thread held in registers between the passes
   const int64_t m = blockIdx.x;
   const char* row = static_cast<const char*>(X) + m * K * kEsize;
   const uint4* row4 = reinterpret_cast<const uint4*>(row);
   const float4* gain4 = reinterpret_cast<const float4*>(gain);
   int8_t* out = xq + m * K;
   const int tid = threadIdx.x, nt = blockDim.x;
-  __shared__ uint32_t red[33];
+  __shared__ uint32_t red[66];
   __shared__ SqBuckets sb;
   __shared__ float fin[2];  // r, s
   sq_clear(&sb);
-  __syncthreads();
 
   auto load_gain = [&](int64_t c, float (&g)[kPer]) {
     if (gain) {
@@ -223,51 +265,49 @@ __global__ void __launch_bounds__(1024) rmsnorm_quant_act_kernel(const void* __r
     return BF16 ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(row)[k] << 16)
                 : reinterpret_cast<const float*>(row)[k];
   };
-
-  // pass 1: max|x * g| and the exact sum of x^2
-  uint32_t amax_t = 0;
-  SqAcc sq;
   const int64_t nch = vec ? K / kPer : 0;
-  uint4 xc[kCache];
-  auto pass1_chunk = [&](const uint4 v, const float (&g)[kPer]) {
-    float x[kPer];
-    unpack_chunk<BF16>(v, x);
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      amax_t = max(amax_t, __float_as_uint(__fmul_rn(x[i], g[i])) & 0x7fffffffu);
-      sq.add(x[i], &sb);
-    }
-  };
+
+  // pass 1: max|x * g| and max|x|
+  uint32_t amax_t = 0, amax_x = 0;
   if (vec) {
+#pragma unroll 1
+    for (int64_t c = tid; c < nch; c += nt) {
+      float x[kPer], g[kPer];
+      unpack_chunk<BF16>(__ldg(row4 + c), x);
+      load_gain(c, g);
 #pragma unroll
-    for (int i = 0; i < kCache; ++i) {
-      const int64_t c = tid + (int64_t)i * nt;
-      if (c < nch) xc[i] = __ldg(row4 + c);  // every load in flight before the first use
-    }
-#pragma unroll
-    for (int i = 0; i < kCache; ++i) {
-      const int64_t c = tid + (int64_t)i * nt;
-      if (c < nch) {
-        float g[kPer];
-        load_gain(c, g);
-        pass1_chunk(xc[i], g);
+      for (int i = 0; i < kPer; ++i) {
+        amax_x = max(amax_x, __float_as_uint(x[i]) & 0x7fffffffu);
+        amax_t = max(amax_t, __float_as_uint(__fmul_rn(x[i], g[i])) & 0x7fffffffu);
       }
     }
-    for (int64_t c = tid + (int64_t)kCache * nt; c < nch; c += nt) {
-      float g[kPer];
-      load_gain(c, g);
-      pass1_chunk(__ldg(row4 + c), g);
-    }
   } else {
+#pragma unroll 1
     for (int64_t k = tid; k < K; k += nt) {
       const float x = load(k);
       const float t = gain ? __fmul_rn(x, __ldg(gain + k)) : x;
+      amax_x = max(amax_x, __float_as_uint(x) & 0x7fffffffu);
       amax_t = max(amax_t, __float_as_uint(t) & 0x7fffffffu);
-      sq.add(x, &sb);
     }
   }
+  block_reduce_max2(amax_t, amax_x, red);  // its barriers also order sq_clear before the adds
+
+  // pass 2: the exact sum of x^2
+  SqAcc sq(sq_group(amax_x));
+  if (vec) {
+#pragma unroll 1
+    for (int64_t c = tid; c < nch; c += nt) {
+      float x[kPer];
+      unpack_chunk<BF16>(__ldg(row4 + c), x);
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) sq.add(x[i], &sb);
+    }
+  } else {
+#pragma unroll 1
+    for (int64_t k = tid; k < K; k += nt) sq.add(load(k), &sb);
+  }
   sq.flush_warp(&sb);
-  amax_t = block_reduce_max(amax_t, red);  // its barriers also order the bucket adds before the finish
+  __syncthreads();
   if (tid < 32) {
     const float ms = sq_mean_f32(&sb, (uint32_t)K, recip_k);  // the whole warp
     const float r = __fsqrt_rn(__fadd_rn(ms, eps));
@@ -283,11 +323,13 @@ __global__ void __launch_bounds__(1024) rmsnorm_quant_act_kernel(const void* __r
   __syncthreads();
   const float r = fin[0], sg = fin[1];
 
-  // pass 2: codes of x_n = fp32(x * g) / r
+  // pass 3: codes of x_n = fp32(x * g) / r
   if (vec) {
-    auto quant_chunk = [&](int64_t c, const uint4 v, const float (&g)[kPer]) {
-      float x[kPer];
-      unpack_chunk<BF16>(v, x);
+#pragma unroll 1
+    for (int64_t c = tid; c < nch; c += nt) {
+      float x[kPer], g[kPer];
+      unpack_chunk<BF16>(__ldg(row4 + c), x);
+      load_gain(c, g);  // the gain row is shared by every token: an L1 hit
       uint32_t q[kPer];
 #pragma unroll
       for (int i = 0; i < kPer; ++i) q[i] = q8(__fdiv_rn(__fmul_rn(x[i], g[i]), r), sg);
@@ -299,22 +341,9 @@ __global__ void __launch_bounds__(1024) rmsnorm_quant_act_kernel(const void* __r
       } else {
         reinterpret_cast<uint32_t*>(out)[c] = q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24);
       }
-    };
-#pragma unroll
-    for (int i = 0; i < kCache; ++i) {
-      const int64_t c = tid + (int64_t)i * nt;
-      if (c < nch) {
-        float g[kPer];
-        load_gain(c, g);  // the gain row is shared by every token: an L1 hit
-        quant_chunk(c, xc[i], g);
-      }
-    }
-    for (int64_t c = tid + (int64_t)kCache * nt; c < nch; c += nt) {
-      float g[kPer];
-      load_gain(c, g);
-      quant_chunk(c, __ldg(row4 + c), g);
     }
   } else {
+#pragma unroll 1
     for (int64_t k = tid; k < K; k += nt) {
       const float x = load(k);
       const float t = gain ? __fmul_rn(x, __ldg(gain + k)) : x;
@@ -584,7 +613,7 @@ cudaError_t launch_rmsnorm_quant_act(const void* X, bool bf16, int64_t M, int64_
   const bool vec = (K * esize) % 16 == 0 && reinterpret_cast<uintptr_t>(X) % 16 == 0 &&
                    (!gain || reinterpret_cast<uintptr_t>(gain) % 16 == 0) &&
                    reinterpret_cast<uintptr_t>(xq) % (bf16 ? 8 : 4) == 0;
-  const int64_t work = vec ? (K * esize / 16 + kRmsCache - 1) / kRmsCache : K;
+  const int64_t work = vec ? K * esize / 16 : K;
   int threads = (int)((work + 31) / 32 * 32);
   if (threads > 1024) threads = 1024;
   const unsigned long long rk = sq_recip((uint32_t)K);
@@ -607,8 +636,9 @@ cudaError_t launch_quant_act(const void* X, bool bf16, int64_t M, int64_t K, int
   int threads = (int)((work + 31) / 32 * 32);
   if (threads > 1024) threads = 1024;
   if (threads < 32) threads = 32;
-  if (bf16) quant_act_kernel<true, false><<<(unsigned)M, threads, 0, stream>>>(X, K, vec, xq, s, nullptr);
-  else quant_act_kernel<false, false><<<(unsigned)M, threads, 0, stream>>>(X, K, vec, xq, s, nullptr);
+  const X8Out none{};
+  if (bf16) quant_act_kernel<true, 0><<<(unsigned)M, threads, 0, stream>>>(X, K, vec, xq, s, nullptr, none);
+  else quant_act_kernel<false, 0><<<(unsigned)M, threads, 0, stream>>>(X, K, vec, xq, s, nullptr, none);
   return cudaGetLastError();
 }
 
@@ -619,8 +649,22 @@ cudaError_t launch_quant_act_x16(const void* X, bool bf16, int64_t M, int64_t K,
   if (threads > 1024) threads = 1024;
   if (threads < 64) threads = 64;
   uint4* o = static_cast<uint4*>(x16);
-  if (bf16) quant_act_kernel<true, true><<<(unsigned)M, threads, 0, stream>>>(X, K, true, xq, s, o);
-  else quant_act_kernel<false, true><<<(unsigned)M, threads, 0, stream>>>(X, K, true, xq, s, o);
+  const X8Out none{};
+  if (bf16) quant_act_kernel<true, 1><<<(unsigned)M, threads, 0, stream>>>(X, K, true, xq, s, o, none);
+  else quant_act_kernel<false, 1><<<(unsigned)M, threads, 0, stream>>>(X, K, true, xq, s, o, none);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_act_x8(const void* X, bool bf16, int64_t M, int64_t K, int8_t* xq, float* s, void* ws,
+                                int num_sms, cudaStream_t stream) {
+  int threads = (int)((K / 16 + 31) / 32 * 32);
+  if (threads > 1024) threads = 1024;
+  if (threads < 64) threads = 64;
+  const int BN = gemm_f8_token_tile(M);
+  const X8Out o8{f8_operand(ws), f8_counters(ws, M, K, num_sms), num_sms, M, gemm_f8_kblocks(K), BN};
+  const unsigned grid = (unsigned)((M + BN - 1) / BN * BN);  // every token of the last tile
+  if (bf16) quant_act_kernel<true, 2><<<grid, threads, 0, stream>>>(X, K, true, xq, s, nullptr, o8);
+  else quant_act_kernel<false, 2><<<grid, threads, 0, stream>>>(X, K, true, xq, s, nullptr, o8);
   return cudaGetLastError();
 }
 

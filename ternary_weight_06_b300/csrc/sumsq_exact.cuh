@@ -9,10 +9,11 @@
 //     x^2 = (sig^2 << 2 (ee & 7)) * 2^(16 g - 300),  sig^2 << 2 (ee & 7) < 2^62,
 // so a 128-bit integer per group holds the exact sum of up to 2^66 squares,
 // and the total is sum_g B[g] * 2^(16 g) units of 2^-300 (below 2^582 for
-// rows of up to 2^24 values).  A thread keeps two 128-bit register sums for
-// the two highest groups it has seen (an activation row spends almost all of
-// its values there) and adds the others into 32 shared 128-bit buckets; one
-// warp then forms the total, divides it by K exactly and rounds once.
+// rows of up to 2^24 values).  With the row's top group known (from max|x|),
+// a thread keeps 128-bit register sums for it and the group below (an
+// activation row spends almost all of its values there) and adds the others
+// into 32 shared 128-bit buckets; one warp then forms the total, divides it
+// by K exactly and rounds once.
 #pragma once
 
 #include <cstdint>
@@ -46,10 +47,16 @@ __device__ __forceinline__ void sq_bucket_add(SqBuckets* sb, uint32_t g, unsigne
   if (v1) atomicAdd(&sb->hi[g], v1);
 }
 
+// Per-thread sums for a row whose top group G (that of max|x|) is known:
+// every value's group is <= G, groups G and G - 1 (nearly all values of an
+// activation row) are summed in registers, any other value is added to its
+// shared bucket directly.
 struct SqAcc {
-  uint32_t G = 0;                     // highest group seen by this thread
-  unsigned long long h0 = 0, h1 = 0;  // sum for group G
-  unsigned long long l0 = 0, l1 = 0;  // sum for group G - 1
+  uint32_t G;
+  unsigned long long h0 = 0, h1 = 0;  // group G
+  unsigned long long l0 = 0, l1 = 0;  // group G - 1
+
+  __device__ __forceinline__ explicit SqAcc(uint32_t top_group) : G(top_group) {}
 
   __device__ __forceinline__ static void add128(unsigned long long& a0, unsigned long long& a1,
                                                 unsigned long long v) {
@@ -66,67 +73,39 @@ struct SqAcc {
     const uint32_t ee = e ? e : 1u;
     const uint32_t g = (ee >> 3) & (kSqGroups - 1);
     const unsigned long long v = ((unsigned long long)sig * sig) << (2u * (ee & 7u));
-    if (g == G) {
-      add128(h0, h1, v);
-    } else if (g + 1u == G) {
-      add128(l0, l1, v);
-    } else if (g > G) {
-      if (g == G + 1u) {
-        if (G >= 1u) sq_bucket_add(sb, G - 1u, l0, l1);
-        l0 = h0;
-        l1 = h1;
-      } else {
-        sq_bucket_add(sb, G, h0, h1);
-        if (G >= 1u) sq_bucket_add(sb, G - 1u, l0, l1);
-        l0 = l1 = 0;
-      }
-      h0 = v;
-      h1 = 0;
-      G = g;
-    } else {
-      sq_bucket_add(sb, g, v, 0);
-    }
+    if (g == G) add128(h0, h1, v);
+    else if (g + 1u == G) add128(l0, l1, v);
+    else sq_bucket_add(sb, g, v, 0);
   }
 
-  // Every lane of the warp must call it.  The register sums are added across
-  // the warp into three slots, the warp's highest group Gw and the two below
-  // it (128-bit adds with carry), and one lane adds each slot into its
-  // bucket; a lane whose own top group lies further down adds its sums
-  // itself.  One atomic per slot and warp instead of one per lane keeps the
-  // warps of a CTA from serialising on the same two buckets.
+  // Every lane of the warp must call it (all share G): the register sums are
+  // added across the warp (128-bit adds with carry) and one lane adds them to
+  // the buckets, so the warps of a CTA do not serialise on the same buckets.
   __device__ __forceinline__ void flush_warp(SqBuckets* sb) {
-    const uint32_t Gw = __reduce_max_sync(0xffffffffu, G);
-    unsigned long long a0 = 0, a1 = 0, b0 = 0, b1 = 0, c0 = 0, c1 = 0;
-    if (G == Gw) {
-      a0 = h0, a1 = h1, b0 = l0, b1 = l1;
-    } else if (G + 1u == Gw) {
-      b0 = h0, b1 = h1, c0 = l0, c1 = l1;
-    } else {
-      sq_bucket_add(sb, G, h0, h1);
-      if (G >= 1u) sq_bucket_add(sb, G - 1u, l0, l1);
-    }
+    unsigned long long a0 = h0, a1 = h1, b0 = l0, b1 = l1;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       const unsigned long long ra0 = __shfl_xor_sync(0xffffffffu, a0, off);
       const unsigned long long ra1 = __shfl_xor_sync(0xffffffffu, a1, off);
       const unsigned long long rb0 = __shfl_xor_sync(0xffffffffu, b0, off);
       const unsigned long long rb1 = __shfl_xor_sync(0xffffffffu, b1, off);
-      const unsigned long long rc0 = __shfl_xor_sync(0xffffffffu, c0, off);
-      const unsigned long long rc1 = __shfl_xor_sync(0xffffffffu, c1, off);
       a0 += ra0;
       a1 += ra1 + ((a0 < ra0) ? 1ull : 0ull);
       b0 += rb0;
       b1 += rb1 + ((b0 < rb0) ? 1ull : 0ull);
-      c0 += rc0;
-      c1 += rc1 + ((c0 < rc0) ? 1ull : 0ull);
     }
     if ((threadIdx.x & 31u) == 0) {
-      sq_bucket_add(sb, Gw, a0, a1);
-      if (Gw >= 1u) sq_bucket_add(sb, Gw - 1u, b0, b1);
-      if (Gw >= 2u) sq_bucket_add(sb, Gw - 2u, c0, c1);
+      sq_bucket_add(sb, G, a0, a1);
+      if (G >= 1u) sq_bucket_add(sb, G - 1u, b0, b1);
     }
   }
 };
+
+// Group of a finite value's squares (see above): that of max|x| bounds them all.
+__device__ __forceinline__ uint32_t sq_group(uint32_t abs_bits) {
+  const uint32_t e = abs_bits >> 23;
+  return ((e ? e : 1u) >> 3) & (kSqGroups - 1);
+}
 
 // floor((2^64 - 1) / K): the reciprocal sq_mean_f32 divides with (host side).
 inline unsigned long long sq_recip(uint32_t K) { return 0xffffffffffffffffull / K; }
@@ -134,8 +113,9 @@ inline unsigned long long sq_recip(uint32_t K) { return 0xffffffffffffffffull / 
 // mean = (sum_g B[g] * 2^(16 g)) / K units of 2^-300, rounded once to fp32
 // (ties to even; +inf above the fp32 range).  1 <= K <= 2^24, recip =
 // sq_recip(K).  Called by all 32 lanes of one warp; every lane returns the
-// result.  Lane i (< 20) holds 32-bit word i of the 640-bit numbers, so
-// nothing is indexed at run time and everything stays in registers:
+// result.  Lane i (< 20) holds 32-bit word i of the 640-bit numbers, so no
+// array is indexed at run time and everything stays in registers; the loops
+// stay rolled (small code: the finish runs once per row):
 //   1. lane i adds up the parts of the (at most 12) groups that overlap its
 //      word, in 64 bits (12 parts of < 2^32 each);
 //   2. the carries run from word 0 up, 20 uniform shuffle steps;
@@ -146,14 +126,14 @@ inline unsigned long long sq_recip(uint32_t K) { return 0xffffffffffffffffull / 
 //   4. rounding: 24 bits from the top set bit p down, but no finer than the
 //      subnormal quantum 2^-149 = 2^151 units; round bit and sticky bit from
 //      the bits below, and the remainder.
-__device__ __forceinline__ float sq_mean_f32(const SqBuckets* sb, uint32_t K, unsigned long long recip) {
+__device__ __noinline__ float sq_mean_f32(const SqBuckets* sb, uint32_t K, unsigned long long recip) {
   constexpr unsigned kFull = 0xffffffffu;
   constexpr int kWords = 20;   // 640 bits
   constexpr int kQmin = 151;   // bit index of the subnormal quantum
   const int lane = (int)(threadIdx.x & 31u);
   unsigned long long v = 0;
   if (lane < kWords) {
-#pragma unroll
+#pragma unroll 1
     for (int j = 0; j < 12; ++j) {
       const int g = 2 * (lane - 5) + j;  // groups whose 144 shifted bits overlap word `lane`
       if (g >= 0 && g < kSqGroups) {
@@ -170,7 +150,7 @@ __device__ __forceinline__ float sq_mean_f32(const SqBuckets* sb, uint32_t K, un
   }
   uint32_t S = 0;
   unsigned long long carry = 0;
-#pragma unroll
+#pragma unroll 1
   for (int i = 0; i < kWords; ++i) {
     const unsigned long long t = __shfl_sync(kFull, v, i) + carry;
     if (lane == i) S = (uint32_t)t;
@@ -178,7 +158,7 @@ __device__ __forceinline__ float sq_mean_f32(const SqBuckets* sb, uint32_t K, un
   }
   uint32_t Q = 0;
   unsigned long long R = 0;
-#pragma unroll
+#pragma unroll 1
   for (int i = kWords - 1; i >= 0; --i) {
     const unsigned long long cur = (R << 32) | __shfl_sync(kFull, S, i);
     unsigned long long q = __umul64hi(cur, recip);

@@ -1,7 +1,9 @@
 """The C-ABI boundary on the CPU: the library builds, loads, exports every
 entry point include/bitlinear.h declares, and rejects bad arguments on the
-host before anything is launched.  No call here reaches a CUDA API: every
-case fails validation first (the pointers are fake and never dereferenced)."""
+host before anything is launched.  No call here launches anything: every
+case fails validation first (the pointers are fake and never dereferenced);
+only the workspace-size query asks the runtime for the current device's SM
+count, and assumes 256 SMs where there is no device."""
 from __future__ import annotations
 
 import ctypes
@@ -9,6 +11,7 @@ import os
 import re
 
 import pytest
+import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "bitlinear.h")
@@ -157,23 +160,38 @@ def test_quant_forward_validation(bl):
     assert qfwd(bl, acc=GOOD + 8) == bl.BL_ERR_MISALIGNED
 
 
+def f8_workspace(M, K, sms):
+    """The fp8 GEMM's workspace written out: the e4m3 operand (two rows per
+    token of a token tile of M rounded up to 16, K rounded up to 512 bytes
+    each), two partial-sum slots per CTA of 128 features x the token tile in
+    fp32, and one arrival counter per CTA, each part rounded up to 256 bytes."""
+    up = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    ntm = (M + 95) // 96  # token tiles of at most 96
+    bn = ((M + ntm - 1) // ntm + 15) // 16 * 16
+    kpad = (K + 511) // 512 * 512
+    return up(ntm * 2 * bn * kpad) + 2 * sms * bn * 128 * 4 + up(4 * sms)
+
+
 def test_forward_workspace_bytes(bl):
     f = bl.bitlinear_forward_workspace_bytes
+    sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 256
     assert f(1, 6912, 2560) == 0 and f(4, 100, 32768) == 0  # the GEMV path needs none
-    assert f(5, 100, 64) == 2 * 5 * 64
+    assert f(5, 100, 64) == f8_workspace(5, 64, sms)  # up to 64 tokens: the fp8 GEMM
+    assert f(64, 100, 2560) == f8_workspace(64, 2560, sms)
+    assert f(65, 100, 2560) == 2 * 65 * 2560  # more: the fp16 operand of the f16 GEMM
     assert f(2048, 6912, 2560) == 2 * 2048 * 2560
-    assert f(1, 100, 32768 + 64) == 2 * (32768 + 64)  # K beyond the GEMV goes to the GEMM
+    assert f(1, 100, 32768 + 64) == f8_workspace(1, 32768 + 64, sms)  # K beyond the GEMV goes to a GEMM
     assert f(0, 1, 64) == 0
 
 
-def fwd_ws(bl, M=8, N=16, K=64, ws=GOOD, ws_bytes=1 << 20, **kw):
+def fwd_ws(bl, M=8, N=16, K=64, ws=GOOD, ws_bytes=1 << 26, **kw):
     args = dict(Wp=GOOD, g=GOOD, xq=GOOD, s=GOOD, y=GOOD, acc=None)
     args.update(kw)
     return bl.get_lib().bitlinear_forward_ws(args["Wp"], args["g"], args["xq"], args["s"], M, N, K, args["y"],
                                              args["acc"], ws, ws_bytes, None)
 
 
-def qfwd_ws(bl, M=8, N=16, K=64, ws=GOOD, ws_bytes=1 << 20, dt=1, flags=0, **kw):
+def qfwd_ws(bl, M=8, N=16, K=64, ws=GOOD, ws_bytes=1 << 26, dt=1, flags=0, **kw):
     args = dict(Wp=GOOD, g=GOOD, X=GOOD, y=GOOD, xq=GOOD, s=GOOD, acc=None)
     args.update(kw)
     return bl.get_lib().bitlinear_quant_forward_ws(args["Wp"], args["g"], args["X"], dt, M, N, K, args["y"],

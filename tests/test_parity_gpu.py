@@ -579,3 +579,46 @@ def test_forward_extreme_magnitudes_large_k(bl, M, N, K):
         assert np.array_equal(y.cpu().numpy().view(np.uint32), y_ref.view(np.uint32))
         del y, acc
     bl.bitlinear_check_device_error()
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 128, 131072), (16, 256, 65536), (64, 19200, 512), (5, 1000, 8640),
+                                   (33, 3000, 4096), (48, 130, 320), (1, 640, 40000 - 64), (3, 1, 131072),
+                                   (176, 300, 8192), (130, 1000, 2560), (96, 128, 65536), (192, 256, 4096),
+                                   (97, 2000, 640)])
+def test_forward_ws_stream_k_splits_exhaustive(bl, M, N, K):
+    """Shapes of the fp8 GEMM, whose (tile, k-block) work is cut into equal
+    ranges per SM: one output tile split over every CTA (N = 128, K = 131072),
+    ranges that start and end inside tiles, a k-block past K (K % 512 != 0),
+    token counts that are not multiples of 16, one and two token tiles (up to
+    96 tokens each, 192 in all); every output against the oracle."""
+    rng = np.random.default_rng(M + N + K)
+    q = rng.integers(-1, 2, size=(N, K)).astype(np.int8)
+    xq = rng.integers(-128, 128, size=(M, K)).astype(np.int8)
+    xq[0, :] = 127
+    s = rng.uniform(0.5, 300, size=M).astype(np.float32)
+    p = oracle.pack(q)
+    forward_case(bl, p, np.float32(0.0123), xq, s, K, np.arange(M), f"stream-K M={M} N={N} K={K}", ws=True)
+    # the fused quantise + forward on the same shape (the quantisation writes the fp8 operand)
+    X = torch.randn((M, K), generator=torch.Generator().manual_seed(M * N)).to(torch.bfloat16)
+    fused_case(bl, p, np.float32(0.02), X, K, np.arange(M), f"stream-K fused M={M} N={N} K={K}", ws=True)
+
+
+def test_forward_ws_back_to_back_reuses_workspace(bl):
+    """Two skinny calls on one workspace, then a third with another shape: the
+    arrival counters left by a call must not leak into the next"""
+    rng = np.random.default_rng(3)
+    shapes = [(16, 640, 8192), (16, 640, 8192), (40, 300, 2560)]
+    ws = torch.empty((max(bl.bitlinear_forward_workspace_bytes(M, N, K) for M, N, K in shapes),),
+                     dtype=torch.uint8, device="cuda")
+    for M, N, K in shapes:
+        q = rng.integers(-1, 2, size=(N, K)).astype(np.int8)
+        xq = rng.integers(-128, 128, size=(M, K)).astype(np.int8)
+        s = rng.uniform(0.5, 3, size=M).astype(np.float32)
+        p = oracle.pack(q)
+        y, acc = bl.bitlinear_forward_ws(gpu(torch.from_numpy(p)), gpu(torch.tensor([0.5])), gpu(torch.from_numpy(xq)),
+                                         gpu(torch.from_numpy(s)), acc=True, workspace=ws)
+        torch.cuda.synchronize()
+        y_ref, acc_ref = oracle.forward(p, np.float32(0.5), xq, s, K, omp=True)
+        assert np.array_equal(acc.cpu().numpy(), acc_ref)
+        assert np.array_equal(y.cpu().numpy().view(np.uint32), y_ref.view(np.uint32))
+    bl.bitlinear_check_device_error()
