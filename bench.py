@@ -673,6 +673,66 @@ def run_gpu(args, dist, rank, world, local):
                    + ("bitlinear_forward_tq5 (quantised activations)" if tq5 else "bitlinear_quant_forward_ws")
                    + " without and with BITLINEAR_RELU2")
 
+    # ---- the lookup-table GEMV beside the conditional-add GEMV, on the layers of
+    # at most 4 tokens (both on quantised activations, graph-replayed)
+    lut = []
+    for l, L in enumerate(wl.layers):
+        if tq5 or L.M > 4:
+            continue
+        if XQrot[l] is None:
+            XQrot[l] = [bl.bitlinear_quant_act(x, stream=stream) for x in Xrot[l]]
+            torch.cuda.synchronize()
+        us_lut = graph_us(lambda j, l=l: bl.bitlinear_forward_lut(Wrot[l][j % Rs[l]], gammas[l], XQrot[l][j % Rs[l]][0],
+                                                                  XQrot[l][j % Rs[l]][1], y=ys[l], stream=stream))
+        us_add = graph_us(lambda j, l=l: bl.bitlinear_forward(Wrot[l][j % Rs[l]], gammas[l], XQrot[l][j % Rs[l]][0],
+                                                              XQrot[l][j % Rs[l]][1], y=ys[l], stream=stream))
+        nbytes = forward_kernel_bytes(L, False)
+        lut.append({"layer": f"M={L.M} K={L.K} N={L.N}", "lut_us": round(us_lut, 3), "dp4a_us": round(us_add, 3),
+                    "lut_GB/s": round(nbytes / (us_lut * 1e-6) / 1e9, 1),
+                    "lut_frac": round(nbytes / (us_lut * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+                    "dp4a_GB/s": round(nbytes / (us_add * 1e-6) / 1e9, 1)})
+    bl.bitlinear_check_device_error(stream)
+
+    # ---- live re-ternarisation: every distinct latent matrix re-packed in place
+    # (gamma + ternarise + pack), as a training step would after each update;
+    # one graph of all the packs, replayed, median per step
+    repack = None
+    if not tq5 and args.repack:
+        latents, outs = [], []
+        for i, L in enumerate(wl.layers):
+            seed = workloads.weight_seed(wl, i)
+            if seed in [s_ for s_, _ in latents]:
+                continue
+            latents.append((seed, workloads.layer_weights(wl, i).to(dev)))
+            outs.append((torch.empty((L.N, L.K // 4), dtype=torch.uint8, device=dev),
+                         torch.empty((1,), dtype=torch.float32, device=dev),
+                         torch.empty((bl.bitlinear_pack_workspace_bytes(L.N, L.K),), dtype=torch.uint8, device=dev)))
+
+        def repack_all(_j):
+            for (_, Wl), (Wp_, g_, ws_) in zip(latents, outs):
+                bl.bitlinear_pack_weights(Wl, W_packed=Wp_, gamma=g_, workspace=ws_, stream=stream)
+
+        repack_all(0)
+        torch.cuda.synchronize()
+        gr = capture(repack_all, 1)
+        times = []
+        for _ in range(7):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            gr.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+        rp_ms = statistics.median(times)
+        rp_bytes = sum(2 * 4 * Wl.numel() + Wl.numel() // 4 for _, Wl in latents)
+        repack = {"ms_per_step": round(rp_ms, 4), "GB/s": round(rp_bytes / (rp_ms * 1e-3) / 1e9, 1),
+                  "frac": round(rp_bytes / (rp_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4), "matrices": len(latents),
+                  "algorithmic_bytes": rp_bytes,
+                  "how": "bitlinear_pack_weights of every distinct latent matrix (read twice, packed bytes "
+                         "written), one CUDA graph replayed 7 times, median; frac of the measured copy bandwidth"}
+        del latents, outs, gr
+        torch.cuda.empty_cache()
+
     e2e = run_e2e(bl, wl, step, Xs_host, y_all, K, Wm, stream, dist, world, unit, step_bytes, step_ops)
 
     config = common_config(args, wl)
@@ -701,6 +761,9 @@ def run_gpu(args, dist, rank, world, local):
                   "note": "bitlinear_quant_act alone per layer, graph-replayed over the rotating X copies; bytes = "
                           "X read + x_q written + s, frac of the measured copy bandwidth"},
         "ffn": ffn,
+        "repack": repack,
+        "lut": {"per_layer": lut, "how": "bitlinear_forward_lut (table lookup) and bitlinear_forward (conditional-add "
+                                         "GEMV) on quantised activations, graph-replayed; bytes = packed W + x_q + y"},
         "pack": {"ms": round(pack_ms, 4), "GB/s": round(pack_bytes / (pack_ms * 1e-3) / 1e9, 1),
                  "matrices": len(by_seed),
                  "note": "gamma + ternarise + pack of every distinct weight matrix (one call each), outside the step"},
@@ -803,6 +866,8 @@ def main():
     ap.add_argument("--layers", default="", help="comma-separated layer indices of the workload (default: all)")
     ap.add_argument("--cpu-seconds", type=float, default=20.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-repack", dest="repack", action="store_false",
+                    help="skip the timing of the per-step re-ternarisation of the latent weights")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

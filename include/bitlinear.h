@@ -247,6 +247,30 @@ bl_status bitlinear_rmsnorm_quant_act(const void* X, bl_dtype dtype, int64_t M, 
 bl_status bitlinear_forward(const uint8_t* W_packed, const float* gamma, const int8_t* x_q, const float* s,
                             int64_t M, int64_t N, int64_t K, float* y, int32_t* acc, cudaStream_t stream);
 
+/*
+ * bitlinear_forward_lut -- bitlinear_forward computed by table lookup instead
+ * of conditional adds: the approach that GPU inference of BitNet b1.58 still
+ * relies on (promptinjection.net, "4. GPU Support: The Fragile Boost"), kept
+ * as a comparison variant.  For every pair of activations of a token, a
+ * 16-entry table holds (c0 - 1) x[2p] + (c1 - 1) x[2p+1] for all 4-bit values
+ * c0 + 4 c1 of two packed codes; the product is then one lookup and one
+ * integer add per two weights.  acc and y are bit-identical to
+ * bitlinear_forward.  The weights are read once per token, so the call suits
+ * a few tokens (decode).
+ *
+ *   W_packed, gamma, x_q, s, y, acc   as for bitlinear_forward (y and acc need
+ *                                     only 4-byte alignment here)
+ *   M, N, K   in   M >= 1, 1 <= N <= 16384 * (number of SMs), K % 64 == 0,
+ *                  64 <= K <= BITLINEAR_MAX_K
+ *   flags     in   0 or BITLINEAR_RELU2
+ *
+ * Errors: BL_ERR_INVALID_ARG (null pointer, size < 1, unknown flag),
+ * BL_ERR_UNSUPPORTED_SHAPE, BL_ERR_MISALIGNED, BL_ERR_CUDA.
+ */
+bl_status bitlinear_forward_lut(const uint8_t* W_packed, const float* gamma, const int8_t* x_q, const float* s,
+                                int64_t M, int64_t N, int64_t K, float* y, int32_t* acc, unsigned flags,
+                                cudaStream_t stream);
+
 /* Flag of bitlinear_quant_forward: W_packed and gamma are NOT written by any
  * work still pending on `stream` (true once the weights are packed and
  * synchronised, as in serving).  The call may then start streaming weights

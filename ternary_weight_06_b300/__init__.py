@@ -14,6 +14,7 @@ Functions carry the C names:
 * :func:`bitlinear_forward`      -- packed W, gamma, x_q, s -> y fp32 [M, N] (and int32 acc)
 * :func:`bitlinear_forward_ws`, :func:`bitlinear_quant_forward_ws` -- the same with a
   caller workspace (:func:`bitlinear_forward_workspace_bytes`) for the tensor-core path
+* :func:`bitlinear_forward_lut` -- the same product by table lookup (comparison variant)
 * :func:`bitlinear_check_device_error`, :func:`bitlinear_status_string`
 """
 from __future__ import annotations
@@ -44,6 +45,7 @@ __all__ = [
     "bitlinear_tq5_row_bytes",
     "bitlinear_pack_weights_tq5",
     "bitlinear_forward_tq5",
+    "bitlinear_forward_lut",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -70,6 +72,7 @@ EXPORTED_SYMBOLS = (
     "bitlinear_tq5_row_bytes",
     "bitlinear_pack_weights_tq5",
     "bitlinear_forward_tq5",
+    "bitlinear_forward_lut",
     "bitlinear_check_device_error",
     "bitlinear_status_string",
 )
@@ -101,6 +104,8 @@ def _load() -> ctypes.CDLL:
     L.bitlinear_pack_weights_tq5.restype = i32
     L.bitlinear_forward_tq5.argtypes = [P, P, P, P, i64, i64, i64, P, P, ctypes.c_uint, P]
     L.bitlinear_forward_tq5.restype = i32
+    L.bitlinear_forward_lut.argtypes = [P, P, P, P, i64, i64, i64, P, P, ctypes.c_uint, P]
+    L.bitlinear_forward_lut.restype = i32
     L.bitlinear_forward.argtypes = [P, P, P, P, i64, i64, i64, P, P, P]
     L.bitlinear_forward.restype = i32
     L.bitlinear_pack_weights_noalloc.argtypes = [P, i64, i64, f32, P, P, P]
@@ -222,6 +227,29 @@ def bitlinear_forward_tq5(W_tq5: torch.Tensor, gamma: torch.Tensor, x_q: torch.T
                                            _dev(x_q, "x_q", torch.int8), _dev(s, "s", torch.float32), M, N, K,
                                            _dev(y, "y", torch.float32), acc_ptr, int(flags), _stream(stream)),
            "bitlinear_forward_tq5")
+    return (y, acc) if want_acc else y
+
+
+def bitlinear_forward_lut(W_packed: torch.Tensor, gamma: torch.Tensor, x_q: torch.Tensor, s: torch.Tensor,
+                          y: torch.Tensor | None = None, acc: torch.Tensor | bool | None = None, flags: int = 0,
+                          stream=None):
+    """:func:`bitlinear_forward` computed by table lookup (16-entry tables per
+    pair of activations, indexed by nibbles of the packed weights); bit-identical
+    results.  Returns y, or (y, acc) with ``acc``."""
+    N, kb = W_packed.shape
+    M, K = x_q.shape
+    if kb * 4 != K:
+        raise ValueError(f"W_packed rows have {kb} bytes but K = {K}")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x_q.device)
+    want_acc = acc is not None and acc is not False
+    if acc is True:
+        acc = torch.empty((M, N), dtype=torch.int32, device=x_q.device)
+    acc_ptr = _dev(acc, "acc", torch.int32) if want_acc else None
+    _check(get_lib().bitlinear_forward_lut(_dev(W_packed, "W_packed", torch.uint8),
+                                           _dev(gamma, "gamma", torch.float32), _dev(x_q, "x_q", torch.int8),
+                                           _dev(s, "s", torch.float32), M, N, K, _dev(y, "y", torch.float32), acc_ptr,
+                                           int(flags), _stream(stream)), "bitlinear_forward_lut")
     return (y, acc) if want_acc else y
 
 

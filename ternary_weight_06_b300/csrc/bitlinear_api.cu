@@ -134,6 +134,23 @@ bl_status bitlinear_forward(const uint8_t* W_packed, const float* gamma, const i
   return from_cuda(bl::launch_gemv(a, d.num_sms, stream));
 }
 
+bl_status bitlinear_forward_lut(const uint8_t* W_packed, const float* gamma, const int8_t* x_q, const float* s,
+                                int64_t M, int64_t N, int64_t K, float* y, int32_t* acc, unsigned flags,
+                                cudaStream_t stream) {
+  if (!W_packed || !gamma || !x_q || !s || !y) return BL_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1) return BL_ERR_INVALID_ARG;
+  if (flags & ~BITLINEAR_RELU2) return BL_ERR_INVALID_ARG;
+  if (K % 64 != 0 || K > BITLINEAR_MAX_K || M > INT32_MAX || N > INT32_MAX) return BL_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(W_packed, 16) || !aligned(x_q, 16) || !aligned(y, 4) || !aligned(gamma, 4) || !aligned(s, 4) ||
+      (acc && !aligned(acc, 4)))
+    return BL_ERR_MISALIGNED;
+  DeviceInfo d;
+  if (bl_status st = device_info(&d)) return st;
+  if (N > (int64_t)16384 * d.num_sms) return BL_ERR_UNSUPPORTED_SHAPE;  // per-CTA row sums must fit shared memory
+  bl::ForwardArgs a{W_packed, gamma, x_q, s, M, N, K, y, acc, d.err, (flags & BITLINEAR_RELU2) != 0};
+  return from_cuda(bl::launch_gemv_lut(a, d.num_sms, stream));
+}
+
 bl_status bitlinear_quant_forward(const uint8_t* W_packed, const float* gamma, const void* X, bl_dtype dtype,
                                   int64_t M, int64_t N, int64_t K, float* y, int8_t* x_q, float* s, int32_t* acc,
                                   unsigned flags, cudaStream_t stream) {

@@ -80,6 +80,11 @@ struct ForwardArgs {
 // bytes), for any M in passes of up to 4 tokens; K % 16 == 0, K <= 40960.
 cudaError_t launch_gemv_tq5(const ForwardArgs& a, int64_t pitch, int num_sms, cudaStream_t stream);
 
+// The GEMV by table lookup (gemv_lut.cu): 16-entry tables per pair of
+// activations, indexed by the nibbles of the packed weights; any M (the
+// weights are read once per token), K % 64 == 0.
+cudaError_t launch_gemv_lut(const ForwardArgs& a, int num_sms, cudaStream_t stream);
+
 // Streaming GEMV for a few tokens (tokens are taken in groups of <= 4; K <= 32768).
 cudaError_t launch_gemv(const ForwardArgs& a, int num_sms, cudaStream_t stream);
 
