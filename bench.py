@@ -255,6 +255,7 @@ def common_config(args, wl) -> dict:
             "path": ("bitlinear_quant_act + bitlinear_forward_tq5" if args.format == "tq5" else
                      ("bitlinear_quant_forward_ws (one fused quantise+GEMV kernel for M <= 4; quantisation "
                       "writing the fp16 operand, then the tcgen05 GEMM otherwise)") if args.path == "fused"
+                     else "bitlinear_quant_act + bitlinear_forward_lut (table-lookup GEMV)" if args.path == "lut"
                      else "bitlinear_quant_act + bitlinear_forward_ws"),
             "l2": "every layer rotates over copies of its packed weights and activations totalling more than "
                   "2x L2 (126 MiB); no L2 flush",
@@ -494,6 +495,9 @@ def run_gpu(args, dist, rank, world, local):
         elif fused:
             bl.bitlinear_quant_forward_ws(Wrot[l][r], gammas[l], Xrot[l][r] if X is None else X, y=ys[l],
                                           x_q=xqs[l], s=ss[l], workspace=workspace, stream=stream)
+        elif args.path == "lut":
+            bl.bitlinear_quant_act(Xrot[l][r] if X is None else X, x_q=xqs[l], s=ss[l], stream=stream)
+            bl.bitlinear_forward_lut(Wrot[l][r], gammas[l], xqs[l], ss[l], y=ys[l], stream=stream)
         else:
             bl.bitlinear_quant_act(Xrot[l][r] if X is None else X, x_q=xqs[l], s=ss[l], stream=stream)
             bl.bitlinear_forward_ws(Wrot[l][r], gammas[l], xqs[l], ss[l], y=ys[l], workspace=workspace, stream=stream)
@@ -512,6 +516,9 @@ def run_gpu(args, dist, rank, world, local):
         elif tq5:
             xq, s = XQrot[l][r]
             bl.bitlinear_forward_tq5(Wrot[l][r], gammas[l], xq, s, y=ys[l], stream=stream)
+        elif args.path == "lut":
+            xq, s = XQrot[l][r]
+            bl.bitlinear_forward_lut(Wrot[l][r], gammas[l], xq, s, y=ys[l], stream=stream)
         else:
             xq, s = XQrot[l][r]
             bl.bitlinear_forward_ws(Wrot[l][r], gammas[l], xq, s, y=ys[l], workspace=workspace, stream=stream)
@@ -548,6 +555,8 @@ def run_gpu(args, dist, rank, world, local):
     nodes = graph_kernel_nodes(g_full)
     if tq5:  # quantise + base-3 forward, one pass per 4 tokens
         rule = sum(1 + -(-L.M // 4) for L in wl.layers)
+    elif args.path == "lut":  # quantise + table-lookup GEMV
+        rule = 2 * len(wl.layers)
     else:  # fused GEMV 1; quantise + GEMV 2; quantise (writing the fp16 operand) + GEMM 2
         rule = sum((1 if fused else 2) if gemv_fused_layer(L) else (2 if fused else 3) for L in wl.layers)
     launches_per_step = nodes / chunk if nodes is not None else rule
@@ -613,8 +622,11 @@ def run_gpu(args, dist, rank, world, local):
     per_layer = []
     for l, L in enumerate(wl.layers):
         e = layer_roofline(L, kern_us[l], fused, args.format, peaks, peak_src)
-        e["kernel"] = "gemv_tq5_kernel" if tq5 else gemm_variant(L, props.multi_processor_count)
-        if fused and gemv_fused_layer(L) and not tq5:
+        e["kernel"] = ("gemv_tq5_kernel" if tq5 else "gemv_lut_kernel" if args.path == "lut"
+                       else gemm_variant(L, props.multi_processor_count))
+        if args.path == "lut":
+            e["note"] = "bitlinear_forward_lut on quantised activations"
+        elif fused and gemv_fused_layer(L) and not tq5:
             e["note"] = "the timed kernel also quantises the activations (fused)"
         elif not gemv_fused_layer(L) and not tq5:
             e["note"] = "bitlinear_forward_ws on quantised activations: the fp16 expansion of x_q plus the GEMM"
@@ -857,8 +869,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--path", default="fused", choices=["fused", "separate"],
-                    help="fused: bitlinear_quant_forward; separate: bitlinear_quant_act + bitlinear_forward")
+    ap.add_argument("--path", default="fused", choices=["fused", "separate", "lut"],
+                    help="fused: bitlinear_quant_forward; separate: bitlinear_quant_act + bitlinear_forward; "
+                         "lut: bitlinear_quant_act + bitlinear_forward_lut")
     ap.add_argument("--format", default="2bit", choices=["2bit", "tq5"],
                     help="weight format: 2-bit (four per byte) or base-3 (five per byte, the forward on x_q)")
     ap.add_argument("--eager", action="store_true",
