@@ -354,9 +354,9 @@ def gemm_variant(L, num_sms: int) -> str:
     ntiles_m = -(-L.M // 256)
     bn = -(-(-(-L.M // ntiles_m)) // 16) * 16
     tiles = -(-L.N // 128) * ntiles_m
-    if tiles > num_sms and bn >= 128:
+    if tiles >= 2 * num_sms and bn >= 128:
         return "gemm_tc_x16_persistent_kernel"
-    return "gemm_tc_x16_kernel" + (" (split K over a cluster)" if tiles < num_sms else "")
+    return "gemm_f16_sk_kernel"
 
 
 def gemv_fused_layer(L) -> bool:

@@ -178,14 +178,12 @@ bl_status bitlinear_quant_forward(const uint8_t* W_packed, const float* gamma, c
 size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   if (M < 1 || K < 1) return 0;
   if (M <= bl::kGemvMaxTokens && K <= bl::kGemvMaxK) return 0;  // the GEMV needs none
-  if (bl::gemm_f8_serves(M, N, K)) {
-    // the fp8 GEMM keeps partial-sum slots per CTA (one CTA per SM); without a
-    // usable device the bound assumes 256 SMs
-    DeviceInfo d;
-    const int sms = device_info(&d) == BL_OK ? d.num_sms : 256;
-    return bl::gemm_f8_workspace_bytes(M, K, sms);
-  }
-  return bl::gemm_x16_workspace_bytes(M, K);
+  // both tensor-core GEMMs keep partial-sum slots per CTA (one CTA per SM);
+  // without a usable device the bound assumes 256 SMs
+  DeviceInfo d;
+  const int sms = device_info(&d) == BL_OK ? d.num_sms : 256;
+  if (bl::gemm_f8_serves(M, N, K)) return bl::gemm_f8_workspace_bytes(M, K, sms);
+  return bl::gemm_sk_workspace_bytes(M, K, sms);
 }
 
 namespace {
@@ -219,8 +217,10 @@ bl_status bitlinear_forward_ws(const uint8_t* W_packed, const float* gamma, cons
     if (cudaError_t e = bl::launch_x8_prepass(x_q, M, K, workspace, d.num_sms, stream)) return from_cuda(e);
     return from_cuda(bl::launch_gemm_f8(a, workspace, d.num_sms, stream));
   }
-  if (cudaError_t e = bl::launch_x16_prepass(x_q, M, K, workspace, d.num_sms, stream)) return from_cuda(e);
-  return from_cuda(bl::launch_gemm_tc_x16(a, workspace, d.num_sms, stream));
+  if (cudaError_t e = bl::launch_x16_sk_prepass(x_q, M, K, workspace, d.num_sms, stream)) return from_cuda(e);
+  if (bl::gemm_x16_persistent_serves(M, N, d.num_sms))
+    return from_cuda(bl::launch_gemm_tc_x16(a, workspace, d.num_sms, stream));
+  return from_cuda(bl::launch_gemm_f16_sk(a, workspace, d.num_sms, stream));
 }
 
 bl_status bitlinear_quant_forward_ws(const uint8_t* W_packed, const float* gamma, const void* X, bl_dtype dtype,
@@ -248,9 +248,12 @@ bl_status bitlinear_quant_forward_ws(const uint8_t* W_packed, const float* gamma
       return from_cuda(e);
     return from_cuda(bl::launch_gemm_f8(a, workspace, d.num_sms, stream));
   }
-  if (cudaError_t e = bl::launch_quant_act_x16(X, dtype == BL_BF16, M, K, x_q, s, workspace, stream))
+  if (cudaError_t e = bl::launch_quant_act_x16(X, dtype == BL_BF16, M, K, x_q, s, workspace,
+                                               bl::sk_counters(workspace, M, K, d.num_sms), d.num_sms, stream))
     return from_cuda(e);
-  return from_cuda(bl::launch_gemm_tc_x16(a, workspace, d.num_sms, stream));
+  if (bl::gemm_x16_persistent_serves(M, N, d.num_sms))
+    return from_cuda(bl::launch_gemm_tc_x16(a, workspace, d.num_sms, stream));
+  return from_cuda(bl::launch_gemm_f16_sk(a, workspace, d.num_sms, stream));
 }
 
 bl_status bitlinear_check_device_error(cudaStream_t stream) {

@@ -139,6 +139,19 @@ __device__ __forceinline__ uint32_t h2_sub(uint32_t a, uint32_t b) {
   return r;
 }
 
+// 16 ternary codes (one packed word, k = 0..15 at bits 2k) -> 16 fp16 of
+// code - 1 as 8 pairs, positions p = 4 i + j holding k = 4 j + i: byte j of
+// (P >> 2i) & 0x03030303 is the code of k = 4 j + i.
+__device__ __forceinline__ void unpack16_f16(uint32_t P, uint32_t* h /* 8 words */) {
+  const uint32_t k1025 = 0x64016401u;  // fp16 (1025, 1025): 1024 + code - 1025 = code - 1
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t S = (P >> (2 * i)) & 0x03030303u;
+    h[2 * i] = h2_sub(bytes_to_h2(S, 0x4140), k1025);
+    h[2 * i + 1] = h2_sub(bytes_to_h2(S, 0x4342), k1025);
+  }
+}
+
 // 16 int8 activations (natural order, 4 words) -> 16 fp16 in order p = 4i + j.
 __device__ __forceinline__ void convert_x16_f16(uint4 v, uint32_t* h /* 8 words */) {
   const uint32_t x0 = v.x ^ 0x80808080u, x1 = v.y ^ 0x80808080u, x2 = v.z ^ 0x80808080u, x3 = v.w ^ 0x80808080u;

@@ -89,31 +89,6 @@ __device__ __forceinline__ void mma_f8_tmem_a(uint32_t d_tmem, uint32_t a_tmem, 
       : "memory");
 }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
-      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
-      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
-      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
 // 16 codes (one packed word, k = 0..15 at bits 2k) -> 16 e4m3 bytes of
 // code - 1 in the order [0, 2, ..., 14, 1, 3, ..., 15]: the low three bits of
 // each selector nibble index the table bytes (the top bit, sign replication,
@@ -200,9 +175,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f8_kernel(const __grid_const
   const uint32_t tmem = *tmem_slot;
 
   if (warp == kWProdWarp || warp == kXProdWarp) {
-    // ---------------- producers: the packed weights (2-D TMA boxes of 128 rows
-    // x 128 B) and the activation blocks (one 1-D bulk copy each)
-    if (lane == 0) {
+    // ---------------- producers (whole warps, one lane issues): the packed
+    // weights (2-D TMA boxes of 128 rows x 128 B) and the activation blocks
+    // (one 1-D bulk copy each)
+    {
       const bool wprod = warp == kWProdWarp;
       if (!wprod) pdl_wait();  // the activation operand comes from the preceding kernel
       const int NS = wprod ? NW : NX;
@@ -215,19 +191,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f8_kernel(const __grid_const
         const int64_t t = i / c.nkb;
         const int kb = (int)(i - t * c.nkb);
         for (int sub = 0; sub < (wprod ? 1 : kKB / kSub); ++sub) {
-          if (!wait_flag(&empty[st], ph ^ 1u, c.err, abort_flag)) {
+          if (!wait_warp(&empty[st], ph ^ 1u, c.err, abort_flag)) {
             ok = false;
             break;
           }
-          if (wprod) {
-            mbar_arrive_expect_tx(&full[st], (uint32_t)kWStage);
-            tma_load_2d(wring + st * kWStage, &tmap_w, kb * (kKB / 4), (int)(t % c.ntn) * kBM, &full[st]);
-          } else {
-            const int64_t mt = t / c.ntn;
-            mbar_arrive_expect_tx(&full[st], (uint32_t)x_bytes);
-            bulk_g2s(xring + st * x_bytes, c.x8 + ((size_t)mt * c.nkb + kb) * (size_t)b_bytes + (size_t)sub * x_bytes,
-                     (uint32_t)x_bytes, &full[st]);
+          if (elect_one()) {
+            if (wprod) {
+              mbar_arrive_expect_tx(&full[st], (uint32_t)kWStage);
+              tma_load_2d(wring + st * kWStage, &tmap_w, kb * (kKB / 4), (int)(t % c.ntn) * kBM, &full[st]);
+            } else {
+              const int64_t mt = t / c.ntn;
+              mbar_arrive_expect_tx(&full[st], (uint32_t)x_bytes);
+              bulk_g2s(xring + st * x_bytes,
+                       c.x8 + ((size_t)mt * c.nkb + kb) * (size_t)b_bytes + (size_t)sub * x_bytes, (uint32_t)x_bytes,
+                       &full[st]);
+            }
           }
+          __syncwarp();
           ++issued;
           if (++st == NS) {
             st = 0;
@@ -235,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f8_kernel(const __grid_const
           }
         }
       }
-      if (*abort_flag) {
+      if (*abort_flag && lane == 0) {
         // let every copy this CTA started land before its shared memory goes away
         for (int g = (issued > NS ? issued - NS : 0); g < issued; ++g) {
           const uint32_t a = smem_u32(&full[g % NS]), par = (uint32_t)(g / NS) & 1u;
@@ -246,12 +226,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f8_kernel(const __grid_const
       }
     }
   } else if (warp == kMma0Warp || warp == kMma1Warp) {
-    // ---------------- MMA issuers: issuer q takes the slots (2 k-block + sub) with
-    // sub % NI == q, into its own accumulator; the epilogue adds the issuers' sums.
-    // The issuing thread's own instructions add to every MMA's issue time, so
-    // descriptors are formed once per stage and the eight MMAs of a slot are unrolled.
+    // ---------------- MMA issuers (whole warps, one lane issues): issuer q takes
+    // the slots (2 k-block + sub) with sub % NI == q, into its own accumulator;
+    // the epilogue adds the issuers' sums.  The eight MMAs of a slot are unrolled.
     const int q = warp == kMma0Warp ? 0 : 1;
-    if (lane == 0 && q < NI) {
+    if (q < NI) {
       const uint32_t idesc = f16_idesc(kBM, NB);  // format fields 0: E4M3 operands under kind::f8f6f4
       const uint64_t box_step = (uint64_t)(b_box >> 4);  // one activation box in the descriptor's address field
       int lt = 0;
@@ -262,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f8_kernel(const __grid_const
         const int kb0 = (int)(i - t * c.nkb);
         const int kb1 = (int)min((int64_t)c.nkb, kb0 + (end - i));
         const int b = lt & 1;
-        if (!wait_flag(&acc_empty[b], ((uint32_t)(lt >> 1) & 1u) ^ 1u, c.err, abort_flag)) break;
+        if (!wait_warp(&acc_empty[b], ((uint32_t)(lt >> 1) & 1u) ^ 1u, c.err, abort_flag)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)((b * NI + q) * NB);
         uint32_t accum = 0u;  // the segment's first MMA overwrites the accumulator
@@ -270,37 +249,44 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f8_kernel(const __grid_const
           for (int sub = q; sub < kKB / kSub; sub += NI) {
             const int g = gsub + sub;
             const int as = g % NA, xs = g % NX;
-            if (!wait_flag(&x_full[xs], (uint32_t)(g / NX) & 1u, c.err, abort_flag) ||
-                !wait_flag(&a_full[as], (uint32_t)(g / NA) & 1u, c.err, abort_flag)) {
+            if (!wait_warp(&x_full[xs], (uint32_t)(g / NX) & 1u, c.err, abort_flag) ||
+                !wait_warp(&a_full[as], (uint32_t)(g / NA) & 1u, c.err, abort_flag)) {
               ok = false;
               break;
             }
             tc_fence_after();
             const uint32_t a_col = tmem + (uint32_t)(c.acol + as * kACols);
             const uint64_t bs = sw128_desc(smem_u32(xring + xs * x_bytes));  // boxes 0, 1 of the stage
-            // K = 32 per MMA: +32 bytes (+2 in the address field) within a box
-            mma_f8_tmem_a(d, a_col + 0, bs + 0, idesc, accum);
-            mma_f8_tmem_a(d, a_col + 8, bs + 2, idesc, 1u);
-            mma_f8_tmem_a(d, a_col + 16, bs + 4, idesc, 1u);
-            mma_f8_tmem_a(d, a_col + 24, bs + 6, idesc, 1u);
-            mma_f8_tmem_a(d, a_col + 32, bs + box_step + 0, idesc, 1u);
-            mma_f8_tmem_a(d, a_col + 40, bs + box_step + 2, idesc, 1u);
-            mma_f8_tmem_a(d, a_col + 48, bs + box_step + 4, idesc, 1u);
-            mma_f8_tmem_a(d, a_col + 56, bs + box_step + 6, idesc, 1u);
+            if (elect_one()) {
+              // K = 32 per MMA: +32 bytes (+2 in the address field) within a box
+              mma_f8_tmem_a(d, a_col + 0, bs + 0, idesc, accum);
+              mma_f8_tmem_a(d, a_col + 8, bs + 2, idesc, 1u);
+              mma_f8_tmem_a(d, a_col + 16, bs + 4, idesc, 1u);
+              mma_f8_tmem_a(d, a_col + 24, bs + 6, idesc, 1u);
+              mma_f8_tmem_a(d, a_col + 32, bs + box_step + 0, idesc, 1u);
+              mma_f8_tmem_a(d, a_col + 40, bs + box_step + 2, idesc, 1u);
+              mma_f8_tmem_a(d, a_col + 48, bs + box_step + 4, idesc, 1u);
+              mma_f8_tmem_a(d, a_col + 56, bs + box_step + 6, idesc, 1u);
+              mma_commit(&a_empty[as]);
+              mma_commit(&x_empty[xs]);
+            }
+            __syncwarp();
             accum = 1u;
-            mma_commit(&a_empty[as]);
-            mma_commit(&x_empty[xs]);
           }
         }
-        if (ok) mma_commit(&acc_full[b]);
+        if (ok && elect_one()) mma_commit(&acc_full[b]);
+        __syncwarp();
         i += kb1 - kb0;
       }
-      // every MMA this thread issued has finished before tensor memory is freed
-      mma_commit(&drain[q]);
-      const uint32_t a = smem_u32(&drain[q]);
-      const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait_sleep(a, 0u, kWaitHintNs) && globaltimer_ns() - t0 < kWaitLimitNs) {
+      // every MMA the issuing lane issued has finished before tensor memory is freed
+      if (elect_one()) {
+        mma_commit(&drain[q]);
+        const uint32_t a = smem_u32(&drain[q]);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait_sleep(a, 0u, kWaitHintNs) && globaltimer_ns() - t0 < kWaitLimitNs) {
+        }
       }
+      __syncwarp();
     }
   } else if (warp < kEpiWarp0) {
     // ---------------- weight expansion: thread = weight row r of the tile; the two

@@ -30,7 +30,6 @@
 
 #include <cstdint>
 #include <cstring>
-#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -58,21 +57,9 @@ struct GemmCfg {
   int M, N, K, BN;
   int relu2;    // epilogue applies the squared ReLU
   int nstages;  // ring depth (the GEMM on pre-expanded activations)
-  int ksplit;   // CTAs of a cluster that split K (1 = no split)
 };
 
 // ---------------------------------------------------------------- operand expansion
-
-// 16 codes (one 32-bit packed word) -> 16 fp16 in order p = 4i + j (k = 4j + i), values c - 1.
-__device__ __forceinline__ void unpack_word_f16(uint32_t P, uint32_t* h /* 8 words */) {
-  const uint32_t k1025 = 0x64016401u;  // fp16 (1025, 1025)
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t S = (P >> (2 * i)) & 0x03030303u;
-    h[2 * i] = h2_sub(bytes_to_h2(S, 0x4140), k1025);
-    h[2 * i + 1] = h2_sub(bytes_to_h2(S, 0x4342), k1025);
-  }
-}
 
 // Store 16-byte unit u (0..7) of row r of a 128-byte-swizzled K-major tile at shared address `tile`.
 __device__ __forceinline__ void st_sw128(uint32_t tile, int r, int u, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -153,19 +140,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ---------------- TMA producer
-    if (lane == 0) {
+    // ---------------- TMA producer (the whole warp, one lane issues)
+    {
       int issued = 0;
       for (int kb = 0; kb < nkb; ++kb) {
         const int slot = kb % kRawStages;
-        if (!wait_flag(&raw_empty[slot], ((uint32_t)(kb / kRawStages) & 1u) ^ 1u, c.err, abort_flag)) break;
+        if (!wait_warp(&raw_empty[slot], ((uint32_t)(kb / kRawStages) & 1u) ^ 1u, c.err, abort_flag)) break;
         uint8_t* wdst = raw_base + slot * (kWRawBytes + x_raw_bytes);
-        mbar_arrive_expect_tx(&raw_full[slot], (uint32_t)(kWRawBytes + x_raw_bytes));
-        tma_load_2d(wdst, &tmap_w, kb * (kBK / 4), n0, &raw_full[slot]);
-        tma_load_2d(wdst + kWRawBytes, &tmap_x, kb * kBK, m0, &raw_full[slot]);
+        if (elect_one()) {
+          mbar_arrive_expect_tx(&raw_full[slot], (uint32_t)(kWRawBytes + x_raw_bytes));
+          tma_load_2d(wdst, &tmap_w, kb * (kBK / 4), n0, &raw_full[slot]);
+          tma_load_2d(wdst + kWRawBytes, &tmap_x, kb * kBK, m0, &raw_full[slot]);
+        }
+        __syncwarp();
         issued = kb + 1;
       }
-      if (*abort_flag) {
+      if (*abort_flag && lane == 0) {
         for (int kb = (issued > kRawStages ? issued - kRawStages : 0); kb < issued; ++kb) {
           const uint32_t a = smem_u32(&raw_full[kb % kRawStages]), par = (uint32_t)(kb / kRawStages) & 1u;
           const uint64_t t0 = globaltimer_ns();
@@ -175,21 +165,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer
-    if (lane == 0) {
+    // ---------------- MMA issuer (the whole warp, one lane issues)
+    {
       const uint32_t idesc = f16_idesc(kBM, BN);
       for (int kb = 0; kb < nkb; ++kb) {
         const int os = kb % kOpStages;
-        if (!wait_flag(&op_full[os], (uint32_t)(kb / kOpStages) & 1u, c.err, abort_flag)) break;
+        if (!wait_warp(&op_full[os], (uint32_t)(kb / kOpStages) & 1u, c.err, abort_flag)) break;
         tc_fence_after();
         const uint32_t a_base = smem_u32(op_base + os * (kAOpBytes + b_op_bytes));
         const uint32_t b_base = a_base + kAOpBytes;
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk)
-          mma_f16(tmem, sw128_desc(a_base + kk * 32), sw128_desc(b_base + kk * 32), idesc, (kb | kk) ? 1u : 0u);
-        mma_commit(&op_empty[os]);
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            mma_f16(tmem, sw128_desc(a_base + kk * 32), sw128_desc(b_base + kk * 32), idesc, (kb | kk) ? 1u : 0u);
+          mma_commit(&op_empty[os]);
+        }
+        __syncwarp();
       }
-      mma_commit(acc_full);  // fires once every MMA issued above has completed
+      if (elect_one()) mma_commit(acc_full);  // fires once every MMA issued above has completed
+      __syncwarp();
     }
   } else {
     // ---------------- converters, then epilogue
@@ -216,10 +210,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = ct >> 1, h = ct & 1;
         const uint2 pw = lds64(wraw + (uint32_t)(r * 16 + h * 8));
         uint32_t f[8];
-        unpack_word_f16(pw.x, f);
+        unpack16_f16(pw.x, f);
         st_sw128(aop, r, 4 * h + 0, f[0], f[1], f[2], f[3]);
         st_sw128(aop, r, 4 * h + 1, f[4], f[5], f[6], f[7]);
-        unpack_word_f16(pw.y, f);
+        unpack16_f16(pw.y, f);
         st_sw128(aop, r, 4 * h + 2, f[0], f[1], f[2], f[3]);
         st_sw128(aop, r, 4 * h + 3, f[4], f[5], f[6], f[7]);
       }
@@ -262,269 +256,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- activations expanded once per call
 //
-// With a workspace, the int8 activations are expanded to fp16 ONCE per call,
-// in the operand order above (p = 4i + j within every 16 k), instead of once
-// per 128-feature tile inside the GEMM: every tile of a prefill-sized problem
-// would otherwise repeat the same conversion N/128 times.  The GEMM then loads
-// the fp16 operand straight into its 128-byte-swizzled layout with a TMA copy.
-
-__global__ void __launch_bounds__(256) x16_prepass_kernel(const uint4* __restrict__ xq, uint64_t ngroups,
-                                                          uint4* __restrict__ x16) {
-  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
-  for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < ngroups; i += stride) {
-    uint32_t f[8];
-    convert_x16_f16(__ldg(xq + i), f);
-    x16[2 * i] = make_uint4(f[0], f[1], f[2], f[3]);
-    x16[2 * i + 1] = make_uint4(f[4], f[5], f[6], f[7]);
-  }
-}
+// With a workspace, the int8 activations are expanded to fp16 ONCE per call
+// (by the quantisation kernel or the x_q prepass of the stream-K GEMM), in the
+// operand order above (p = 4i + j within every 16 k), instead of once per
+// 128-feature tile inside the GEMM; the GEMM loads the fp16 operand straight
+// into its 128-byte-swizzled layout with a TMA copy.
 
 constexpr int kX16MaxStages = 12;
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// All threads of every CTA of the cluster; release/acquire orders the shared
-// memory written before it against the peers' reads after it.
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
-}
-
-__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void sts_f32(uint32_t addr, float v) {
-  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
-// The GEMM on pre-expanded activations.  Stage s of the ring holds
-// [A op 16 KB | B op BN*128 | packed W 2 KB]; the producer fills B (fp16 x,
-// swizzled by TMA) and the packed W tile, the converter warps expand W into A,
-// and one thread issues the MMAs.  Barriers per stage: tma_full (TMA bytes),
-// op_full (eight converter warps), op_empty (MMA commit).  The ring depth
-// c.nstages is chosen on the host from the shared memory a stage needs.
-//
-// Split K (c.ksplit = S > 1): the S CTAs of a thread-block cluster share one
-// output tile and take consecutive ranges of k-blocks.  Each stores its partial
-// accumulator in its own (by then idle) ring memory as R[token][feature]; after
-// a cluster barrier, rank r reduces the 16-token column chunks c with
-// c % S == r by reading the S partials (its own and its peers', over
-// distributed shared memory) in rank order and writes y.  Every partial is an
-// integer of magnitude < 2^24, so the fp32 sums are exact in any order.
-__global__ void __launch_bounds__(kThreads, 1)
-    gemm_tc_x16_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x16,
-                       const GemmCfg c) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int BN = c.BN;
-  const int NS = c.nstages;
-  const int S = c.ksplit;
-  const int b_bytes = BN * kARowBytes;
-  const int stage_bytes = kAOpBytes + b_bytes + kWRawBytes;  // a multiple of 1024
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NS * stage_bytes);
-  uint64_t* tma_full = bars;
-  uint64_t* op_full = tma_full + kX16MaxStages;
-  uint64_t* op_empty = op_full + kX16MaxStages;
-  uint64_t* acc_full = op_empty + kX16MaxStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
-  volatile uint32_t* abort_flag = tmem_slot + 1;
-  float* tscale = reinterpret_cast<float*>(tmem_slot + 4);  // [BN]
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * kBM;
-  const int m0 = blockIdx.y * BN;
-  const int nkb_all = c.K / kBK;
-  const int z = (int)blockIdx.z;  // = rank in the cluster (cluster dims 1 x 1 x S)
-  const int kb0 = (int)((int64_t)z * nkb_all / S), kb1 = (int)((int64_t)(z + 1) * nkb_all / S);
-  const int nkb = kb1 - kb0;
-  const uint32_t tmem_cols = BN <= 32 ? 32u : BN <= 64 ? 64u : BN <= 128 ? 128u : 256u;
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(&tma_full[i], 1);
-      mbar_init(&op_full[i], kConvWarps);
-      mbar_init(&op_empty[i], 1);
-    }
-    mbar_init(acc_full, 1);
-    *abort_flag = 0u;
-    fence_mbarrier_init();
-  }
-  if (warp == 1) tmem_alloc(tmem_slot, tmem_cols);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp == 0) {
-    // ---------------- TMA producer
-    if (lane == 0) {
-      pdl_wait();  // the activations may come from the preceding kernel
-      int issued = 0, os = 0;
-      uint32_t ph = 0;  // ring slot and phase parity, advanced without divisions
-      for (int i = 0; i < nkb; ++i) {
-        if (!wait_flag(&op_empty[os], ph ^ 1u, c.err, abort_flag)) break;
-        uint8_t* st = smem + os * stage_bytes;
-        const int kb = kb0 + i;
-        mbar_arrive_expect_tx(&tma_full[os], (uint32_t)(b_bytes + kWRawBytes));
-        tma_load_2d(st + kAOpBytes + b_bytes, &tmap_w, kb * (kBK / 4), n0, &tma_full[os]);
-        tma_load_2d(st + kAOpBytes, &tmap_x16, kb * kBK, m0, &tma_full[os]);
-        issued = i + 1;
-        if (++os == NS) {
-          os = 0;
-          ph ^= 1u;
-        }
-      }
-      if (*abort_flag) {
-        for (int i = (issued > NS ? issued - NS : 0); i < issued; ++i) {
-          const uint32_t a = smem_u32(&tma_full[i % NS]), par = (uint32_t)(i / NS) & 1u;
-          const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait_sleep(a, par, kWaitHintNs) && globaltimer_ns() - t0 < kWaitLimitNs) {
-          }
-        }
-      }
-    }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = f16_idesc(kBM, BN);
-      int os = 0;
-      uint32_t par = 0;
-      for (int i = 0; i < nkb; ++i) {
-        if (!wait_flag(&op_full[os], par, c.err, abort_flag) || !wait_flag(&tma_full[os], par, c.err, abort_flag))
-          break;
-        tc_fence_after();
-        const uint32_t a_base = smem_u32(smem + os * stage_bytes);
-        const uint32_t b_base = a_base + kAOpBytes;
-#pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk)
-          mma_f16(tmem, sw128_desc(a_base + kk * 32), sw128_desc(b_base + kk * 32), idesc, (i | kk) ? 1u : 0u);
-        mma_commit(&op_empty[os]);
-        if (++os == NS) {
-          os = 0;
-          par ^= 1u;
-        }
-      }
-      mma_commit(acc_full);
-    }
-  } else {
-    // ---------------- W converters
-    const int ct = threadIdx.x - 64;  // 0 .. 255
-    pdl_wait();
-    const float gamma = __ldg(c.gamma);
-    for (int j = ct; j < BN; j += 32 * kConvWarps) {
-      const int m = m0 + j;
-      tscale[j] = m < c.M ? __fdiv_rn(gamma, __ldg(c.s + m)) : 0.0f;
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(32 * kConvWarps) : "memory");
-    int os = 0;
-    uint32_t par = 0;
-    for (int i = 0; i < nkb; ++i) {
-      if (!wait_flag(&tma_full[os], par, c.err, abort_flag)) break;
-      const uint32_t aop = smem_u32(smem + os * stage_bytes);
-      const uint32_t wraw = aop + kAOpBytes + b_bytes;
-      const int r = ct >> 1, h = ct & 1;
-      const uint2 pw = lds64(wraw + (uint32_t)(r * 16 + h * 8));
-      uint32_t f[8];
-      unpack_word_f16(pw.x, f);
-      st_sw128(aop, r, 4 * h + 0, f[0], f[1], f[2], f[3]);
-      st_sw128(aop, r, 4 * h + 1, f[4], f[5], f[6], f[7]);
-      unpack_word_f16(pw.y, f);
-      st_sw128(aop, r, 4 * h + 2, f[0], f[1], f[2], f[3]);
-      st_sw128(aop, r, 4 * h + 3, f[4], f[5], f[6], f[7]);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&op_full[os]);
-      if (++os == NS) {
-        os = 0;
-        par ^= 1u;
-      }
-    }
-  }
-
-  // ---------------- epilogue (converter warps 2..9)
-  const bool epi = warp >= 2;
-  bool done = false;
-  if (epi) {
-    done = wait_flag(acc_full, 0u, c.err, abort_flag);
-    tc_fence_after();
-  }
-  if (S == 1) {
-    if (epi && done) epilogue_store(c, tmem, tscale, warp, lane, n0, m0);
-  } else {
-    // partial accumulator -> R[token][feature] in this CTA's ring memory
-    const uint32_t R = smem_u32(smem);
-    const int q = warp & 3, f = q * 32 + lane;
-    if (epi && done) {
-      for (int j0 = ((warp - 2) >> 2) * 16; j0 < BN; j0 += 32) {
-        uint32_t r[16];
-        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)j0, r);
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) sts_f32(R + (uint32_t)(((j0 + jj) * kBM + f) * 4), __uint_as_float(r[jj]));
-      }
-    }
-    __syncwarp();
-    cluster_sync_all();
-    if (epi) {
-      // Units of work: (16-token chunk, lane quarter) pairs, dealt round-robin to
-      // the S ranks; the two warps of a quarter take 8 tokens each, and a
-      // thread's 8 reads from one peer are issued together.
-      const int rank = (int)cluster_ctarank();
-      const int h = (warp - 2) >> 2;
-      const int npairs = (BN / 16) * 4;
-      for (int pair = rank; pair < npairs; pair += S) {
-        if ((pair & 3) != q) continue;
-        const int j0 = (pair >> 2) * 16 + 8 * h;
-        const int n = n0 + f;
-        float v[8];
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) v[jj] = 0.0f;
-        for (int pr = 0; pr < S; ++pr) {
-          const uint32_t base = map_to_rank(R + (uint32_t)((j0 * kBM + f) * 4), (uint32_t)pr);
-          float w[8];
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj) w[jj] = ld_cluster_f32(base + (uint32_t)(jj * kBM * 4));
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj) v[jj] += w[jj];
-        }
-        if (n < c.N) {
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            const int m = m0 + j0 + jj;
-            if (m < c.M) {
-              const int64_t o = (int64_t)m * c.N + n;
-              c.y[o] = out_act(__fmul_rn(v[jj], tscale[j0 + jj]), c.relu2);
-              if (c.acc) c.acc[o] = __float2int_rn(v[jj]);
-            }
-          }
-        }
-      }
-    }
-    __syncwarp();
-    cluster_sync_all();  // peers keep their shared memory until every read is done
-  }
-  if (epi) tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    const uint32_t a = smem_u32(acc_full);
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait_sleep(a, 0u, kWaitHintNs) && globaltimer_ns() - t0 < kWaitLimitNs) {
-    }
-    tc_fence_after();
-    tmem_dealloc(tmem, tmem_cols);
-  }
-}
 
 // ---------------------------------------------------------------- persistent variant for large grids
 //
@@ -586,8 +324,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ---------------- TMA producer
-    if (lane == 0) {
+    // ---------------- TMA producer (the whole warp, one lane issues)
+    {
       pdl_wait();
       int os = 0, issued = 0;
       uint32_t ph = 0;
@@ -595,14 +333,17 @@ __global__ void __launch_bounds__(kPThreads, 1)
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
         const int n0 = (t % ntn) * kBM, m0 = (t / ntn) * BN;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!wait_flag(&op_empty[os], ph ^ 1u, c.err, abort_flag)) {
+          if (!wait_warp(&op_empty[os], ph ^ 1u, c.err, abort_flag)) {
             ok = false;
             break;
           }
           uint8_t* st = smem + os * stage_bytes;
-          mbar_arrive_expect_tx(&tma_full[os], (uint32_t)(b_bytes + kWRawBytes));
-          tma_load_2d(st + kAOpBytes + b_bytes, &tmap_w, kb * (kBK / 4), n0, &tma_full[os]);
-          tma_load_2d(st + kAOpBytes, &tmap_x16, kb * kBK, m0, &tma_full[os]);
+          if (elect_one()) {
+            mbar_arrive_expect_tx(&tma_full[os], (uint32_t)(b_bytes + kWRawBytes));
+            tma_load_2d(st + kAOpBytes + b_bytes, &tmap_w, kb * (kBK / 4), n0, &tma_full[os]);
+            tma_load_2d(st + kAOpBytes, &tmap_x16, kb * kBK, m0, &tma_full[os]);
+          }
+          __syncwarp();
           ++issued;
           if (++os == NS) {
             os = 0;
@@ -610,7 +351,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           }
         }
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         for (int g = (issued > NS ? issued - NS : 0); g < issued; ++g) {
           const uint32_t a = smem_u32(&tma_full[g % NS]), par = (uint32_t)(g / NS) & 1u;
           const uint64_t t0 = globaltimer_ns();
@@ -620,35 +361,39 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer
-    if (lane == 0) {
+    // ---------------- MMA issuer (the whole warp, one lane issues)
+    {
       const uint32_t idesc = f16_idesc(kBM, BN);
       int os = 0, lt = 0;
       uint32_t par = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++lt) {
         const int b = lt & 1;
-        if (!wait_flag(&acc_empty[b], ((uint32_t)(lt >> 1) & 1u) ^ 1u, c.err, abort_flag)) break;
+        if (!wait_warp(&acc_empty[b], ((uint32_t)(lt >> 1) & 1u) ^ 1u, c.err, abort_flag)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(b * 256);
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!wait_flag(&op_full[os], par, c.err, abort_flag) || !wait_flag(&tma_full[os], par, c.err, abort_flag)) {
+          if (!wait_warp(&op_full[os], par, c.err, abort_flag) || !wait_warp(&tma_full[os], par, c.err, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t a_base = smem_u32(smem + os * stage_bytes);
           const uint32_t b_base = a_base + kAOpBytes;
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            mma_f16(d, sw128_desc(a_base + kk * 32), sw128_desc(b_base + kk * 32), idesc, (kb | kk) ? 1u : 0u);
-          mma_commit(&op_empty[os]);
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              mma_f16(d, sw128_desc(a_base + kk * 32), sw128_desc(b_base + kk * 32), idesc, (kb | kk) ? 1u : 0u);
+            mma_commit(&op_empty[os]);
+          }
+          __syncwarp();
           if (++os == NS) {
             os = 0;
             par ^= 1u;
           }
         }
-        if (ok) mma_commit(&acc_full[b]);
+        if (ok && elect_one()) mma_commit(&acc_full[b]);
+        __syncwarp();
       }
     }
   } else if (warp < 2 + kConvWarps) {
@@ -667,10 +412,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const uint32_t aop = smem_u32(smem + os * stage_bytes);
         const uint2 pw = lds64(aop + kAOpBytes + b_bytes + (uint32_t)(r * 16 + h * 8));
         uint32_t f[8];
-        unpack_word_f16(pw.x, f);
+        unpack16_f16(pw.x, f);
         st_sw128(aop, r, 4 * h + 0, f[0], f[1], f[2], f[3]);
         st_sw128(aop, r, 4 * h + 1, f[4], f[5], f[6], f[7]);
-        unpack_word_f16(pw.y, f);
+        unpack16_f16(pw.y, f);
         st_sw128(aop, r, 4 * h + 2, f[0], f[1], f[2], f[3]);
         st_sw128(aop, r, 4 * h + 3, f[4], f[5], f[6], f[7]);
         fence_proxy_async_smem();
@@ -726,7 +471,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   __syncthreads();
   if (warp == 1) {
     // every MMA this thread issued has finished before tensor memory is freed
-    if (lane == 0) mma_commit(drain);
+    if (elect_one()) mma_commit(drain);  // the issuing lane: its MMAs are the ones tracked
     __syncwarp();
     const uint32_t a = smem_u32(drain);
     const uint64_t t0 = globaltimer_ns();
@@ -748,128 +493,41 @@ int token_tile(int64_t M, int64_t* ntiles) {
 
 }  // namespace
 
-size_t gemm_x16_workspace_bytes(int64_t M, int64_t K) { return (size_t)M * (size_t)K * 2; }
-
-cudaError_t launch_x16_prepass(const int8_t* xq, int64_t M, int64_t K, void* x16, int num_sms, cudaStream_t stream) {
-  const uint64_t ngroups = (uint64_t)M * (uint64_t)K / 16;
-  const uint64_t want = (ngroups + 255) / 256;
-  const int grid = (int)(want < (uint64_t)num_sms * 8 ? (want ? want : 1) : (uint64_t)num_sms * 8);
-  x16_prepass_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint4*>(xq), ngroups,
-                                               reinterpret_cast<uint4*>(x16));
-  return cudaGetLastError();
+bool gemm_x16_persistent_serves(int64_t M, int64_t N, int num_sms) {
+  int64_t ntiles = 0;
+  const int BN = token_tile(M, &ntiles);
+  const int64_t tiles = (N + kBM - 1) / kBM * ntiles;
+  return BN >= 128 && tiles >= 2 * (int64_t)num_sms;
 }
+
 
 namespace {
 
-constexpr size_t kMaxDynSmem = 227 * 1024;       // per CTA (opt-in limit)
-constexpr size_t kSmemPerSm = 228 * 1024;        // per SM
-constexpr size_t kSmemReservedPerCta = 1024;     // reserved by the system per resident CTA
-
-size_t x16_smem_bytes(int BN, int NS) {
-  return 1024 + (size_t)NS * (kAOpBytes + (size_t)BN * kARowBytes + kWRawBytes) + (3 * kX16MaxStages + 1) * 8 + 16 +
-         (size_t)BN * 4;
-}
-
-// Largest cluster size S <= 8 (and <= k-blocks / 4) for which every cluster of
-// the grid is resident at once, when the tile grid alone fills fewer than all
-// SMs; 1 otherwise.  Results are cached per (tiles, k-blocks, BN, stages).
-int choose_ksplit(int64_t tiles, int nkb, int BN, int NS, size_t smem, int num_sms) {
-  if (tiles >= num_sms) return 1;
-  struct Entry {
-    int64_t tiles;
-    int nkb, BN, NS, S;
-  };
-  static std::mutex mu;
-  static Entry cache[64];
-  static int ncache = 0;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    for (int i = 0; i < ncache; ++i)
-      if (cache[i].tiles == tiles && cache[i].nkb == nkb && cache[i].BN == BN && cache[i].NS == NS) return cache[i].S;
-  }
-  int best = 1;
-  for (int S = 8; S >= 2; --S) {
-    if (tiles * S > 2 * (int64_t)num_sms || nkb / S < 4) continue;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(1, 1, (unsigned)S);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = (unsigned)S;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int nclusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&nclusters, gemm_tc_x16_kernel, &cfg) != cudaSuccess) {
-      cudaGetLastError();
-      continue;
-    }
-    if (nclusters >= tiles) {
-      best = S;
-      break;
-    }
-  }
-  std::lock_guard<std::mutex> lock(mu);
-  if (ncache < 64) cache[ncache++] = Entry{tiles, nkb, BN, NS, best};
-  return best;
-}
+constexpr size_t kMaxDynSmem = 227 * 1024;  // per CTA (opt-in limit)
 
 }  // namespace
 
 cudaError_t launch_gemm_tc_x16(const ForwardArgs& a, const void* x16, int num_sms, cudaStream_t stream) {
   int64_t ntiles = 0;
   const int BN = token_tile(a.M, &ntiles);
+  const int64_t tiles = (a.N + kBM - 1) / kBM * ntiles;
+  if (tiles < num_sms || BN < 128) return cudaErrorInvalidValue;  // the stream-K GEMM serves these shapes
   CUtensorMap tw, tx;
   if (!encode_u8_2d(&tw, a.Wp, (uint64_t)a.K / 4, (uint64_t)a.N, kBK / 4, kBM, 0)) return cudaErrorInvalidValue;
   if (!encode_f16_2d_sw128(&tx, x16, (uint64_t)a.K, (uint64_t)a.M, (uint32_t)BN)) return cudaErrorInvalidValue;
-  const int64_t tiles = (a.N + kBM - 1) / kBM * ntiles;
-  if (tiles > num_sms && BN >= 128) {
-    // persistent: one CTA per SM, the deepest ring that fits beside [2][BN] scales
-    const size_t stage = kAOpBytes + (size_t)BN * kARowBytes + kWRawBytes;
-    const size_t fixed = 1024 + (3 * kX16MaxStages + 5) * 8 + 16 + (size_t)BN * 8;
-    int NS = (int)((kMaxDynSmem - fixed) / stage);
-    if (NS > kX16MaxStages) NS = kX16MaxStages;
-    const size_t smem = fixed + (size_t)NS * stage;
-    cudaError_t e =
-        cudaFuncSetAttribute(gemm_tc_x16_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    GemmCfg c{a.gamma, a.s, a.y, a.acc, a.err, (int)a.M, (int)a.N, (int)a.K, BN, a.relu2 ? 1 : 0, NS, 1};
-    const int grid = (int)(tiles < num_sms ? tiles : num_sms);
-    gemm_tc_x16_persistent_kernel<<<grid, kPThreads, smem, stream>>>(tw, tx, c);
-    return cudaGetLastError();
-  }
-  // Ring depth: two CTAs per SM when that still leaves >= 4 stages (small
-  // token tiles: the grid then fits in fewer waves), else one CTA with the
-  // deepest ring that fits.
+  // one CTA per SM, the deepest ring that fits beside [2][BN] scales
   const size_t stage = kAOpBytes + (size_t)BN * kARowBytes + kWRawBytes;
-  const size_t fixed = x16_smem_bytes(BN, 0);
-  int NS = (int)((kSmemPerSm / 2 - kSmemReservedPerCta - fixed) / stage);
-  if (NS < 4) NS = (int)((kMaxDynSmem - fixed) / stage);
+  const size_t fixed = 1024 + (3 * kX16MaxStages + 5) * 8 + 16 + (size_t)BN * 8;
+  int NS = (int)((kMaxDynSmem - fixed) / stage);
   if (NS > kX16MaxStages) NS = kX16MaxStages;
-  const size_t smem = x16_smem_bytes(BN, NS);
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_x16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t smem = fixed + (size_t)NS * stage;
+  cudaError_t e =
+      cudaFuncSetAttribute(gemm_tc_x16_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const int ntn = (int)((a.N + kBM - 1) / kBM);
-  const int nkb = (int)(a.K / kBK);
-  int S = choose_ksplit((int64_t)ntn * ntiles, nkb, BN, NS, smem, num_sms);
-  // the split partials live in the ring memory: 128 x BN fp32
-  if ((size_t)kBM * BN * 4 > (size_t)NS * stage) S = 1;
-  GemmCfg c{a.gamma, a.s, a.y, a.acc, a.err, (int)a.M, (int)a.N, (int)a.K, BN, a.relu2 ? 1 : 0, NS, S};
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)ntn, (unsigned)ntiles, (unsigned)S);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = (unsigned)S;
-  cfg.attrs = attr;
-  cfg.numAttrs = S > 1 ? 1 : 0;  // an unsplit grid is launched without clusters
-  return cudaLaunchKernelEx(&cfg, gemm_tc_x16_kernel, tw, tx, c);
+  GemmCfg c{a.gamma, a.s, a.y, a.acc, a.err, (int)a.M, (int)a.N, (int)a.K, BN, a.relu2 ? 1 : 0, NS};
+  const int grid = (int)(tiles < num_sms ? tiles : num_sms);
+  gemm_tc_x16_persistent_kernel<<<grid, kPThreads, smem, stream>>>(tw, tx, c);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_gemm_tc(const ForwardArgs& a, int num_sms, cudaStream_t stream) {
@@ -879,7 +537,7 @@ cudaError_t launch_gemm_tc(const ForwardArgs& a, int num_sms, cudaStream_t strea
   CUtensorMap tw, tx;
   if (!encode_u8_2d(&tw, a.Wp, (uint64_t)a.K / 4, (uint64_t)a.N, kBK / 4, kBM, 0)) return cudaErrorInvalidValue;
   if (!encode_u8_2d(&tx, a.xq, (uint64_t)a.K, (uint64_t)a.M, kBK, (uint32_t)BN, 0)) return cudaErrorInvalidValue;
-  GemmCfg c{a.gamma, a.s, a.y, a.acc, a.err, (int)a.M, (int)a.N, (int)a.K, BN, a.relu2 ? 1 : 0, 0, 1};
+  GemmCfg c{a.gamma, a.s, a.y, a.acc, a.err, (int)a.M, (int)a.N, (int)a.K, BN, a.relu2 ? 1 : 0, 0};
   const size_t smem = 1024 + (size_t)kOpStages * (kAOpBytes + BN * kARowBytes) +
                       (size_t)kRawStages * (kWRawBytes + BN * kBK) + (2 * kRawStages + 2 * kOpStages + 1) * 8 + 16 +
                       (size_t)BN * 4;

@@ -54,15 +54,16 @@ cudaError_t launch_pack_tq5(const float* W, int64_t N, int64_t K, int64_t pitch,
 cudaError_t launch_quant_act(const void* X, bool bf16, int64_t M, int64_t K, int8_t* xq, float* s, int num_sms,
                              uint32_t* err, cudaStream_t stream);
 
-// The same quantisation, also writing the GEMM's fp16 activation operand
-// (gemm_x16_workspace_bytes(M, K) bytes at x16, 16-byte aligned); K % 16 == 0.
 // Sub-layer RMS normalisation folded into the quantisation: x_q = quant(X * gain),
 // s = s(X * gain) * sqrt(mean(X^2) + eps).  gain may be null (all ones).
 cudaError_t launch_rmsnorm_quant_act(const void* X, bool bf16, int64_t M, int64_t K, const float* gain, float eps,
                                      int8_t* xq, float* s, cudaStream_t stream);
 
+// The per-token quantisation, also writing the GEMM's fp16 activation operand
+// (M x K halves at x16, 16-byte aligned; K % 16 == 0); the first CTA zeroes
+// cnt[0 .. ncnt), the stream-K GEMM's arrival counters (cnt may be null).
 cudaError_t launch_quant_act_x16(const void* X, bool bf16, int64_t M, int64_t K, int8_t* xq, float* s, void* x16,
-                                 cudaStream_t stream);
+                                 uint32_t* cnt, int ncnt, cudaStream_t stream);
 
 struct ForwardArgs {
   const uint8_t* Wp;
@@ -120,14 +121,30 @@ uint8_t* f8_operand(void* ws);
 cudaError_t launch_quant_act_x8(const void* X, bool bf16, int64_t M, int64_t K, int8_t* xq, float* s, void* ws,
                                 int num_sms, cudaStream_t stream);
 
+// Stream-K fp16 tensor-core GEMM (gemm_f16_sk.cu) for more than
+// kF8MaxTokens tokens, in token tiles of at most kSkMaxTile, through a
+// workspace of gemm_sk_workspace_bytes(M, K, num_sms) bytes (16-byte aligned):
+// the fp16 activation operand (M x K halves at its start), partial-sum slots
+// and arrival counters.  The operand and the zeroed counters come from
+// launch_x16_sk_prepass (from x_q) or launch_quant_act_x16 with
+// sk_counters(...) and num_sms counters (from X), in stream order before
+// launch_gemm_f16_sk.
+constexpr int kSkMaxTile = 192;
+int gemm_sk_token_tile(int64_t M);  // tokens per tile: M split into tiles of <= 192, rounded up to 16
+size_t gemm_sk_workspace_bytes(int64_t M, int64_t K, int num_sms);
+uint32_t* sk_counters(void* ws, int64_t M, int64_t K, int num_sms);
+cudaError_t launch_x16_sk_prepass(const int8_t* xq, int64_t M, int64_t K, void* ws, int num_sms, cudaStream_t stream);
+cudaError_t launch_gemm_f16_sk(const ForwardArgs& a, void* ws, int num_sms, cudaStream_t stream);
+
 // Tensor-core GEMM (tcgen05) for more tokens than the GEMV handles well.
 cudaError_t launch_gemm_tc(const ForwardArgs& a, int num_sms, cudaStream_t stream);
 
-// The same GEMM with the activations expanded to fp16 once per call into a
-// workspace of gemm_x16_workspace_bytes(M, K) bytes (16-byte aligned):
-// launch_x16_prepass writes it from x_q, then launch_gemm_tc_x16 reads it.
-size_t gemm_x16_workspace_bytes(int64_t M, int64_t K);
-cudaError_t launch_x16_prepass(const int8_t* xq, int64_t M, int64_t K, void* x16, int num_sms, cudaStream_t stream);
+// The same GEMM on activations expanded to fp16 once per call (M x K halves
+// at x16, written by the quantisation kernel or the stream-K GEMM's prepass):
+// the persistent one-CTA-per-SM kernel.  It serves the shapes where whole
+// output tiles (token tiles of up to 256) fill the SMs at least twice over,
+// gemm_x16_persistent_serves; the stream-K GEMM serves the rest.
+bool gemm_x16_persistent_serves(int64_t M, int64_t N, int num_sms);
 cudaError_t launch_gemm_tc_x16(const ForwardArgs& a, const void* x16, int num_sms, cudaStream_t stream);
 
 }  // namespace bl

@@ -36,9 +36,10 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 
 // Where the fp8 GEMM's operand goes (OUT == 2): the tiled layout of
 // x8_group_offset, tokens in tiles of BN, nkb 512-k blocks, M real tokens.
+// cnt / ncnt also serve OUT == 1 (the stream-K GEMM's counters).
 struct X8Out {
   uint8_t* x8;
-  uint32_t* cnt;  // arrival counters, zeroed by block 0
+  uint32_t* cnt;  // arrival counters, zeroed by block 0 (OUT != 0)
   int ncnt;
   int64_t M, nkb;
   int BN;
@@ -54,9 +55,9 @@ __global__ void __launch_bounds__(1024) quant_act_kernel(const void* __restrict_
                                                          uint4* __restrict__ xop, const X8Out o8) {
   constexpr int kEsize = BF16 ? 2 : 4;
   const int64_t m = blockIdx.x;
+  if (OUT != 0 && blockIdx.x == 0)
+    for (int i = threadIdx.x; i < o8.ncnt; i += blockDim.x) o8.cnt[i] = 0u;
   if (OUT == 2) {
-    if (blockIdx.x == 0)
-      for (int i = threadIdx.x; i < o8.ncnt; i += blockDim.x) o8.cnt[i] = 0u;
     const int64_t kpad = o8.nkb * kX8Block;
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
     for (int64_t k16 = (m < o8.M ? K : 0) + 16 * (int64_t)threadIdx.x; k16 < kpad; k16 += 16 * (int64_t)blockDim.x) {
@@ -643,15 +644,17 @@ cudaError_t launch_quant_act(const void* X, bool bf16, int64_t M, int64_t K, int
 }
 
 cudaError_t launch_quant_act_x16(const void* X, bool bf16, int64_t M, int64_t K, int8_t* xq, float* s, void* x16,
-                                 cudaStream_t stream) {
+                                 uint32_t* cnt, int ncnt, cudaStream_t stream) {
   // one 16-element group per thread in the second pass (K % 16 == 0)
   int threads = (int)((K / 16 + 31) / 32 * 32);
   if (threads > 1024) threads = 1024;
   if (threads < 64) threads = 64;
   uint4* o = static_cast<uint4*>(x16);
-  const X8Out none{};
-  if (bf16) quant_act_kernel<true, 1><<<(unsigned)M, threads, 0, stream>>>(X, K, true, xq, s, o, none);
-  else quant_act_kernel<false, 1><<<(unsigned)M, threads, 0, stream>>>(X, K, true, xq, s, o, none);
+  X8Out counters{};
+  counters.cnt = cnt;
+  counters.ncnt = cnt ? ncnt : 0;
+  if (bf16) quant_act_kernel<true, 1><<<(unsigned)M, threads, 0, stream>>>(X, K, true, xq, s, o, counters);
+  else quant_act_kernel<false, 1><<<(unsigned)M, threads, 0, stream>>>(X, K, true, xq, s, o, counters);
   return cudaGetLastError();
 }
 

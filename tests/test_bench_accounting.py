@@ -62,7 +62,8 @@ def test_restated_routing_labels():
     assert bench.gemm_variant(layer(16, 3200, 8640), 148) == "gemm_f8_kernel"
     assert bench.gemm_variant(layer(64, 3200, 8640), 148) == "gemm_f8_kernel"
     assert bench.gemm_variant(layer(1, 32768 + 64, 100), 148) == "gemm_f8_kernel"
-    assert bench.gemm_variant(layer(176, 8192, 28672), 148) == "gemm_tc_x16_persistent_kernel"
+    assert bench.gemm_variant(layer(176, 8192, 28672), 148) == "gemm_f16_sk_kernel"  # 224 tiles: stream-K
+    assert bench.gemm_variant(layer(176, 28672, 8192), 148) == "gemm_f16_sk_kernel"
 
 
 PEAKS = {"hbm_gbs": 6484.9, "bf16_tflops": 1755.4}  # ridge about 270.7 op/B

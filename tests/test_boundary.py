@@ -172,14 +172,26 @@ def f8_workspace(M, K, sms):
     return up(ntm * 2 * bn * kpad) + 2 * sms * bn * 128 * 4 + up(4 * sms)
 
 
+def sk_workspace(M, K, sms):
+    """The stream-K fp16 GEMM's workspace written out: the fp16 operand (M x K
+    halves), two partial-sum slots per CTA of 128 features x the token tile
+    (M split into tiles of at most 192, rounded up to 16) in fp32, and one
+    arrival counter per CTA, the first and last part rounded up to 256 bytes."""
+    up = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    ntm = (M + 191) // 192
+    bn = ((M + ntm - 1) // ntm + 15) // 16 * 16
+    return up(2 * M * K) + 2 * sms * bn * 128 * 4 + up(4 * sms)
+
+
 def test_forward_workspace_bytes(bl):
     f = bl.bitlinear_forward_workspace_bytes
     sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 256
     assert f(1, 6912, 2560) == 0 and f(4, 100, 32768) == 0  # the GEMV path needs none
     assert f(5, 100, 64) == f8_workspace(5, 64, sms)  # up to 64 tokens: the fp8 GEMM
     assert f(64, 100, 2560) == f8_workspace(64, 2560, sms)
-    assert f(65, 100, 2560) == 2 * 65 * 2560  # more: the fp16 operand of the f16 GEMM
-    assert f(2048, 6912, 2560) == 2 * 2048 * 2560
+    assert f(65, 100, 2560) == sk_workspace(65, 2560, sms)  # more: the stream-K fp16 GEMM
+    assert f(176, 8192, 28672) == sk_workspace(176, 28672, sms)
+    assert f(2048, 6912, 2560) == sk_workspace(2048, 2560, sms)
     assert f(1, 100, 32768 + 64) == f8_workspace(1, 32768 + 64, sms)  # K beyond the GEMV goes to a GEMM
     assert f(0, 1, 64) == 0
 
