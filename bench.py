@@ -660,7 +660,8 @@ def run_gpu(args, dist, rank, world, local):
     # ---- the FFN pieces around each layer, timed the same way (outside the step):
     # the sub-layer RMS norm then the quantisation of the layer's X, and the
     # fused forward with and without the squared-ReLU epilogue
-    ffn = {"rmsnorm_quant": [], "forward_us": [], "forward_relu2_us": []}
+    ffn = {"rmsnorm_quant": [], "forward_us": [], "forward_relu2_us": [], "norm_forward_one_call_us": [],
+           "norm_forward_two_calls_us": []}
     for l, L in enumerate(wl.layers):
         gain = torch.rand((L.K,), generator=torch.Generator().manual_seed(l), dtype=torch.float32).add_(0.5).to(dev)
         us = graph_us(lambda j, l=l, gain=gain: bl.bitlinear_rmsnorm_quant_act(
@@ -679,11 +680,25 @@ def run_gpu(args, dist, rank, world, local):
                 ffn[key].append(round(graph_us(lambda j, l=l, fl=fl: bl.bitlinear_quant_forward_ws(
                     Wrot[l][j % Rs[l]], gammas[l], Xrot[l][j % Rs[l]], y=ys[l], x_q=xqs[l], s=ss[l],
                     workspace=workspace, flags=fl, stream=stream)), 3))
+        if not tq5:
+            # the FFN's second BitLinear: RMS norm + quantisation + forward in one call
+            # (the normalising kernel writes the GEMM's operand) against the two calls
+            def two_calls(j, l=l, gain=gain):
+                bl.bitlinear_rmsnorm_quant_act(Xrot[l][j % Rs[l]], gain=gain, x_q=xqs[l], s=ss[l], stream=stream)
+                bl.bitlinear_forward_ws(Wrot[l][j % Rs[l]], gammas[l], xqs[l], ss[l], y=ys[l], workspace=workspace,
+                                        stream=stream)
+            ffn["norm_forward_one_call_us"].append(round(graph_us(
+                lambda j, l=l, gain=gain: bl.bitlinear_rmsnorm_quant_forward_ws(
+                    Wrot[l][j % Rs[l]], gammas[l], Xrot[l][j % Rs[l]], gain=gain, y=ys[l], x_q=xqs[l], s=ss[l],
+                    workspace=workspace, stream=stream)), 3))
+            ffn["norm_forward_two_calls_us"].append(round(graph_us(two_calls), 3))
     bl.bitlinear_check_device_error(stream)
     ffn["note"] = ("rmsnorm_quant: bitlinear_rmsnorm_quant_act on each layer's X with a per-channel gain, bytes = "
                    "X read + x_q write + s + gain, frac of the measured copy bandwidth; forward(_relu2)_us: "
                    + ("bitlinear_forward_tq5 (quantised activations)" if tq5 else "bitlinear_quant_forward_ws")
-                   + " without and with BITLINEAR_RELU2")
+                   + " without and with BITLINEAR_RELU2; norm_forward_one_call_us: bitlinear_rmsnorm_quant_forward_ws "
+                   "(the normalising kernel writes the GEMM operand) against norm_forward_two_calls_us: "
+                   "bitlinear_rmsnorm_quant_act then bitlinear_forward_ws")
 
     # ---- the lookup-table GEMV beside the conditional-add GEMV, on the layers of
     # at most 4 tokens (both on quantised activations, graph-replayed)

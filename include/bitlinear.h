@@ -358,6 +358,33 @@ bl_status bitlinear_quant_forward_ws(const uint8_t* W_packed, const float* gamma
                                      unsigned flags, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * bitlinear_rmsnorm_quant_forward_ws -- the second BitLinear of a BitNet FFN
+ * in one call: the sub-layer RMS normalisation and per-token quantisation of
+ * bitlinear_rmsnorm_quant_act (same x_q and s, bit for bit), then the forward
+ * of bitlinear_forward_ws on them (same y and acc, bit for bit).  For more
+ * than 4 tokens (or K > 32768) the normalising kernel also writes the
+ * tensor-core GEMM's activation operand into the workspace, so the operand
+ * needs no separate expansion pass; for up to 4 tokens it is followed by the
+ * GEMV on x_q.
+ *
+ *   W_packed, gamma, y, acc, workspace, workspace_bytes
+ *             as for bitlinear_forward_ws (same workspace size)
+ *   X         in   [M, K] row-major, BL_BF16 or BL_F32, 16-byte aligned
+ *   gain      in   fp32 [K], 16-byte aligned, or NULL for all ones
+ *   eps       in   finite, > 0
+ *   x_q, s    out  as for bitlinear_quant_act; x_q 16-byte aligned
+ *   flags     in   0 or BITLINEAR_RELU2
+ *   K % 64 == 0, K <= BITLINEAR_MAX_K.
+ *
+ * Errors as for bitlinear_forward_ws; BL_ERR_INVALID_ARG also for a bad eps
+ * or flag.
+ */
+bl_status bitlinear_rmsnorm_quant_forward_ws(const uint8_t* W_packed, const float* gamma, const void* X, bl_dtype dtype,
+                                             int64_t M, int64_t N, int64_t K, const float* gain, float eps, float* y,
+                                             int8_t* x_q, float* s, int32_t* acc, unsigned flags, void* workspace,
+                                             size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * bitlinear_check_device_error -- waits for `stream`, then reports and clears
  * the library's device error word: BL_ERR_TIMEOUT if a kernel gave up on a
  * bounded wait since the last check, BL_ERR_CUDA if the stream itself failed,

@@ -37,6 +37,7 @@ __all__ = [
     "bitlinear_forward_workspace_bytes",
     "bitlinear_forward_ws",
     "bitlinear_quant_forward_ws",
+    "bitlinear_rmsnorm_quant_forward_ws",
     "bitlinear_check_device_error",
     "bitlinear_status_string",
     "BITLINEAR_WEIGHTS_RESIDENT",
@@ -69,6 +70,7 @@ EXPORTED_SYMBOLS = (
     "bitlinear_forward_workspace_bytes",
     "bitlinear_forward_ws",
     "bitlinear_quant_forward_ws",
+    "bitlinear_rmsnorm_quant_forward_ws",
     "bitlinear_tq5_row_bytes",
     "bitlinear_pack_weights_tq5",
     "bitlinear_forward_tq5",
@@ -118,6 +120,9 @@ def _load() -> ctypes.CDLL:
     L.bitlinear_forward_ws.restype = i32
     L.bitlinear_quant_forward_ws.argtypes = [P, P, P, i32, i64, i64, i64, P, P, P, P, ctypes.c_uint, P, sz, P]
     L.bitlinear_quant_forward_ws.restype = i32
+    L.bitlinear_rmsnorm_quant_forward_ws.argtypes = [P, P, P, i32, i64, i64, i64, P, ctypes.c_float, P, P, P, P,
+                                                     ctypes.c_uint, P, sz, P]
+    L.bitlinear_rmsnorm_quant_forward_ws.restype = i32
     L.bitlinear_check_device_error.argtypes = [P]
     L.bitlinear_check_device_error.restype = i32
     L.bitlinear_status_string.argtypes = [i32]
@@ -426,6 +431,50 @@ def bitlinear_quant_forward_ws(W_packed: torch.Tensor, gamma: torch.Tensor, X: t
                                                 _dev(y, "y", torch.float32), _dev(x_q, "x_q", torch.int8),
                                                 _dev(s, "s", torch.float32), acc_ptr, int(flags), ws_ptr, ws_bytes,
                                                 _stream(stream)), "bitlinear_quant_forward_ws")
+    return (y, x_q, s, acc) if want_acc else (y, x_q, s)
+
+
+def bitlinear_rmsnorm_quant_forward_ws(W_packed: torch.Tensor, gamma: torch.Tensor, X: torch.Tensor,
+                                       gain: torch.Tensor | None = None, eps: float = 1e-5,
+                                       y: torch.Tensor | None = None, x_q: torch.Tensor | None = None,
+                                       s: torch.Tensor | None = None, acc: torch.Tensor | bool | None = None,
+                                       flags: int = 0, workspace: torch.Tensor | None = None, stream=None):
+    """The FFN's second BitLinear in one call: :func:`bitlinear_rmsnorm_quant_act`
+    (sub-layer RMS norm with optional gain, eps > 0) then the forward of
+    :func:`bitlinear_forward_ws` on its x_q and s; for more than 4 tokens the
+    normalising kernel writes the GEMM's operand itself.  Returns (y, x_q, s)
+    or (y, x_q, s, acc)."""
+    N, K4 = W_packed.shape
+    M, K = X.shape
+    if K4 * 4 != K:
+        raise ValueError(f"W_packed has K/4 = {K4} but X has K = {K}")
+    if X.dtype == torch.bfloat16:
+        dt = BL_BF16
+    elif X.dtype == torch.float32:
+        dt = BL_F32
+    else:
+        raise ValueError(f"X must be bf16 or fp32, got {X.dtype}")
+    if not eps > 0.0:
+        raise ValueError("eps must be > 0")
+    dev = X.device
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    if x_q is None:
+        x_q = torch.empty((M, K), dtype=torch.int8, device=dev)
+    if s is None:
+        s = torch.empty((M,), dtype=torch.float32, device=dev)
+    want_acc = acc is not None and acc is not False
+    if acc is True:
+        acc = torch.empty((M, N), dtype=torch.int32, device=dev)
+    acc_ptr = _dev(acc, "acc", torch.int32) if want_acc else None
+    g_ptr = _dev(gain, "gain", torch.float32) if gain is not None else None
+    ws_ptr, ws_bytes = _workspace(M, N, K, workspace, dev)
+    _check(get_lib().bitlinear_rmsnorm_quant_forward_ws(_dev(W_packed, "W_packed", torch.uint8),
+                                                        _dev(gamma, "gamma", torch.float32), _dev(X, "X"), dt, M, N,
+                                                        K, g_ptr, float(eps), _dev(y, "y", torch.float32),
+                                                        _dev(x_q, "x_q", torch.int8), _dev(s, "s", torch.float32),
+                                                        acc_ptr, int(flags), ws_ptr, ws_bytes, _stream(stream)),
+           "bitlinear_rmsnorm_quant_forward_ws")
     return (y, x_q, s, acc) if want_acc else (y, x_q, s)
 
 

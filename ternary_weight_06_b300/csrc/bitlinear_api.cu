@@ -256,6 +256,43 @@ bl_status bitlinear_quant_forward_ws(const uint8_t* W_packed, const float* gamma
   return from_cuda(bl::launch_gemm_f16_sk(a, workspace, d.num_sms, stream));
 }
 
+bl_status bitlinear_rmsnorm_quant_forward_ws(const uint8_t* W_packed, const float* gamma, const void* X, bl_dtype dtype,
+                                             int64_t M, int64_t N, int64_t K, const float* gain, float eps, float* y,
+                                             int8_t* x_q, float* s, int32_t* acc, unsigned flags, void* workspace,
+                                             size_t workspace_bytes, cudaStream_t stream) {
+  if (!W_packed || !gamma || !X || !y || !x_q || !s) return BL_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1) return BL_ERR_INVALID_ARG;
+  if (dtype != BL_F32 && dtype != BL_BF16) return BL_ERR_INVALID_ARG;
+  if (!std::isfinite(eps) || !(eps > 0.0f)) return BL_ERR_INVALID_ARG;
+  if (flags & ~BITLINEAR_RELU2) return BL_ERR_INVALID_ARG;
+  if (K % 64 != 0 || K > BITLINEAR_MAX_K || M > INT32_MAX || N > INT32_MAX) return BL_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(W_packed, 16) || !aligned(X, 16) || !aligned(x_q, 16) || !aligned(y, 16) || !aligned(gamma, 4) ||
+      !aligned(s, 4) || (gain && !aligned(gain, 16)) || (acc && !aligned(acc, 16)))
+    return BL_ERR_MISALIGNED;
+  if (bl_status st = check_workspace(M, N, K, workspace, workspace_bytes)) return st;
+  DeviceInfo d;
+  if (bl_status st = device_info(&d)) return st;
+  bl::ForwardArgs a{W_packed, gamma, x_q, s, M, N, K, y, acc, d.err, (flags & BITLINEAR_RELU2) != 0};
+  const bool bf16 = dtype == BL_BF16;
+  if (M <= bl::kGemvMaxTokens && K <= bl::kGemvMaxK) {
+    // a few tokens: the RMS-norm quantisation, then the GEMV on x_q
+    if (cudaError_t e = bl::launch_rmsnorm_quant_act(X, bf16, M, K, gain, eps, x_q, s, stream)) return from_cuda(e);
+    return from_cuda(bl::launch_gemv(a, d.num_sms, stream));
+  }
+  // more: the RMS-norm quantisation writes the GEMM's operand directly
+  if (bl::gemm_f8_serves(M, N, K)) {
+    if (cudaError_t e = bl::launch_rmsnorm_quant_act_x8(X, bf16, M, K, gain, eps, x_q, s, workspace, d.num_sms, stream))
+      return from_cuda(e);
+    return from_cuda(bl::launch_gemm_f8(a, workspace, d.num_sms, stream));
+  }
+  if (cudaError_t e = bl::launch_rmsnorm_quant_act_x16(X, bf16, M, K, gain, eps, x_q, s, workspace,
+                                                       bl::sk_counters(workspace, M, K, d.num_sms), d.num_sms, stream))
+    return from_cuda(e);
+  if (bl::gemm_x16_persistent_serves(M, N, d.num_sms))
+    return from_cuda(bl::launch_gemm_tc_x16(a, workspace, d.num_sms, stream));
+  return from_cuda(bl::launch_gemm_f16_sk(a, workspace, d.num_sms, stream));
+}
+
 bl_status bitlinear_check_device_error(cudaStream_t stream) {
   DeviceInfo d;
   if (bl_status st = device_info(&d)) return st;

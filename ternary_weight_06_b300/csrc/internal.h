@@ -59,6 +59,16 @@ cudaError_t launch_quant_act(const void* X, bool bf16, int64_t M, int64_t K, int
 cudaError_t launch_rmsnorm_quant_act(const void* X, bool bf16, int64_t M, int64_t K, const float* gain, float eps,
                                      int8_t* xq, float* s, cudaStream_t stream);
 
+// The RMS-norm quantisation, also writing a tensor-core GEMM's activation
+// operand: the fp16 image (x16 at the start of the stream-K workspace, cnt as
+// in launch_quant_act_x16) or the fp8 split (in the fp8 GEMM's workspace, as
+// launch_quant_act_x8).  X, gain and xq 16-byte aligned, K % 16 == 0.
+cudaError_t launch_rmsnorm_quant_act_x16(const void* X, bool bf16, int64_t M, int64_t K, const float* gain, float eps,
+                                         int8_t* xq, float* s, void* x16, uint32_t* cnt, int ncnt,
+                                         cudaStream_t stream);
+cudaError_t launch_rmsnorm_quant_act_x8(const void* X, bool bf16, int64_t M, int64_t K, const float* gain, float eps,
+                                        int8_t* xq, float* s, void* ws, int num_sms, cudaStream_t stream);
+
 // The per-token quantisation, also writing the GEMM's fp16 activation operand
 // (M x K halves at x16, 16-byte aligned; K % 16 == 0); the first CTA zeroes
 // cnt[0 .. ncnt), the stream-K GEMM's arrival counters (cnt may be null).

@@ -229,14 +229,29 @@ __device__ __forceinline__ void unpack_chunk(const uint4 v, float* x) {
   }
 }
 
-template <bool BF16>
+// OUT as in quant_act_kernel: 0 x_q and s only; 1 also the fp16 GEMM operand;
+// 2 also the fp8 GEMM operand (the grid then covers every token of the last
+// tile; padding tokens write zeros only).  OUT != 0 needs vec and K % 16 == 0.
+template <bool BF16, int OUT>
 __global__ void __launch_bounds__(1024) rmsnorm_quant_act_kernel(const void* __restrict__ X, int64_t K, bool vec,
                                                                  const float* __restrict__ gain, float eps,
                                                                  unsigned long long recip_k, int8_t* __restrict__ xq,
-                                                                 float* __restrict__ s) {
+                                                                 float* __restrict__ s, uint4* __restrict__ xop,
+                                                                 const X8Out o8) {
   constexpr int kEsize = BF16 ? 2 : 4;
   constexpr int kPer = 16 / kEsize;  // elements per 16-byte chunk
   const int64_t m = blockIdx.x;
+  if (OUT != 0 && blockIdx.x == 0)
+    for (int i = threadIdx.x; i < o8.ncnt; i += blockDim.x) o8.cnt[i] = 0u;
+  if (OUT == 2) {
+    const int64_t kpad = o8.nkb * kX8Block;
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    for (int64_t k16 = (m < o8.M ? K : 0) + 16 * (int64_t)threadIdx.x; k16 < kpad; k16 += 16 * (int64_t)blockDim.x) {
+      *reinterpret_cast<uint4*>(o8.x8 + x8_group_offset(m, k16, 0, o8.BN, o8.nkb)) = z;
+      *reinterpret_cast<uint4*>(o8.x8 + x8_group_offset(m, k16, 1, o8.BN, o8.nkb)) = z;
+    }
+    if (m >= o8.M) return;  // a padding token of the last tile: zeros only (whole CTA, before any barrier)
+  }
   const char* row = static_cast<const char*>(X) + m * K * kEsize;
   const uint4* row4 = reinterpret_cast<const uint4*>(row);
   const float4* gain4 = reinterpret_cast<const float4*>(gain);
@@ -325,7 +340,40 @@ __global__ void __launch_bounds__(1024) rmsnorm_quant_act_kernel(const void* __r
   const float r = fin[0], sg = fin[1];
 
   // pass 3: codes of x_n = fp32(x * g) / r
-  if (vec) {
+  if (OUT != 0) {
+    // one 16-element group per thread: x_q (natural order) and the GEMM's operand
+#pragma unroll 1
+    for (int64_t gq = tid; gq < K / 16; gq += nt) {
+      uint32_t nat[4];
+#pragma unroll
+      for (int c2 = 0; c2 < 16 / kPer; ++c2) {
+        const int64_t c = gq * (16 / kPer) + c2;
+        float x[kPer], g[kPer];
+        unpack_chunk<BF16>(__ldg(row4 + c), x);
+        load_gain(c, g);
+        uint32_t q[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) q[i] = q8(__fdiv_rn(__fmul_rn(x[i], g[i]), r), sg);
+#pragma unroll
+        for (int w = 0; w < kPer / 4; ++w)
+          nat[c2 * (kPer / 4) + w] = q[4 * w] | (q[4 * w + 1] << 8) | (q[4 * w + 2] << 16) | (q[4 * w + 3] << 24);
+      }
+      const uint4 q4 = make_uint4(nat[0], nat[1], nat[2], nat[3]);
+      reinterpret_cast<uint4*>(out)[gq] = q4;
+      if (OUT == 1) {
+        uint32_t h[8];
+        convert_x16_f16(q4, h);
+        uint4* xo = xop + m * (K / 8);
+        xo[2 * gq] = make_uint4(h[0], h[1], h[2], h[3]);
+        xo[2 * gq + 1] = make_uint4(h[4], h[5], h[6], h[7]);
+      } else {
+        uint4 hi, lo;
+        x8_rows16(q4, &hi, &lo);
+        *reinterpret_cast<uint4*>(o8.x8 + x8_group_offset(m, 16 * gq, 0, o8.BN, o8.nkb)) = hi;
+        *reinterpret_cast<uint4*>(o8.x8 + x8_group_offset(m, 16 * gq, 1, o8.BN, o8.nkb)) = lo;
+      }
+    }
+  } else if (vec) {
 #pragma unroll 1
     for (int64_t c = tid; c < nch; c += nt) {
       float x[kPer], g[kPer];
@@ -618,8 +666,56 @@ cudaError_t launch_rmsnorm_quant_act(const void* X, bool bf16, int64_t M, int64_
   int threads = (int)((work + 31) / 32 * 32);
   if (threads > 1024) threads = 1024;
   const unsigned long long rk = sq_recip((uint32_t)K);
-  if (bf16) rmsnorm_quant_act_kernel<true><<<(unsigned)M, threads, 0, stream>>>(X, K, vec, gain, eps, rk, xq, s);
-  else rmsnorm_quant_act_kernel<false><<<(unsigned)M, threads, 0, stream>>>(X, K, vec, gain, eps, rk, xq, s);
+  const X8Out none{};
+  if (bf16)
+    rmsnorm_quant_act_kernel<true, 0><<<(unsigned)M, threads, 0, stream>>>(X, K, vec, gain, eps, rk, xq, s, nullptr, none);
+  else
+    rmsnorm_quant_act_kernel<false, 0><<<(unsigned)M, threads, 0, stream>>>(X, K, vec, gain, eps, rk, xq, s, nullptr, none);
+  return cudaGetLastError();
+}
+
+namespace {
+
+// Threads of the RMS-norm kernels that write a GEMM operand: one 16-element
+// group per thread in the codes pass, one 16-byte chunk per thread in the
+// reductions.
+int rmsnorm_operand_threads(int64_t K, bool bf16) {
+  const int64_t chunks = K * (bf16 ? 2 : 4) / 16;
+  int threads = (int)((chunks + 31) / 32 * 32);
+  if (threads > 1024) threads = 1024;
+  if (threads < 64) threads = 64;
+  return threads;
+}
+
+}  // namespace
+
+cudaError_t launch_rmsnorm_quant_act_x16(const void* X, bool bf16, int64_t M, int64_t K, const float* gain, float eps,
+                                         int8_t* xq, float* s, void* x16, uint32_t* cnt, int ncnt,
+                                         cudaStream_t stream) {
+  const int threads = rmsnorm_operand_threads(K, bf16);
+  const unsigned long long rk = sq_recip((uint32_t)K);
+  X8Out counters{};
+  counters.cnt = cnt;
+  counters.ncnt = cnt ? ncnt : 0;
+  uint4* o = static_cast<uint4*>(x16);
+  if (bf16)
+    rmsnorm_quant_act_kernel<true, 1><<<(unsigned)M, threads, 0, stream>>>(X, K, true, gain, eps, rk, xq, s, o, counters);
+  else
+    rmsnorm_quant_act_kernel<false, 1><<<(unsigned)M, threads, 0, stream>>>(X, K, true, gain, eps, rk, xq, s, o, counters);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm_quant_act_x8(const void* X, bool bf16, int64_t M, int64_t K, const float* gain, float eps,
+                                        int8_t* xq, float* s, void* ws, int num_sms, cudaStream_t stream) {
+  const int threads = rmsnorm_operand_threads(K, bf16);
+  const unsigned long long rk = sq_recip((uint32_t)K);
+  const int BN = gemm_f8_token_tile(M);
+  const X8Out o8{f8_operand(ws), f8_counters(ws, M, K, num_sms), num_sms, M, gemm_f8_kblocks(K), BN};
+  const unsigned grid = (unsigned)((M + BN - 1) / BN * BN);  // every token of the last tile
+  if (bf16)
+    rmsnorm_quant_act_kernel<true, 2><<<grid, threads, 0, stream>>>(X, K, true, gain, eps, rk, xq, s, nullptr, o8);
+  else
+    rmsnorm_quant_act_kernel<false, 2><<<grid, threads, 0, stream>>>(X, K, true, gain, eps, rk, xq, s, nullptr, o8);
   return cudaGetLastError();
 }
 

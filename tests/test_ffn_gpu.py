@@ -172,3 +172,63 @@ def test_ffn_chain(bl, M):
     assert np.all(yr[~nz] == 0)
     assert (np.abs(yr[nz] - y_ref[nz]) / np.abs(y_ref[nz])).max() <= Y_RTOL
     bl.bitlinear_check_device_error()
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 300, 1024), (4, 999, 2560), (16, 1000, 2560), (64, 700, 8192 + 64),
+                                   (97, 2000, 640), (176, 3000, 8192), (300, 19000, 128)])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("with_gain,relu2", [(False, False), (True, True)])
+def test_rmsnorm_quant_forward_ws_every_path(bl, M, N, K, dtype, with_gain, relu2):
+    """the FFN's second BitLinear in one call, on each route (GEMV after the
+    normalising kernel; the normalising kernel writing the fp8 GEMM's split
+    operand, or the fp16 operand of the stream-K or persistent GEMM): x_q and s
+    bit-exact against the oracle's RMS-norm quantisation, acc and y bit-exact
+    against the oracle's forward on them; special rows included"""
+    rng = np.random.default_rng(M * 7 + N + K)
+    q = rng.integers(-1, 2, size=(N, K)).astype(np.int8)
+    p = oracle.pack(q)
+    g = torch.Generator().manual_seed(M + K)
+    X = torch.randn((M, K), generator=g) * 3.0
+    X[0] = 0.0  # an all-zero token
+    if M > 2:
+        X[M // 2] *= 1e30  # squares overflow fp32: r = inf, codes 0
+        X[M - 1] *= 1e-40
+    X = X.to(dtype)
+    gain = (torch.rand((K,), generator=g) * 2.0).to(torch.float32) if with_gain else None
+    xq_ref, s_ref = oracle.rmsnorm_quant_act(X.to(torch.float32).numpy(), gain=None if gain is None else gain.numpy())
+    y_ref, acc_ref = oracle.forward(p, np.float32(0.04), xq_ref, s_ref, K, omp=True)
+    if relu2:
+        y_ref = oracle.relu2(y_ref)
+    y, xq, s, acc = bl.bitlinear_rmsnorm_quant_forward_ws(
+        torch.from_numpy(p).cuda(), torch.tensor([0.04]).cuda(), X.cuda(),
+        gain=None if gain is None else gain.cuda(), acc=True, flags=bl.BITLINEAR_RELU2 if relu2 else 0)
+    torch.cuda.synchronize()
+    assert np.array_equal(xq.cpu().numpy(), xq_ref), "codes must be bit-exact"
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), s_ref.view(np.uint32)), "s must be bit-exact"
+    assert np.array_equal(acc.cpu().numpy(), acc_ref)
+    assert np.array_equal(y.cpu().numpy().view(np.uint32), y_ref.view(np.uint32))
+    bl.bitlinear_check_device_error()
+
+
+@pytest.mark.parametrize("M", [1, 16, 176])
+def test_ffn_chain_one_call_second_bitlinear(bl, M):
+    """the down projection through bitlinear_rmsnorm_quant_forward_ws equals
+    the two-call chain (bitlinear_rmsnorm_quant_act, then bitlinear_forward_ws)
+    bit for bit"""
+    rng = np.random.default_rng(100 + M)
+    D, H = 512, 1536
+    p_up = oracle.pack(rng.integers(-1, 2, size=(H, D)).astype(np.int8))
+    p_dn = oracle.pack(rng.integers(-1, 2, size=(D, H)).astype(np.int8))
+    gain = torch.from_numpy(rng.uniform(0.5, 1.5, size=H).astype(np.float32)).cuda()
+    X = torch.randn((M, D), generator=torch.Generator().manual_seed(9)).to(torch.bfloat16).cuda()
+    Wu, Wd = torch.from_numpy(p_up).cuda(), torch.from_numpy(p_dn).cuda()
+    gu, gd = torch.tensor([0.03]).cuda(), torch.tensor([0.02]).cuda()
+    h, _, _ = bl.bitlinear_quant_forward_ws(Wu, gu, X, flags=bl.BITLINEAR_RELU2)
+    hq, hs = bl.bitlinear_rmsnorm_quant_act(h, gain=gain)
+    y2 = bl.bitlinear_forward_ws(Wd, gd, hq, hs)
+    y1, hq1, hs1 = bl.bitlinear_rmsnorm_quant_forward_ws(Wd, gd, h, gain=gain)
+    torch.cuda.synchronize()
+    assert torch.equal(hq1, hq)
+    assert torch.equal(hs1.view(torch.int32), hs.view(torch.int32))
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
+    bl.bitlinear_check_device_error()
