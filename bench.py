@@ -661,7 +661,7 @@ def run_gpu(args, dist, rank, world, local):
     # the sub-layer RMS norm then the quantisation of the layer's X, and the
     # fused forward with and without the squared-ReLU epilogue
     ffn = {"rmsnorm_quant": [], "forward_us": [], "forward_relu2_us": [], "norm_forward_one_call_us": [],
-           "norm_forward_two_calls_us": []}
+           "norm_forward_two_calls_us": [], "forward_requant_us": [], "forward_then_quant_us": []}
     for l, L in enumerate(wl.layers):
         gain = torch.rand((L.K,), generator=torch.Generator().manual_seed(l), dtype=torch.float32).add_(0.5).to(dev)
         us = graph_us(lambda j, l=l, gain=gain: bl.bitlinear_rmsnorm_quant_act(
@@ -692,13 +692,31 @@ def run_gpu(args, dist, rank, world, local):
                     Wrot[l][j % Rs[l]], gammas[l], Xrot[l][j % Rs[l]], gain=gain, y=ys[l], x_q=xqs[l], s=ss[l],
                     workspace=workspace, stream=stream)), 3))
             ffn["norm_forward_two_calls_us"].append(round(graph_us(two_calls), 3))
+            # the FFN's first BitLinear with its squared-ReLU output quantised for the
+            # next layer in the same call, against the two calls
+            yq = torch.empty((L.M, L.N), dtype=torch.int8, device=dev)
+            sy = torch.empty((L.M,), dtype=torch.float32, device=dev)
+
+            def then_quant(j, l=l, yq=yq, sy=sy):
+                bl.bitlinear_quant_forward_ws(Wrot[l][j % Rs[l]], gammas[l], Xrot[l][j % Rs[l]], y=ys[l], x_q=xqs[l],
+                                              s=ss[l], workspace=workspace, flags=bl.BITLINEAR_RELU2, stream=stream)
+                bl.bitlinear_quant_act(ys[l], x_q=yq, s=sy, stream=stream)
+            ffn["forward_requant_us"].append(round(graph_us(
+                lambda j, l=l, yq=yq, sy=sy: bl.bitlinear_quant_forward_requant_ws(
+                    Wrot[l][j % Rs[l]], gammas[l], Xrot[l][j % Rs[l]], y=ys[l], x_q=xqs[l], s=ss[l], y_q=yq, s_y=sy,
+                    workspace=workspace, flags=bl.BITLINEAR_RELU2, stream=stream)), 3))
+            ffn["forward_then_quant_us"].append(round(graph_us(then_quant), 3))
+            del yq, sy
     bl.bitlinear_check_device_error(stream)
     ffn["note"] = ("rmsnorm_quant: bitlinear_rmsnorm_quant_act on each layer's X with a per-channel gain, bytes = "
                    "X read + x_q write + s + gain, frac of the measured copy bandwidth; forward(_relu2)_us: "
                    + ("bitlinear_forward_tq5 (quantised activations)" if tq5 else "bitlinear_quant_forward_ws")
                    + " without and with BITLINEAR_RELU2; norm_forward_one_call_us: bitlinear_rmsnorm_quant_forward_ws "
                    "(the normalising kernel writes the GEMM operand) against norm_forward_two_calls_us: "
-                   "bitlinear_rmsnorm_quant_act then bitlinear_forward_ws")
+                   "bitlinear_rmsnorm_quant_act then bitlinear_forward_ws; forward_requant_us: "
+                   "bitlinear_quant_forward_requant_ws with BITLINEAR_RELU2 (y also quantised to int8 in the same "
+                   "call, read back from L2) against forward_then_quant_us: bitlinear_quant_forward_ws with "
+                   "BITLINEAR_RELU2 then bitlinear_quant_act on y")
 
     # ---- the lookup-table GEMV beside the conditional-add GEMV, on the layers of
     # at most 4 tokens (both on quantised activations, graph-replayed)

@@ -2,11 +2,11 @@
  * bitlinear.h -- C ABI of libbitlinear.so, the BitNet b1.58 BitLinear forward
  * pass on NVIDIA B300 (sm_103a).
  *
- * The operation (BitLinear in place of a dense linear layer: weights
- * constrained to {-1, 0, +1} by an absmean quantiser, activations at 8 bits;
- * anthology note-168 on arXiv 2402.17764, section "What it does"; the
- * yousumm.com transcript of the BitNet b1.58 2B4T video, paragraph on the
- * "ABS mean quantizer" and the "eight-bit numbers"):
+ * The operation (BitLinear replaces a dense linear layer; its weights take
+ * only the values -1, 0, +1, chosen by an absmean quantiser, and its
+ * activations are 8-bit integers; anthology note-168 on arXiv 2402.17764,
+ * section "What it does"; the yousumm.com transcript of the BitNet b1.58 2B4T
+ * video, the paragraph on the warehouse analogy):
  *
  *   gamma  = mean(|W|)                                 one fp32 per matrix
  *   W_q    = clip(round(W / (gamma + eps)), -1, +1)
@@ -27,7 +27,7 @@
  *     all-zero token gives x_q = 0 and y = 0;
  *   - y[m,n] = fp32( fp32(acc[m,n]) * fp32(gamma / s[m]) ).
  *
- * Packed weight layout ("bundles four chips into a single byte", yousumm.com
+ * Packed weight layout (four ternary weights per byte: yousumm.com
  * transcript, paragraph on running the model on graphics cards): row-major
  * [N, K/4] bytes; weight (n, k) is the 2-bit code W_q + 1 in {0, 1, 2} at
  * bits 2*(k % 4) of byte n*K/4 + k/4.  Code 3 is never written.
@@ -87,8 +87,8 @@ size_t bitlinear_pack_workspace_bytes(int64_t N, int64_t K);
 
 /*
  * bitlinear_pack_weights -- absmean ternarisation and 2-bit packing of one
- * latent weight matrix (anthology note-168, "What it does": weights
- * constrained to {-1, 0, +1} by an absmean quantisation; yousumm.com
+ * latent weight matrix (anthology note-168, "What it does": an absmean
+ * quantiser maps every weight to -1, 0 or +1; yousumm.com
  * transcript: four weights per byte).
  *
  *   W          in   fp32 [N, K] row-major, 16-byte aligned, finite values
@@ -145,7 +145,7 @@ int64_t bitlinear_tq5_row_bytes(int64_t K);
 /*
  * bitlinear_pack_weights_tq5 -- bitlinear_pack_weights written in the base-3
  * format: five ternary weights per byte, 1.6 bits per weight, close to the
- * log2(3) = 1.58 bits of information in one weight (yousumm.com transcript,
+ * log2(3) = 1.58 bits a three-valued weight carries (yousumm.com transcript,
  * the GPU-plumbing paragraph; anthology note-168, "What it does").  Byte j
  * of row n holds sum_{i<5} (W_q[n, 5j+i] + 1) * 3^i, least significant digit
  * first, a value in 0..242; positions at or past K count as W_q = 0, and each
@@ -228,8 +228,9 @@ bl_status bitlinear_rmsnorm_quant_act(const void* X, bl_dtype dtype, int64_t M, 
  * product accumulated exactly in int32, rescaled per token by gamma/s[m] in
  * a fused epilogue (anthology note-168, "The part that is a bet rather than a
  * measurement": the product only involves integer addition; yousumm.com
- * transcript: packed weights are unpacked next to the math engine and
- * multiplied with the 8-bit activations).
+ * transcript, the paragraph on running the model on graphics cards: packed
+ * weights are expanded beside the arithmetic units and multiplied with the
+ * 8-bit activations).
  *
  *   W_packed  in   uint8 [N, K/4] from bitlinear_pack_weights, 16-byte aligned
  *   gamma     in   one fp32 (device)
@@ -332,7 +333,8 @@ size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * inside the GEMM, which removes most of the GEMM's operand-conversion work
  * for many tokens.  The product is that of bitlinear_forward (anthology
  * note-168, "The part that is a bet rather than a measurement"; yousumm.com
- * transcript: unpacked next to the math engine).
+ * transcript, the paragraph on running the model on graphics cards: weights
+ * expanded beside the arithmetic units).
  *
  *   arguments as bitlinear_forward, plus
  *   workspace        tmp  >= bitlinear_forward_workspace_bytes(M, N, K)
@@ -356,6 +358,37 @@ bl_status bitlinear_forward_ws(const uint8_t* W_packed, const float* gamma, cons
 bl_status bitlinear_quant_forward_ws(const uint8_t* W_packed, const float* gamma, const void* X, bl_dtype dtype,
                                      int64_t M, int64_t N, int64_t K, float* y, int8_t* x_q, float* s, int32_t* acc,
                                      unsigned flags, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * bitlinear_quant_forward_requant_ws -- bitlinear_quant_forward_ws whose
+ * output is also quantised to int8 for the BitLinear that consumes it: every
+ * layer of the model takes 8-bit activations (anthology note-168, "What it
+ * does"; yousumm.com transcript, the paragraph on the warehouse analogy), and
+ * in the FFN the squared-ReLU output of the first BitLinear feeds the second
+ * (yousumm.com transcript, the paragraph on the sub-layer norm and squared
+ * ReLU).  After the forward, the per-token quantisation kernel reads y back
+ * while it is still resident in L2 and writes
+ *
+ *   s_y[m]    = 127 / max(max_n |y[m,n]|, BITLINEAR_ACT_CLAMP_EPS)
+ *   y_q[m,n]  = clip(round(y[m,n] * s_y[m]), -128, 127)
+ *
+ * which are, bit for bit, bitlinear_quant_act on y (BL_F32).  y, x_q and s
+ * are bit-identical to bitlinear_quant_forward_ws.
+ *
+ *   arguments as bitlinear_quant_forward_ws, without acc, plus
+ *   y_q    out  int8 [M, N], 16-byte aligned
+ *   s_y    out  fp32 [M], 4-byte aligned
+ *   flags  in   0 or BITLINEAR_RELU2 (the squared ReLU is applied before the
+ *               maximum is taken, as the next layer sees it)
+ *   K % 64 == 0, K <= BITLINEAR_MAX_K.
+ *
+ * Errors as for bitlinear_quant_forward_ws.  No path of this call applies the
+ * RMS norm: the one-call FFN form is bitlinear_rmsnorm_quant_forward_ws.
+ */
+bl_status bitlinear_quant_forward_requant_ws(const uint8_t* W_packed, const float* gamma, const void* X, bl_dtype dtype,
+                                             int64_t M, int64_t N, int64_t K, float* y, int8_t* x_q, float* s,
+                                             int8_t* y_q, float* s_y, unsigned flags, void* workspace,
+                                             size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * bitlinear_rmsnorm_quant_forward_ws -- the second BitLinear of a BitNet FFN

@@ -27,7 +27,7 @@
  *       fp32 with round-half-to-even.  It does not depend on summation order.
  *   R2  gamma + eps is one fp32 addition (RNE); W / (gamma+eps) is one IEEE
  *       fp32 division; round() is round-half-to-even.
- *   R3  packing: four codes per byte ("bundles four chips into a single byte",
+ *   R3  packing: four codes per byte (four ternary weights in one byte,
  *       yousumm.com transcript); code = q + 1 in {0,1,2}; weight k of a row
  *       sits in byte k/4 at bits 2*(k%4) (least significant first); rows are
  *       contiguous, K/4 bytes each.  Code 3 is never written.

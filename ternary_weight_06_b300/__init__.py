@@ -14,6 +14,8 @@ Functions carry the C names:
 * :func:`bitlinear_forward`      -- packed W, gamma, x_q, s -> y fp32 [M, N] (and int32 acc)
 * :func:`bitlinear_forward_ws`, :func:`bitlinear_quant_forward_ws` -- the same with a
   caller workspace (:func:`bitlinear_forward_workspace_bytes`) for the tensor-core path
+* :func:`bitlinear_quant_forward_requant_ws` -- the forward with y also quantised to int8 for the next layer
+* :func:`bitlinear_rmsnorm_quant_forward_ws` -- the FFN's second BitLinear (RMS norm, quantisation, forward)
 * :func:`bitlinear_forward_lut` -- the same product by table lookup (comparison variant)
 * :func:`bitlinear_check_device_error`, :func:`bitlinear_status_string`
 """
@@ -38,6 +40,7 @@ __all__ = [
     "bitlinear_forward_ws",
     "bitlinear_quant_forward_ws",
     "bitlinear_rmsnorm_quant_forward_ws",
+    "bitlinear_quant_forward_requant_ws",
     "bitlinear_check_device_error",
     "bitlinear_status_string",
     "BITLINEAR_WEIGHTS_RESIDENT",
@@ -71,6 +74,7 @@ EXPORTED_SYMBOLS = (
     "bitlinear_forward_ws",
     "bitlinear_quant_forward_ws",
     "bitlinear_rmsnorm_quant_forward_ws",
+    "bitlinear_quant_forward_requant_ws",
     "bitlinear_tq5_row_bytes",
     "bitlinear_pack_weights_tq5",
     "bitlinear_forward_tq5",
@@ -120,6 +124,9 @@ def _load() -> ctypes.CDLL:
     L.bitlinear_forward_ws.restype = i32
     L.bitlinear_quant_forward_ws.argtypes = [P, P, P, i32, i64, i64, i64, P, P, P, P, ctypes.c_uint, P, sz, P]
     L.bitlinear_quant_forward_ws.restype = i32
+    L.bitlinear_quant_forward_requant_ws.argtypes = [P, P, P, i32, i64, i64, i64, P, P, P, P, P, ctypes.c_uint, P,
+                                                     sz, P]
+    L.bitlinear_quant_forward_requant_ws.restype = i32
     L.bitlinear_rmsnorm_quant_forward_ws.argtypes = [P, P, P, i32, i64, i64, i64, P, ctypes.c_float, P, P, P, P,
                                                      ctypes.c_uint, P, sz, P]
     L.bitlinear_rmsnorm_quant_forward_ws.restype = i32
@@ -432,6 +439,46 @@ def bitlinear_quant_forward_ws(W_packed: torch.Tensor, gamma: torch.Tensor, X: t
                                                 _dev(s, "s", torch.float32), acc_ptr, int(flags), ws_ptr, ws_bytes,
                                                 _stream(stream)), "bitlinear_quant_forward_ws")
     return (y, x_q, s, acc) if want_acc else (y, x_q, s)
+
+
+def bitlinear_quant_forward_requant_ws(W_packed: torch.Tensor, gamma: torch.Tensor, X: torch.Tensor,
+                                       y: torch.Tensor | None = None, x_q: torch.Tensor | None = None,
+                                       s: torch.Tensor | None = None, y_q: torch.Tensor | None = None,
+                                       s_y: torch.Tensor | None = None, flags: int = 0,
+                                       workspace: torch.Tensor | None = None, stream=None):
+    """:func:`bitlinear_quant_forward_ws` whose output is also quantised for the
+    next BitLinear: y_q and s_y are :func:`bitlinear_quant_act` of y, bit for
+    bit.  Returns (y, x_q, s, y_q, s_y)."""
+    N, K4 = W_packed.shape
+    M, K = X.shape
+    if K4 * 4 != K:
+        raise ValueError(f"W_packed has K/4 = {K4} but X has K = {K}")
+    if X.dtype == torch.bfloat16:
+        dt = BL_BF16
+    elif X.dtype == torch.float32:
+        dt = BL_F32
+    else:
+        raise ValueError(f"X must be bf16 or fp32, got {X.dtype}")
+    dev = X.device
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    if x_q is None:
+        x_q = torch.empty((M, K), dtype=torch.int8, device=dev)
+    if s is None:
+        s = torch.empty((M,), dtype=torch.float32, device=dev)
+    if y_q is None:
+        y_q = torch.empty((M, N), dtype=torch.int8, device=dev)
+    if s_y is None:
+        s_y = torch.empty((M,), dtype=torch.float32, device=dev)
+    ws_ptr, ws_bytes = _workspace(M, N, K, workspace, dev)
+    _check(get_lib().bitlinear_quant_forward_requant_ws(_dev(W_packed, "W_packed", torch.uint8),
+                                                        _dev(gamma, "gamma", torch.float32), _dev(X, "X"), dt, M, N,
+                                                        K, _dev(y, "y", torch.float32), _dev(x_q, "x_q", torch.int8),
+                                                        _dev(s, "s", torch.float32), _dev(y_q, "y_q", torch.int8),
+                                                        _dev(s_y, "s_y", torch.float32), int(flags), ws_ptr,
+                                                        ws_bytes, _stream(stream)),
+           "bitlinear_quant_forward_requant_ws")
+    return y, x_q, s, y_q, s_y
 
 
 def bitlinear_rmsnorm_quant_forward_ws(W_packed: torch.Tensor, gamma: torch.Tensor, X: torch.Tensor,

@@ -256,6 +256,42 @@ bl_status bitlinear_quant_forward_ws(const uint8_t* W_packed, const float* gamma
   return from_cuda(bl::launch_gemm_f16_sk(a, workspace, d.num_sms, stream));
 }
 
+bl_status bitlinear_quant_forward_requant_ws(const uint8_t* W_packed, const float* gamma, const void* X, bl_dtype dtype,
+                                             int64_t M, int64_t N, int64_t K, float* y, int8_t* x_q, float* s,
+                                             int8_t* y_q, float* s_y, unsigned flags, void* workspace,
+                                             size_t workspace_bytes, cudaStream_t stream) {
+  if (!W_packed || !gamma || !X || !y || !x_q || !s || !y_q || !s_y) return BL_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1) return BL_ERR_INVALID_ARG;
+  if (dtype != BL_F32 && dtype != BL_BF16) return BL_ERR_INVALID_ARG;
+  if (flags & ~BITLINEAR_RELU2) return BL_ERR_INVALID_ARG;
+  if (K % 64 != 0 || K > BITLINEAR_MAX_K || M > INT32_MAX || N > INT32_MAX) return BL_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(W_packed, 16) || !aligned(X, 16) || !aligned(x_q, 16) || !aligned(y, 16) || !aligned(gamma, 4) ||
+      !aligned(s, 4) || !aligned(y_q, 16) || !aligned(s_y, 4))
+    return BL_ERR_MISALIGNED;
+  if (bl_status st = check_workspace(M, N, K, workspace, workspace_bytes)) return st;
+  DeviceInfo d;
+  if (bl_status st = device_info(&d)) return st;
+  bl::ForwardArgs a{W_packed, gamma, x_q, s, M, N, K, y, nullptr, d.err, (flags & BITLINEAR_RELU2) != 0};
+  const bool bf16 = dtype == BL_BF16;
+  cudaError_t e;
+  if (M <= bl::kGemvMaxTokens && K <= bl::kGemvMaxK) {
+    e = bl::launch_gemv_fused(a, X, bf16, x_q, s, false, false, d.num_sms, stream);
+  } else if (bl::gemm_f8_serves(M, N, K)) {
+    e = bl::launch_quant_act_x8(X, bf16, M, K, x_q, s, workspace, d.num_sms, stream);
+    if (e == cudaSuccess) e = bl::launch_gemm_f8(a, workspace, d.num_sms, stream);
+  } else {
+    e = bl::launch_quant_act_x16(X, bf16, M, K, x_q, s, workspace, bl::sk_counters(workspace, M, K, d.num_sms),
+                                 d.num_sms, stream);
+    if (e == cudaSuccess)
+      e = bl::gemm_x16_persistent_serves(M, N, d.num_sms) ? bl::launch_gemm_tc_x16(a, workspace, d.num_sms, stream)
+                                                          : bl::launch_gemm_f16_sk(a, workspace, d.num_sms, stream);
+  }
+  if (e != cudaSuccess) return from_cuda(e);
+  // y is still resident in L2 (at most M x N x 4 bytes, written just now): the
+  // per-token quantisation reads it back from there
+  return from_cuda(bl::launch_quant_act(y, false, M, N, y_q, s_y, d.num_sms, d.err, stream));
+}
+
 bl_status bitlinear_rmsnorm_quant_forward_ws(const uint8_t* W_packed, const float* gamma, const void* X, bl_dtype dtype,
                                              int64_t M, int64_t N, int64_t K, const float* gain, float eps, float* y,
                                              int8_t* x_q, float* s, int32_t* acc, unsigned flags, void* workspace,

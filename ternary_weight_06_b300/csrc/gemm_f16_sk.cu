@@ -3,10 +3,12 @@
 // evenly over all SMs (stream-K), and pairs of SMs share the activation
 // stream by cluster multicast; tcgen05 kind::f16, sm_103a.
 //
-// "unpacks it right next to the math engine, and multiplies it with those
-// little 8-bit bricks" (yousumm.com BitNet b1.58 2B4T transcript): packed
-// weights are read next to the tensor core, expanded, and multiply the fp16
-// image of the int8 activations.
+// The video transcript on yousumm.com (BitNet b1.58 2B4T, the paragraph on
+// running the model on graphics cards) describes the kernel shape: weights
+// travel packed and are expanded only beside the arithmetic units, which
+// multiply them with 8-bit activations.  Here the packed weights are read
+// next to the tensor core, expanded, and multiply the fp16 image of the int8
+// activations.
 //
 // Exactness.  As in every tensor-core path here: ternary weights and int8
 // activations are exact in fp16, every product is an integer of magnitude

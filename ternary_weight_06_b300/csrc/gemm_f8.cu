@@ -1,8 +1,10 @@
 // gemm_f8.cu -- tensor-core BitLinear GEMM on e4m3 operands for skinny token
 // counts (tcgen05 kind::f8f6f4, sm_103a).
 //
-// "unpacks it right next to the math engine, and multiplies it with those
-// little 8-bit bricks" (yousumm.com BitNet b1.58 2B4T transcript): the packed
+// The video transcript on yousumm.com (BitNet b1.58 2B4T, the paragraph on
+// running the model on graphics cards) describes the kernel shape: weights
+// travel packed and are expanded only beside the arithmetic units, which
+// multiply them with 8-bit activations.  Here the packed
 // ternary weights stream from HBM by TMA, are expanded next to the tensor core
 // straight into tensor memory, and multiply 8-bit activation operands.
 //

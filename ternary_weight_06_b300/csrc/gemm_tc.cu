@@ -1,7 +1,9 @@
 // gemm_tc.cu -- tensor-core BitLinear GEMM for many tokens (tcgen05, sm_103a).
 //
-// "unpacks it right next to the math engine, and multiplies it with those
-// little 8-bit bricks" (yousumm.com BitNet b1.58 2B4T transcript): packed
+// The video transcript on yousumm.com (BitNet b1.58 2B4T, the paragraph on
+// running the model on graphics cards) describes the kernel shape: weights
+// travel packed and are expanded only beside the arithmetic units, which
+// multiply them with 8-bit activations.  Here packed
 // ternary tiles and int8 activation tiles are staged in shared memory by TMA,
 // expanded next to the tensor core into an exact MMA operand format, and
 // multiplied by tcgen05.mma with the accumulator in tensor memory.

@@ -1,11 +1,12 @@
 // gemv.cu -- streaming ternary GEMV for a few tokens (decode), with the
 // dequant epilogue fused, and optionally the activation quantisation too.
 //
-// The work is bounded by reading the packed weights from HBM once ("bundles
-// four chips into a single byte, slides that bundle across the GPU highway,
-// unpacks it right next to the math engine": yousumm.com BitNet b1.58 2B4T
-// transcript; memory and bandwidth savings are the measured part: anthology
-// note-168, "The part that is a bet rather than a measurement").
+// The work is bounded by reading the packed weights from HBM once: four
+// weights travel in each byte and are expanded only where they are multiplied
+// (yousumm.com BitNet b1.58 2B4T transcript, the paragraph on running the
+// model on graphics cards); the memory and bandwidth savings are what the
+// method has measured (anthology note-168, "The part that is a bet rather
+// than a measurement").
 //
 // Layout of the work:
 //   * up to two CTAs per SM; each owns a contiguous block of output rows.

@@ -54,8 +54,9 @@ cudaError_t launch_pack_tq5(const float* W, int64_t N, int64_t K, int64_t pitch,
 cudaError_t launch_quant_act(const void* X, bool bf16, int64_t M, int64_t K, int8_t* xq, float* s, int num_sms,
                              uint32_t* err, cudaStream_t stream);
 
-// Sub-layer RMS normalisation folded into the quantisation: x_q = quant(X * gain),
-// s = s(X * gain) * sqrt(mean(X^2) + eps).  gain may be null (all ones).
+// Sub-layer RMS normalisation, then the quantisation: r = fp32 sqrt(fp32(ms + eps))
+// with ms the exact mean of X^2 rounded once, x_n = fp32(fp32(X * gain) / r), and
+// x_q, s the per-token quantisation of x_n.  gain may be null (all ones).
 cudaError_t launch_rmsnorm_quant_act(const void* X, bool bf16, int64_t M, int64_t K, const float* gain, float eps,
                                      int8_t* xq, float* s, cudaStream_t stream);
 

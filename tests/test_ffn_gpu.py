@@ -232,3 +232,60 @@ def test_ffn_chain_one_call_second_bitlinear(bl, M):
     assert torch.equal(hs1.view(torch.int32), hs.view(torch.int32))
     assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
     bl.bitlinear_check_device_error()
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 300, 1024), (4, 999, 2560), (3, 260, 40000), (16, 1000, 2560),
+                                   (64, 700, 8192 + 64), (97, 2002, 640), (176, 3000, 8192), (2048, 4800, 128)])
+@pytest.mark.parametrize("relu2", [False, True])
+def test_quant_forward_requant_every_path(bl, M, N, K, relu2):
+    """y quantised for the next BitLinear in the same call, on each route (fused GEMV; fp8 GEMM, also for a few tokens
+    with K past the GEMV's limit; stream-K GEMM; persistent GEMM): y_q and s_y
+    bit-exact against the oracle's per-token quantisation of the oracle's y;
+    y, x_q and s bit-exact too.  Rows: an all-zero token (clamped scale), a
+    large one and a tiny one whose squared output underflows to zero."""
+    rng = np.random.default_rng(M * 11 + N + K)
+    p = oracle.pack(rng.integers(-1, 2, size=(N, K)).astype(np.int8))
+    X = torch.randn((M, K), generator=torch.Generator().manual_seed(M + 3 * K)) * 2.0
+    X[0] = 0.0
+    if M > 2:
+        X[M // 2] *= 1e12
+        X[M - 1] *= 1e-30
+    X = X.to(torch.bfloat16)
+    xq_ref, s_ref = oracle.quant_act(X.to(torch.float32).numpy(), omp=True)
+    y_ref, _ = oracle.forward(p, np.float32(0.05), xq_ref, s_ref, K, omp=True)
+    if relu2:
+        y_ref = oracle.relu2(y_ref)
+    yq_ref, sy_ref = oracle.quant_act(y_ref, omp=True)
+    y, xq, s, yq, sy = bl.bitlinear_quant_forward_requant_ws(torch.from_numpy(p).cuda(), torch.tensor([0.05]).cuda(),
+                                                             X.cuda(), flags=bl.BITLINEAR_RELU2 if relu2 else 0)
+    torch.cuda.synchronize()
+    assert np.array_equal(xq.cpu().numpy(), xq_ref)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(y.cpu().numpy().view(np.uint32), y_ref.view(np.uint32))
+    assert np.array_equal(sy.cpu().numpy().view(np.uint32), sy_ref.view(np.uint32)), "s_y must be bit-exact"
+    assert np.array_equal(yq.cpu().numpy(), yq_ref), "y_q must be bit-exact"
+    bl.bitlinear_check_device_error()
+
+
+@pytest.mark.parametrize("M", [1, 16, 176])
+def test_ffn_chain_requant_feeds_second_bitlinear(bl, M):
+    """the up projection's squared-ReLU output quantised in its own call feeds
+    the down projection's bitlinear_forward_ws and gives the y of the chain
+    that quantises h in a separate bitlinear_quant_act call, bit for bit"""
+    rng = np.random.default_rng(300 + M)
+    D, H = 512, 1536
+    Wu = torch.from_numpy(oracle.pack(rng.integers(-1, 2, size=(H, D)).astype(np.int8))).cuda()
+    Wd = torch.from_numpy(oracle.pack(rng.integers(-1, 2, size=(D, H)).astype(np.int8))).cuda()
+    gu, gd = torch.tensor([0.03]).cuda(), torch.tensor([0.02]).cuda()
+    X = torch.randn((M, D), generator=torch.Generator().manual_seed(11)).to(torch.bfloat16).cuda()
+    h, _, _ = bl.bitlinear_quant_forward_ws(Wu, gu, X, flags=bl.BITLINEAR_RELU2)
+    hq, hs = bl.bitlinear_quant_act(h)
+    y2 = bl.bitlinear_forward_ws(Wd, gd, hq, hs)
+    h1, _, _, hq1, hs1 = bl.bitlinear_quant_forward_requant_ws(Wu, gu, X, flags=bl.BITLINEAR_RELU2)
+    y1 = bl.bitlinear_forward_ws(Wd, gd, hq1, hs1)
+    torch.cuda.synchronize()
+    assert torch.equal(h1.view(torch.int32), h.view(torch.int32))
+    assert torch.equal(hq1, hq)
+    assert torch.equal(hs1.view(torch.int32), hs.view(torch.int32))
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
+    bl.bitlinear_check_device_error()
