@@ -170,36 +170,58 @@ __device__ __forceinline__ void convert_x16_f16(uint4 v, uint32_t* h /* 8 words 
 // ---- e4m3 activation operand of the fp8 GEMM (shared by the GEMM's prepass
 // and the activation quantisation, which can write the operand directly)
 
-// e4m3 bits of an integer v with |v| <= 128 and at most four significant bits
-// (l in [0, 15], or 16 h with |h| <= 8): exponent from the top bit, the three
-// bits below it as the mantissa.
-__device__ __forceinline__ uint32_t e4m3_small(int v) {
+// e4m3 bits of v * 2^-d for an integer v with 1 <= |v| <= 15 (or 0) and
+// d in {0, 2}: exponent from the top bit, the three bits below it as the
+// mantissa; every such value is a normal e4m3 number, exactly.
+__device__ __forceinline__ uint32_t e4m3_small(int v, int d) {
   if (v == 0) return 0u;
   const uint32_t s = v < 0 ? 0x80u : 0u;
   const uint32_t a = (uint32_t)(v < 0 ? -v : v);
   const uint32_t e = 31u - __clz(a);
-  return s | ((e + 7u) << 3) | (((a << 3) >> e) & 7u);
+  return s | ((e + 7u - (uint32_t)d) << 3) | (((a << 3) >> e) & 7u);
 }
 
 // 16 int8 activations (natural k order, 4 words) -> the token's two e4m3
-// operand rows of the fp8 GEMM, 16 h and l (x = 16 h + l, h = x >> 4,
-// l = x & 15), 16 bytes each, in the k order [0, 2, ..., 14, 1, ..., 15].
+// operand rows of the fp8 GEMM, h and l (x = 16 h + l, h = x >> 4 in
+// [-8, 7], l = x & 15), 16 bytes each.  Position p = 4 i + j of a row holds
+// k = 4 j + i: the order in which the GEMM expands a packed weight word by
+// masks.  The weight bytes at odd i carry 4 c (the code shifted by two bits),
+// so the activation there is h / 4 or l / 4 (exact in e4m3).
 __device__ __forceinline__ void x8_rows16(uint4 v, uint4* hi, uint4* lo) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   uint32_t H[4] = {0u, 0u, 0u, 0u}, L[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
   for (int k = 0; k < 16; ++k) {
     const int x = (int)(int8_t)((w[k >> 2] >> (8 * (k & 3))) & 0xffu);
-    const int p = (k & 1) ? 8 + (k >> 1) : (k >> 1);  // position of k in the operand order
-    H[p >> 2] |= e4m3_small(16 * (x >> 4)) << (8 * (p & 3));
-    L[p >> 2] |= e4m3_small(x & 15) << (8 * (p & 3));
+    const int i = k & 3, j = k >> 2, d = (i & 1) ? 2 : 0;  // word i, byte j of the row's 16 bytes
+    H[i] |= e4m3_small(x >> 4, d) << (8 * j);
+    L[i] |= e4m3_small(x & 15, d) << (8 * j);
   }
   *hi = make_uint4(H[0], H[1], H[2], H[3]);
   *lo = make_uint4(L[0], L[1], L[2], L[3]);
 }
 
+// Sum of the 16 int8 values of a group (4 words).
+__device__ __forceinline__ int sum16_i8(uint4 v) {
+  return __dp4a((int)v.w, 0x01010101, __dp4a((int)v.z, 0x01010101, __dp4a((int)v.y, 0x01010101, __dp4a((int)v.x, 0x01010101, 0))));
+}
+
+// The sum of v over the CTA, written by thread 0 to *dst.  Every thread of
+// the CTA calls it once (blockDim.x a multiple of 32).
+__device__ __forceinline__ void block_sum_store(int v, int32_t* dst) {
+  __shared__ int part[32];
+  v = __reduce_add_sync(0xffffffffu, v);
+  if ((threadIdx.x & 31u) == 0u) part[threadIdx.x >> 5] = v;
+  __syncthreads();
+  if (threadIdx.x < 32u) {
+    int w = threadIdx.x < (blockDim.x >> 5) ? part[threadIdx.x] : 0;
+    w = __reduce_add_sync(0xffffffffu, w);
+    if (threadIdx.x == 0u) *dst = w;
+  }
+}
+
 // Tiled layout of that operand: blocks of BN tokens x kX8Block k, each block
-// NB = 2 BN rows (16 h and l of every token) of kX8Block bytes stored as four
+// NB = 2 BN rows (h and l of every token) of kX8Block bytes stored as four
 // 128-byte-wide boxes [NB rows][128 B] one after another, with the 128-byte
 // swizzle of the MMA's shared-memory operands applied (16-byte chunk c of row
 // j at chunk c ^ (j & 7)); block (token tile mt, k-block kb) starts at byte
@@ -208,8 +230,13 @@ __device__ __forceinline__ void x8_rows16(uint4 v, uint4* hi, uint4* lo) {
 // past K are zero.
 constexpr int kX8Block = 512;
 
+// Every token's sum of activations comes in partial sums over 4096-k chunks
+// (the last one short): x8_sum_parts(K) int32 per token, token-major.
+constexpr int kX8SumK = 4096;
+__host__ __device__ __forceinline__ int x8_sum_parts(int64_t K) { return (int)((K + kX8SumK - 1) / kX8SumK); }
+
 // Byte offset of the 16-byte group of k = k16 .. k16 + 15 (k16 % 16 == 0) in
-// row hl (0: 16 h, 1: l) of token m.
+// row hl (0: h, 1: l) of token m.
 __device__ __forceinline__ size_t x8_group_offset(int64_t m, int64_t k16, int hl, int BN, int64_t nkb) {
   const int64_t mt = m / BN, kb = k16 / kX8Block;
   const int t = (int)(m - mt * BN), kk = (int)(k16 - kb * kX8Block);

@@ -141,18 +141,6 @@ __device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
 
 // Position in a ring of n slots: the slot and the parity of its current
 // phase, advanced by `by` slots at a time (no division on the hot loops).
-struct RingPos {
-  int idx;
-  uint32_t ph;
-  __device__ __forceinline__ void step(int by, int n) {
-    idx += by;
-    while (idx >= n) {
-      idx -= n;
-      ph ^= 1u;
-    }
-  }
-};
-
 // Cluster whose range holds flattened unit i: begin(c) = floor(c U / C) <= i.
 __device__ __forceinline__ int cluster_of(int64_t i, int64_t U, int C) { return (int)(((i + 1) * C + U - 1) / U) - 1; }
 

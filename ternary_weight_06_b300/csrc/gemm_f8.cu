@@ -14,26 +14,33 @@
 // K = 32 per instruction against 16 for kind::f16, and its operands are half
 // the bytes.
 //
-// Exactness.  -1, 0 and +1 are e4m3 values.  An int8 activation x in
-// [-128, 127] is split as x = 16 h + l with h = x >> 4 in [-8, 7] and
-// l = x & 15 in [0, 15]; 16 h and l both have at most four significant bits,
-// so both are e4m3 values.  Every token contributes two operand rows (16 h
-// and l), every product is an integer of magnitude <= 128, and every partial
-// sum of either row is an integer of magnitude <= 128 K <= 2^24 (K <= 131072),
-// exact in the fp32 accumulator; acc = D(16 h row) + D(l row) is one exact
-// fp32 add.  The test-suite drives |acc| to 2^24.
+// Weights by masks.  A byte b <= 15 read as e4m3 is exactly b * 2^-9 (the
+// subnormals and the first binade are evenly spaced).  So a packed word P of
+// 16 codes c = W_q + 1 in {0, 1, 2} becomes weight operand bytes with two
+// masks and one shift: P & 0x03030303 holds the codes k = 0, 4, 8, 12 as
+// c * 2^-9, P & 0x0C0C0C0C the codes k = 1, 5, 9, 13 as 4 c * 2^-9, and the
+// same two masks of P >> 4 the codes k = 2, 6, ... and 3, 7, ...  The operand
+// weights are then linear in c, and the epilogue subtracts the token's sum of
+// activations: sum (c - 1) x = sum c x - sum x.
+//
+// Exactness.  An int8 activation x is split as x = 16 h + l with h = x >> 4
+// in [-8, 7] and l = x & 15 in [0, 15]; every token contributes two operand
+// rows, h and l, divided by 4 at the positions whose weight byte carries 4 c,
+// all exact e4m3 values.  Every product is c h 2^-9 or c l 2^-9, so each row
+// of D is 2^-9 times an integer of magnitude <= 30 K <= 2^22 (K <= 131072),
+// exact in the fp32 accumulator, and the epilogue forms
+// acc = 16 (2^9 D_h) + 2^9 D_l - sum x in int32, exactly.
 //
 // Operand order.  Within every group of 16 consecutive k, both operands hold
-// the k in the order [0, 2, 4, ..., 14, 1, 3, ..., 15]: that is the order in
-// which four byte permutes expand a packed word of 16 codes (below), and a sum
-// over k does not depend on it.
+// the k in the order p = 4 i + j <-> k = 4 j + i (word i, byte j of the
+// expanded word), and a sum over k does not depend on it.
 //
-// Work split (stream-K).  The (output tile, 256-k block) pairs of the problem,
+// Work split (stream-K).  The (output tile, 512-k block) pairs of the problem,
 // tile-major, are cut into G equal contiguous ranges, one per CTA (one CTA
 // per SM), so every SM streams the same number of weight bytes.  A tile whose
 // k-blocks all fall in one range is finished in tensor memory.  A tile cut by
 // range boundaries is reduced exactly: each contributor stores its partial
-// sums (integers, exact in fp32) to its own slot of the workspace, then adds
+// sums (int32) to its own slot of the workspace, then adds
 // its k-block count to the tile's counter; the contributor that completes the
 // count adds the other slots to its own sums and writes y.
 //
@@ -64,7 +71,6 @@ constexpr int kWProdWarp = 0, kMma0Warp = 1, kMma1Warp = 2, kXProdWarp = 3;
 constexpr int kConvWarp0 = 4, kConvWarps = 8;  // two per tensor-memory lane quarter, each half of a slot's columns
 constexpr int kEpiWarp0 = kConvWarp0 + kConvWarps, kEpiWarps = 4;
 constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
-constexpr uint32_t kE4m3Lut = 0x003800B8u;        // bytes 0, 1, 2: e4m3 of code - 1 = -1, 0, +1
 constexpr size_t kF8SmemBudget = 220 * 1024;      // dynamic shared memory per CTA
 
 struct F8Cfg {
@@ -74,12 +80,14 @@ struct F8Cfg {
   int32_t* acc;
   uint32_t* err;
   const uint8_t* x8;  // tiled activation operand (see x8_group_offset)
-  float* part;    // partial-sum slots: [2 * G][BN][kBM]
+  const int32_t* sx;  // per token: x8_sum_parts(K) partial sums of its int8 activations
+  int32_t* part;  // partial-sum slots: [2 * G][BN][kBM]
   uint32_t* cnt;  // arrival counters of cut tiles: [G], zero at entry
   int M, N, K, BN, nw, nx, ni, ntn, nkb, G;  // nw, nx: ring depths; ni: MMA-issuing warps (1 or 2)
   int na, acol;  // expanded-weight slots and their first tensor-memory column
   int64_t units;  // output tiles * nkb
   int relu2;
+  int nsx;  // partial sums per token in sx
 };
 
 __device__ __forceinline__ void mma_f8_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
@@ -91,16 +99,14 @@ __device__ __forceinline__ void mma_f8_tmem_a(uint32_t d_tmem, uint32_t a_tmem, 
       : "memory");
 }
 
-// 16 codes (one packed word, k = 0..15 at bits 2k) -> 16 e4m3 bytes of
-// code - 1 in the order [0, 2, ..., 14, 1, 3, ..., 15]: the low three bits of
-// each selector nibble index the table bytes (the top bit, sign replication,
-// is always clear: codes are at most 2).
+// 16 codes (one packed word, k = 0..15 at bits 2k) -> 16 e4m3 bytes, word i
+// byte j holding code k = 4 j + i as c * 2^-9 (i even) or 4 c * 2^-9 (i odd).
 __device__ __forceinline__ void expand16(uint32_t P, uint32_t* o) {
-  const uint32_t X = P & 0x33333333u, Y = (P >> 2) & 0x33333333u;
-  o[0] = __byte_perm(kE4m3Lut, 0u, X);
-  o[1] = __byte_perm(kE4m3Lut, 0u, X >> 16);
-  o[2] = __byte_perm(kE4m3Lut, 0u, Y);
-  o[3] = __byte_perm(kE4m3Lut, 0u, Y >> 16);
+  const uint32_t T = P >> 4;
+  o[0] = P & 0x03030303u;
+  o[1] = P & 0x0C0C0C0Cu;
+  o[2] = T & 0x03030303u;
+  o[3] = T & 0x0C0C0C0Cu;
 }
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 2, %0;" ::"n"(32 * kEpiWarps) : "memory"); }
@@ -123,7 +129,7 @@ __device__ __forceinline__ int cta_of(int64_t i, int64_t U, int G) { return (int
 __global__ void __launch_bounds__(kThreads, 1) gemm_f8_kernel(const __grid_constant__ CUtensorMap tmap_w, const F8Cfg c) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int BN = c.BN, NB = 2 * BN;  // MMA N: a 16 h row and an l row per token
+  const int BN = c.BN, NB = 2 * BN;  // MMA N: an h row and an l row per token
   const int NW = c.nw, NX = c.nx, NI = c.ni, NA = c.na;
   const int b_box = NB * 128;         // one 128-byte-wide box of the activation operand
   const int b_bytes = NB * kKB;       // a k-block's activation block: four boxes
@@ -143,6 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f8_kernel(const __grid_const
   volatile uint32_t* abort_flag = tmem_slot + 1;
   volatile uint32_t* last_flag = tmem_slot + 2;
   float* tscale = reinterpret_cast<float*>(tmem_slot + 4);  // [2][kF8MaxTile]
+  int* tsum = reinterpret_cast<int*>(tscale + 2 * kF8MaxTile);  // [2][kF8MaxTile]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t U = c.units;
@@ -189,9 +196,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f8_kernel(const __grid_const
       int st = 0, issued = 0;
       uint32_t ph = 0;
       bool ok = true;
+      // (token tile mt, feature tile tn, k-block kb) of unit i, stepped without division
+      const int64_t t0 = begin / c.nkb;
+      int kb = (int)(begin - t0 * c.nkb), tn = (int)(t0 % c.ntn);
+      int64_t mt = t0 / c.ntn;
       for (int64_t i = begin; i < end && ok; ++i) {
-        const int64_t t = i / c.nkb;
-        const int kb = (int)(i - t * c.nkb);
         for (int sub = 0; sub < (wprod ? 1 : kKB / kSub); ++sub) {
           if (!wait_warp(&empty[st], ph ^ 1u, c.err, abort_flag)) {
             ok = false;
@@ -200,9 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f8_kernel(const __grid_const
           if (elect_one()) {
             if (wprod) {
               mbar_arrive_expect_tx(&full[st], (uint32_t)kWStage);
-              tma_load_2d(wring + st * kWStage, &tmap_w, kb * (kKB / 4), (int)(t % c.ntn) * kBM, &full[st]);
+              tma_load_2d(wring + st * kWStage, &tmap_w, kb * (kKB / 4), tn * kBM, &full[st]);
             } else {
-              const int64_t mt = t / c.ntn;
               mbar_arrive_expect_tx(&full[st], (uint32_t)x_bytes);
               bulk_g2s(xring + st * x_bytes,
                        c.x8 + ((size_t)mt * c.nkb + kb) * (size_t)b_bytes + (size_t)sub * x_bytes, (uint32_t)x_bytes,
@@ -214,6 +222,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f8_kernel(const __grid_const
           if (++st == NS) {
             st = 0;
             ph ^= 1u;
+          }
+        }
+        if (++kb == c.nkb) {
+          kb = 0;
+          if (++tn == c.ntn) {
+            tn = 0;
+            ++mt;
           }
         }
       }
@@ -236,7 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f8_kernel(const __grid_const
       const uint32_t idesc = f16_idesc(kBM, NB);  // format fields 0: E4M3 operands under kind::f8f6f4
       const uint64_t box_step = (uint64_t)(b_box >> 4);  // one activation box in the descriptor's address field
       int lt = 0;
-      int gsub = 0;  // sequence number of the next sub-block (both sub-blocks counted): its A slot and x stage
+      // this issuer's sub-blocks are q, q + NI, q + 2 NI, ... of the CTA's sequence: their A slots and x stages
+      RingPos ap{q, 0u}, xp{q, 0u};
       bool ok = true;
       for (int64_t i = begin; i < end && ok; ++lt) {
         const int64_t t = i / c.nkb;
@@ -247,12 +263,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f8_kernel(const __grid_const
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)((b * NI + q) * NB);
         uint32_t accum = 0u;  // the segment's first MMA overwrites the accumulator
-        for (int kb = kb0; kb < kb1 && ok; ++kb, gsub += kKB / kSub) {
+        for (int kb = kb0; kb < kb1 && ok; ++kb) {
           for (int sub = q; sub < kKB / kSub; sub += NI) {
-            const int g = gsub + sub;
-            const int as = g % NA, xs = g % NX;
-            if (!wait_warp(&x_full[xs], (uint32_t)(g / NX) & 1u, c.err, abort_flag) ||
-                !wait_warp(&a_full[as], (uint32_t)(g / NA) & 1u, c.err, abort_flag)) {
+            const int as = ap.idx, xs = xp.idx;
+            if (!wait_warp(&x_full[xs], xp.ph, c.err, abort_flag) || !wait_warp(&a_full[as], ap.ph, c.err, abort_flag)) {
               ok = false;
               break;
             }
@@ -274,6 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f8_kernel(const __grid_const
             }
             __syncwarp();
             accum = 1u;
+            ap.step(NI, NA);
+            xp.step(NI, NX);
           }
         }
         if (ok && elect_one()) mma_commit(&acc_full[b]);
@@ -358,34 +374,41 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f8_kernel(const __grid_const
       const int b = lt & 1;
       const int n0 = (int)(t % c.ntn) * kBM, m0 = (int)(t / c.ntn) * BN;
       float* ts = tscale + b * kF8MaxTile;
+      int* tx = tsum + b * kF8MaxTile;
       for (int j = et; j < BN; j += 32 * kEpiWarps) {
         const int m = m0 + j;
         ts[j] = m < c.M ? __fdiv_rn(gamma, __ldg(c.s + m)) : 0.0f;
+        int sum = 0;
+        if (m < c.M)
+          for (int pc = 0; pc < c.nsx; ++pc) sum += __ldg(c.sx + (int64_t)m * c.nsx + pc);
+        tx[j] = sum;
       }
       const bool got = wait_flag(&acc_full[b], (uint32_t)(lt >> 1) & 1u, c.err, abort_flag);
       if (epi_bar_or(!got)) break;  // the scales above are visible, and every warp agrees
       tc_fence_after();
       const int n = n0 + r;
       const bool whole = kb0 == 0 && kb1 == c.nkb;
-      // acc of tokens j0 .. j0 + 15: the 16 h and l rows of every issuer's accumulator (exact fp32 adds)
-      auto load_acc16 = [&](int j0, float (&a)[16]) {
+      // sum c x of tokens j0 .. j0 + 15 from the h and l rows of every issuer's
+      // accumulator: 16 (2^9 D_h) + 2^9 D_l, each 2^9 D an exact integer
+      auto load_acc16 = [&](int j0, int (&a)[16]) {
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) a[jj] = 0.0f;
+        for (int jj = 0; jj < 16; ++jj) a[jj] = 0;
         for (int qi = 0; qi < NI; ++qi) {
           uint32_t v[32];
           tmem_ld32(lane_base + (uint32_t)((b * NI + qi) * NB + 2 * j0), v);
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj)
-            a[jj] = __fadd_rn(a[jj], __fadd_rn(__uint_as_float(v[2 * jj]), __uint_as_float(v[2 * jj + 1])));
+            a[jj] += 16 * __float2int_rn(__fmul_rn(__uint_as_float(v[2 * jj]), 512.0f)) +
+                     __float2int_rn(__fmul_rn(__uint_as_float(v[2 * jj + 1]), 512.0f));
         }
       };
       bool last = whole;
       const int my_slot = 2 * (int)blockIdx.x + ((int)t == first_tile ? 0 : 1);
       if (!whole) {
         // store this CTA's partial sums, then count the tile's k-blocks
-        float* slot = c.part + (size_t)my_slot * (BN * kBM);
+        int32_t* slot = c.part + (size_t)my_slot * (BN * kBM);
         for (int j0 = 0; j0 < BN; j0 += 16) {
-          float a[16];
+          int a[16];
           load_acc16(j0, a);
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) slot[(j0 + jj) * kBM + r] = a[jj];
@@ -404,14 +427,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f8_kernel(const __grid_const
       if (last) {
         const int clo = whole ? 0 : cta_of(t * c.nkb, U, c.G), chi = whole ? -1 : cta_of((t + 1) * c.nkb - 1, U, c.G);
         for (int j0 = 0; j0 < BN; j0 += 16) {
-          float a[16];
+          int a[16];
           load_acc16(j0, a);
           for (int cc = clo; cc <= chi; ++cc) {
             if (cc == (int)blockIdx.x) continue;
             const int ctile = (int)(((int64_t)cc * U / c.G) / c.nkb);  // first tile of CTA cc
-            const float* slot = c.part + (size_t)(2 * cc + (ctile == (int)t ? 0 : 1)) * (BN * kBM);
+            const int32_t* slot = c.part + (size_t)(2 * cc + (ctile == (int)t ? 0 : 1)) * (BN * kBM);
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) a[jj] = __fadd_rn(a[jj], __ldcg(slot + (j0 + jj) * kBM + r));
+            for (int jj = 0; jj < 16; ++jj) a[jj] += __ldcg(slot + (j0 + jj) * kBM + r);
           }
           if (n < c.N) {
 #pragma unroll
@@ -419,8 +442,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f8_kernel(const __grid_const
               const int m = m0 + j0 + jj;
               if (m < c.M) {
                 const int64_t o = (int64_t)m * c.N + n;
-                c.y[o] = out_act(__fmul_rn(a[jj], ts[j0 + jj]), c.relu2);
-                if (c.acc) c.acc[o] = __float2int_rn(a[jj]);
+                const int v = a[jj] - tx[j0 + jj];  // sum (c - 1) x
+                c.y[o] = out_act(__fmul_rn(__int2float_rn(v), ts[j0 + jj]), c.relu2);
+                if (c.acc) c.acc[o] = v;
               }
             }
           }
@@ -440,23 +464,29 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f8_kernel(const __grid_const
 
 // ---------------------------------------------------------------- activation operand from x_q
 
-// The tiled activation operand from x_q: one thread per 16-k group of one
-// token row, over every token tile and k-block (rows past M and k past K
-// written as zeros); block 0 also zeroes the arrival counters.
+// The tiled activation operand from x_q: CTA (c, m) writes the 16-k groups
+// of 4096-k chunk c of token row m (rows past M and k past K as zeros) and
+// that chunk's sum of activations; CTA (0, 0) also zeroes the arrival
+// counters.  256 threads, one group each.
 __global__ void __launch_bounds__(256) x8_prepass_kernel(const uint4* __restrict__ xq, int64_t M, int64_t K, int BN,
                                                          int64_t nkb, uint8_t* __restrict__ x8,
-                                                         uint32_t* __restrict__ cnt, int ncnt) {
-  if (blockIdx.x == 0)
+                                                         int32_t* __restrict__ sx, uint32_t* __restrict__ cnt,
+                                                         int ncnt) {
+  if (blockIdx.x == 0 && blockIdx.y == 0)
     for (int i = threadIdx.x; i < ncnt; i += blockDim.x) cnt[i] = 0u;
-  const int64_t Mp = (M + BN - 1) / BN * BN, gpr = nkb * (kX8Block / 16), ngroups = Mp * gpr;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < ngroups; g += stride) {
-    const int64_t m = g / gpr, j = g - m * gpr;
+  const int64_t m = blockIdx.y, j = (int64_t)blockIdx.x * (kX8SumK / 16) + threadIdx.x;
+  int sum = 0;
+  if (j < nkb * (kX8Block / 16)) {
     uint4 hi = make_uint4(0u, 0u, 0u, 0u), lo = hi;
-    if (m < M && j < K / 16) x8_rows16(__ldg(xq + m * (K / 16) + j), &hi, &lo);
+    if (m < M && j < K / 16) {
+      const uint4 v = __ldg(xq + m * (K / 16) + j);
+      x8_rows16(v, &hi, &lo);
+      sum = sum16_i8(v);
+    }
     *reinterpret_cast<uint4*>(x8 + x8_group_offset(m, 16 * j, 0, BN, nkb)) = hi;
     *reinterpret_cast<uint4*>(x8 + x8_group_offset(m, 16 * j, 1, BN, nkb)) = lo;
   }
+  block_sum_store(sum, sx + m * gridDim.x + blockIdx.x);
 }
 
 }  // namespace
@@ -481,41 +511,49 @@ size_t x8_bytes(int64_t M, int64_t K) {
 
 struct F8Layout {
   uint8_t* x8;
-  float* part;
+  int32_t* part;
   uint32_t* cnt;
+  int32_t* sx;
 };
+
+int64_t padded_tokens(int64_t M) {
+  const int BN = gemm_f8_token_tile(M);
+  return (M + BN - 1) / BN * BN;
+}
 
 F8Layout f8_layout(void* ws, int64_t M, int64_t K, int num_sms) {
   uint8_t* p = static_cast<uint8_t*>(ws);
   F8Layout l;
   l.x8 = p;
   p += (x8_bytes(M, K) + 255) / 256 * 256;
-  l.part = reinterpret_cast<float*>(p);
-  p += (size_t)2 * num_sms * gemm_f8_token_tile(M) * kBM * sizeof(float);
+  l.part = reinterpret_cast<int32_t*>(p);
+  p += (size_t)2 * num_sms * gemm_f8_token_tile(M) * kBM * sizeof(int32_t);
   l.cnt = reinterpret_cast<uint32_t*>(p);
+  p += ((size_t)num_sms * sizeof(uint32_t) + 255) / 256 * 256;
+  l.sx = reinterpret_cast<int32_t*>(p);
   return l;
 }
 
 }  // namespace
 
 size_t gemm_f8_workspace_bytes(int64_t M, int64_t K, int num_sms) {
-  return (x8_bytes(M, K) + 255) / 256 * 256 + (size_t)2 * num_sms * gemm_f8_token_tile(M) * kBM * sizeof(float) +
-         ((size_t)num_sms * sizeof(uint32_t) + 255) / 256 * 256;
+  return (x8_bytes(M, K) + 255) / 256 * 256 + (size_t)2 * num_sms * gemm_f8_token_tile(M) * kBM * sizeof(int32_t) +
+         ((size_t)num_sms * sizeof(uint32_t) + 255) / 256 * 256 +
+         ((size_t)padded_tokens(M) * x8_sum_parts(K) * sizeof(int32_t) + 255) / 256 * 256;
 }
 
 cudaError_t launch_x8_prepass(const int8_t* xq, int64_t M, int64_t K, void* ws, int num_sms, cudaStream_t stream) {
   const F8Layout l = f8_layout(ws, M, K, num_sms);
   const int BN = gemm_f8_token_tile(M);
   const int64_t nkb = gemm_f8_kblocks(K);
-  const int64_t ngroups = (M + BN - 1) / BN * BN * nkb * (kX8Block / 16);
-  const int64_t want = (ngroups + 255) / 256;
-  const int grid = (int)(want < (int64_t)num_sms * 8 ? (want ? want : 1) : (int64_t)num_sms * 8);
-  x8_prepass_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint4*>(xq), M, K, BN, nkb, l.x8, l.cnt,
-                                               num_sms);
+  const dim3 grid((unsigned)x8_sum_parts(K), (unsigned)padded_tokens(M));
+  x8_prepass_kernel<<<grid, kX8SumK / 16, 0, stream>>>(reinterpret_cast<const uint4*>(xq), M, K, BN, nkb, l.x8, l.sx,
+                                                      l.cnt, num_sms);
   return cudaGetLastError();
 }
 
 uint32_t* f8_counters(void* ws, int64_t M, int64_t K, int num_sms) { return f8_layout(ws, M, K, num_sms).cnt; }
+int32_t* f8_sums(void* ws, int64_t M, int64_t K, int num_sms) { return f8_layout(ws, M, K, num_sms).sx; }
 uint8_t* f8_operand(void* ws) { return static_cast<uint8_t*>(ws); }
 
 cudaError_t launch_gemm_f8(const ForwardArgs& a, void* ws, int num_sms, cudaStream_t stream) {
@@ -540,15 +578,15 @@ cudaError_t launch_gemm_f8(const ForwardArgs& a, void* ws, int num_sms, cudaStre
   int NX = (int)((96 * 1024) / xstage);  // the activation blocks come from L2: a short ring
   if (NX > kMaxXStages) NX = kMaxXStages;
   if (NX < 2) NX = 2;
-  const size_t fixed = 1024 + (2 * kMaxWStages + 2 * kMaxXStages + 2 * kMaxASlots + 6) * 8 + 16 + 2 * kF8MaxTile * 4;
+  const size_t fixed = 1024 + (2 * kMaxWStages + 2 * kMaxXStages + 2 * kMaxASlots + 6) * 8 + 16 + 4 * kF8MaxTile * 4;
   int NW = (int)((kF8SmemBudget - fixed - NX * xstage) / kWStage);
   if (NW > kMaxWStages) NW = kMaxWStages;
   if (NW < 2) return cudaErrorInvalidValue;
   const size_t smem = fixed + (size_t)NW * kWStage + (size_t)NX * xstage;
   cudaError_t e = cudaFuncSetAttribute(gemm_f8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  F8Cfg c{a.gamma, a.s, a.y, a.acc, a.err, l.x8, l.part, l.cnt, (int)a.M, (int)a.N, (int)a.K, BN, NW, NX, NI, ntn, nkb,
-          G, NA, acol, units, a.relu2 ? 1 : 0};
+  F8Cfg c{a.gamma, a.s, a.y, a.acc, a.err, l.x8, l.sx, l.part, l.cnt, (int)a.M, (int)a.N, (int)a.K, BN, NW, NX, NI, ntn, nkb,
+          G, NA, acol, units, a.relu2 ? 1 : 0, x8_sum_parts(a.K)};
   gemm_f8_kernel<<<G, kThreads, smem, stream>>>(tw, c);
   return cudaGetLastError();
 }

@@ -114,7 +114,8 @@ constexpr int64_t kTq5MaxK = 40960;  // 16 K slices x 32 lanes x 4 words x 20 we
 // of at most kF8MaxTile), through a
 // workspace of gemm_f8_workspace_bytes(M, K, num_sms) bytes (16-byte aligned)
 // that holds the e4m3 activation operand (2 rows per token), partial-sum
-// slots and arrival counters.  The operand and the zeroed counters come from
+// slots, arrival counters and every token's sum of activations.  The
+// operand, the sums and the zeroed counters come from
 // launch_x8_prepass (from x_q) or launch_quant_act_x8 (from X), in stream
 // order before launch_gemm_f8.
 constexpr int64_t kF8MaxTokens = 64;  // the kernel handles up to 2 tiles of 96; past 64 tokens the f16 GEMM is faster
@@ -126,6 +127,7 @@ size_t gemm_f8_workspace_bytes(int64_t M, int64_t K, int num_sms);
 cudaError_t launch_x8_prepass(const int8_t* xq, int64_t M, int64_t K, void* ws, int num_sms, cudaStream_t stream);
 cudaError_t launch_gemm_f8(const ForwardArgs& a, void* ws, int num_sms, cudaStream_t stream);
 uint32_t* f8_counters(void* ws, int64_t M, int64_t K, int num_sms);
+int32_t* f8_sums(void* ws, int64_t M, int64_t K, int num_sms);  // per token (padded): the sum of its activations
 uint8_t* f8_operand(void* ws);
 // The per-token quantisation, also writing the fp8 operand (and zeroing the
 // counters) of the workspace; K % 16 == 0.

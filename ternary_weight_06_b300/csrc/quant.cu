@@ -43,6 +43,7 @@ struct X8Out {
   int ncnt;
   int64_t M, nkb;
   int BN;
+  int32_t* sx;  // OUT == 2: every token's x8_sum_parts(K) partial sums of int8 activations (0 for padding tokens)
 };
 
 // OUT: 0 x_q and s only; 1 also the fp16 operand of the f16 GEMM (x16,
@@ -64,7 +65,10 @@ __global__ void __launch_bounds__(1024) quant_act_kernel(const void* __restrict_
       *reinterpret_cast<uint4*>(o8.x8 + x8_group_offset(m, k16, 0, o8.BN, o8.nkb)) = z;
       *reinterpret_cast<uint4*>(o8.x8 + x8_group_offset(m, k16, 1, o8.BN, o8.nkb)) = z;
     }
-    if (m >= o8.M) return;  // a padding token of the last tile: zeros only (whole CTA, before any barrier)
+    if (m >= o8.M) {  // a padding token of the last tile: zeros only (whole CTA, before any barrier)
+      for (int pc = threadIdx.x; pc < x8_sum_parts(K); pc += blockDim.x) o8.sx[m * x8_sum_parts(K) + pc] = 0;
+      return;
+    }
   }
   const char* row = static_cast<const char*>(X) + m * K * kEsize;
   int8_t* out = xq + m * K;
@@ -110,6 +114,7 @@ __global__ void __launch_bounds__(1024) quant_act_kernel(const void* __restrict_
     // fp16 in the order p = 4i + j within the group, or the two e4m3 rows;
     // K % 16 == 0
     const uint4* r4 = reinterpret_cast<const uint4*>(row);
+    int xsum = 0;
     for (int64_t g = tid; g < K / 16; g += nt) {
       uint32_t nat[4];
       if (BF16) {
@@ -140,7 +145,12 @@ __global__ void __launch_bounds__(1024) quant_act_kernel(const void* __restrict_
         x8_rows16(q4, &hi, &lo);
         *reinterpret_cast<uint4*>(o8.x8 + x8_group_offset(m, 16 * g, 0, o8.BN, o8.nkb)) = hi;
         *reinterpret_cast<uint4*>(o8.x8 + x8_group_offset(m, 16 * g, 1, o8.BN, o8.nkb)) = lo;
+        xsum += sum16_i8(q4);
       }
+    }
+    if (OUT == 2) {  // the whole row's sum in the first of the token's partial sums, zeros in the rest
+      for (int pc = 1 + tid; pc < x8_sum_parts(K); pc += nt) o8.sx[m * x8_sum_parts(K) + pc] = 0;
+      block_sum_store(xsum, o8.sx + m * x8_sum_parts(K));
     }
   } else if (vec) {
     const uint4* r4 = reinterpret_cast<const uint4*>(row);
@@ -250,7 +260,10 @@ __global__ void __launch_bounds__(1024) rmsnorm_quant_act_kernel(const void* __r
       *reinterpret_cast<uint4*>(o8.x8 + x8_group_offset(m, k16, 0, o8.BN, o8.nkb)) = z;
       *reinterpret_cast<uint4*>(o8.x8 + x8_group_offset(m, k16, 1, o8.BN, o8.nkb)) = z;
     }
-    if (m >= o8.M) return;  // a padding token of the last tile: zeros only (whole CTA, before any barrier)
+    if (m >= o8.M) {  // a padding token of the last tile: zeros only (whole CTA, before any barrier)
+      for (int pc = threadIdx.x; pc < x8_sum_parts(K); pc += blockDim.x) o8.sx[m * x8_sum_parts(K) + pc] = 0;
+      return;
+    }
   }
   const char* row = static_cast<const char*>(X) + m * K * kEsize;
   const uint4* row4 = reinterpret_cast<const uint4*>(row);
@@ -342,6 +355,7 @@ __global__ void __launch_bounds__(1024) rmsnorm_quant_act_kernel(const void* __r
   // pass 3: codes of x_n = fp32(x * g) / r
   if (OUT != 0) {
     // one 16-element group per thread: x_q (natural order) and the GEMM's operand
+    int xsum = 0;
 #pragma unroll 1
     for (int64_t gq = tid; gq < K / 16; gq += nt) {
       uint32_t nat[4];
@@ -371,7 +385,12 @@ __global__ void __launch_bounds__(1024) rmsnorm_quant_act_kernel(const void* __r
         x8_rows16(q4, &hi, &lo);
         *reinterpret_cast<uint4*>(o8.x8 + x8_group_offset(m, 16 * gq, 0, o8.BN, o8.nkb)) = hi;
         *reinterpret_cast<uint4*>(o8.x8 + x8_group_offset(m, 16 * gq, 1, o8.BN, o8.nkb)) = lo;
+        xsum += sum16_i8(q4);
       }
+    }
+    if (OUT == 2) {  // the whole row's sum in the first of the token's partial sums, zeros in the rest
+      for (int pc = 1 + tid; pc < x8_sum_parts(K); pc += nt) o8.sx[m * x8_sum_parts(K) + pc] = 0;
+      block_sum_store(xsum, o8.sx + m * x8_sum_parts(K));
     }
   } else if (vec) {
 #pragma unroll 1
@@ -710,7 +729,8 @@ cudaError_t launch_rmsnorm_quant_act_x8(const void* X, bool bf16, int64_t M, int
   const int threads = rmsnorm_operand_threads(K, bf16);
   const unsigned long long rk = sq_recip((uint32_t)K);
   const int BN = gemm_f8_token_tile(M);
-  const X8Out o8{f8_operand(ws), f8_counters(ws, M, K, num_sms), num_sms, M, gemm_f8_kblocks(K), BN};
+  const X8Out o8{f8_operand(ws), f8_counters(ws, M, K, num_sms), num_sms, M, gemm_f8_kblocks(K), BN,
+                 f8_sums(ws, M, K, num_sms)};
   const unsigned grid = (unsigned)((M + BN - 1) / BN * BN);  // every token of the last tile
   if (bf16)
     rmsnorm_quant_act_kernel<true, 2><<<grid, threads, 0, stream>>>(X, K, true, gain, eps, rk, xq, s, nullptr, o8);
@@ -760,7 +780,8 @@ cudaError_t launch_quant_act_x8(const void* X, bool bf16, int64_t M, int64_t K, 
   if (threads > 1024) threads = 1024;
   if (threads < 64) threads = 64;
   const int BN = gemm_f8_token_tile(M);
-  const X8Out o8{f8_operand(ws), f8_counters(ws, M, K, num_sms), num_sms, M, gemm_f8_kblocks(K), BN};
+  const X8Out o8{f8_operand(ws), f8_counters(ws, M, K, num_sms), num_sms, M, gemm_f8_kblocks(K), BN,
+                 f8_sums(ws, M, K, num_sms)};
   const unsigned grid = (unsigned)((M + BN - 1) / BN * BN);  // every token of the last tile
   if (bf16) quant_act_kernel<true, 2><<<grid, threads, 0, stream>>>(X, K, true, xq, s, nullptr, o8);
   else quant_act_kernel<false, 2><<<grid, threads, 0, stream>>>(X, K, true, xq, s, nullptr, o8);

@@ -136,6 +136,22 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
+// Position in a ring of n slots and the parity of its current pass, stepped
+// without division: the loops that issue copies and MMAs share their SM's
+// issue slots with the expansion warps, and a division per step is enough
+// to make them the critical path.
+struct RingPos {
+  int idx;
+  uint32_t ph;
+  __device__ __forceinline__ void step(int by, int n) {
+    idx += by;
+    while (idx >= n) {
+      idx -= n;
+      ph ^= 1u;
+    }
+  }
+};
+
 // wait_flag by every lane of a converged warp, with one answer for the warp.
 __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, uint32_t* err, volatile uint32_t* abort_flag) {
   return __all_sync(0xffffffffu, wait_flag(bar, parity, err, abort_flag)) != 0;

@@ -164,12 +164,13 @@ def f8_workspace(M, K, sms):
     """The fp8 GEMM's workspace written out: the e4m3 operand (two rows per
     token of a token tile of M rounded up to 16, K rounded up to 512 bytes
     each), two partial-sum slots per CTA of 128 features x the token tile in
-    fp32, and one arrival counter per CTA, each part rounded up to 256 bytes."""
+    int32, one arrival counter per CTA, and int32 sums of activations per
+    (padded) token over 4096-k chunks, each part rounded up to 256 bytes."""
     up = lambda v: (v + 255) // 256 * 256  # noqa: E731
     ntm = (M + 95) // 96  # token tiles of at most 96
     bn = ((M + ntm - 1) // ntm + 15) // 16 * 16
     kpad = (K + 511) // 512 * 512
-    return up(ntm * 2 * bn * kpad) + 2 * sms * bn * 128 * 4 + up(4 * sms)
+    return up(ntm * 2 * bn * kpad) + 2 * sms * bn * 128 * 4 + up(4 * sms) + up(4 * ntm * bn * ((K + 4095) // 4096))
 
 
 def sk_workspace(M, K, sms):
