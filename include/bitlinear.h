@@ -170,7 +170,7 @@ bl_status bitlinear_pack_weights_tq5(const float* W, int64_t N, int64_t K, float
  *   gamma, x_q, s, y, acc   as for bitlinear_forward
  *   M, N, K   in   M >= 1, 1 <= N <= 2048 * (number of SMs), K % 16 == 0,
  *                  16 <= K <= BITLINEAR_TQ5_MAX_K
- *   flags     in   0 or BITLINEAR_RELU2
+ *   flags     in   0, BITLINEAR_RELU2, and/or the test hook BITLINEAR_TEST_STALL
  *
  * Errors: BL_ERR_INVALID_ARG (null pointer, size < 1, unknown flag),
  * BL_ERR_UNSUPPORTED_SHAPE, BL_ERR_MISALIGNED, BL_ERR_CUDA.
@@ -286,12 +286,20 @@ bl_status bitlinear_forward_lut(const uint8_t* W_packed, const float* gamma, con
  * holds the raw integer products. */
 #define BITLINEAR_RELU2 2u
 
-/* Test hook of bitlinear_quant_forward(_ws), not for production use: on the
- * one-kernel path (M <= 4, K <= 32768) the kernel issues no weight copies, so
- * its bounded waits run out (after about two seconds); it then records
+/* Test hook, not for production use, of bitlinear_quant_forward(_ws) and
+ * bitlinear_forward_tq5: the kernels that wait on copies or on other warps
+ * start none of the work those waits depend on, so their bounded waits run
+ * out (after about two seconds each); every such kernel then records
  * BL_ERR_TIMEOUT in the device error word, writes no y, and exits cleanly.
- * Lets a test exercise the timeout path without faulting or hanging the GPU.
- * Rejected with BL_ERR_INVALID_ARG on the multi-kernel path. */
+ * Lets a test exercise every timeout path without faulting or hanging the
+ * GPU.  Which kernels stall:
+ *   - M <= 4, K <= 32768: the fused quantise + GEMV kernel;
+ *   - bitlinear_quant_forward_ws otherwise: the tensor-core GEMM of the route
+ *     (fp8, persistent or stream-K);
+ *   - bitlinear_quant_forward otherwise: the GEMM, and the quantisation too
+ *     where it is the staged kernel (from 256 tokens), whose x_q and s are
+ *     then unspecified;
+ *   - bitlinear_forward_tq5: the base-3 GEMV. */
 #define BITLINEAR_TEST_STALL 0x80000000u
 
 /*

@@ -84,7 +84,7 @@ bl_status bitlinear_forward_tq5(const uint8_t* W_tq5, const float* gamma, const 
                                 cudaStream_t stream) {
   if (!W_tq5 || !gamma || !x_q || !s || !y) return BL_ERR_INVALID_ARG;
   if (M < 1 || N < 1 || K < 1) return BL_ERR_INVALID_ARG;
-  if (flags & ~BITLINEAR_RELU2) return BL_ERR_INVALID_ARG;
+  if (flags & ~(BITLINEAR_RELU2 | BITLINEAR_TEST_STALL)) return BL_ERR_INVALID_ARG;
   if (K % 16 != 0 || K > bl::kTq5MaxK || M > INT32_MAX) return BL_ERR_UNSUPPORTED_SHAPE;
   if (!aligned(W_tq5, 16) || !aligned(x_q, 16) || !aligned(y, 16) || !aligned(gamma, 4) || !aligned(s, 4) ||
       (acc && !aligned(acc, 16)))
@@ -92,7 +92,8 @@ bl_status bitlinear_forward_tq5(const uint8_t* W_tq5, const float* gamma, const 
   DeviceInfo d;
   if (bl_status st = device_info(&d)) return st;
   if (N > (int64_t)2048 * d.num_sms) return BL_ERR_UNSUPPORTED_SHAPE;  // per-CTA row sums must fit shared memory
-  bl::ForwardArgs a{W_tq5, gamma, x_q, s, M, N, K, y, acc, d.err, (flags & BITLINEAR_RELU2) != 0};
+  bl::ForwardArgs a{W_tq5, gamma, x_q, s, M, N, K, y, acc, d.err, (flags & BITLINEAR_RELU2) != 0,
+                    (flags & BITLINEAR_TEST_STALL) != 0};
   return from_cuda(bl::launch_gemv_tq5(a, bitlinear_tq5_row_bytes(K), d.num_sms, stream));
 }
 
@@ -169,8 +170,8 @@ bl_status bitlinear_quant_forward(const uint8_t* W_packed, const float* gamma, c
   if (M <= bl::kGemvMaxTokens && K <= bl::kGemvMaxK)
     return from_cuda(bl::launch_gemv_fused(a, X, dtype == BL_BF16, x_q, s, (flags & BITLINEAR_WEIGHTS_RESIDENT) != 0,
                                            stall, d.num_sms, stream));
-  if (stall) return BL_ERR_INVALID_ARG;  // the test hook exists on the one-kernel path only
-  if (cudaError_t e = bl::launch_quant_act(X, dtype == BL_BF16, M, K, x_q, s, d.num_sms, d.err, stream))
+  a.test_stall = stall;  // the staged quantisation (from 256 tokens) and the GEMM each give up
+  if (cudaError_t e = bl::launch_quant_act(X, dtype == BL_BF16, M, K, x_q, s, d.num_sms, d.err, stream, stall))
     return from_cuda(e);
   return from_cuda(bl::launch_gemm_tc(a, d.num_sms, stream));
 }
@@ -242,7 +243,7 @@ bl_status bitlinear_quant_forward_ws(const uint8_t* W_packed, const float* gamma
   if (M <= bl::kGemvMaxTokens && K <= bl::kGemvMaxK)
     return from_cuda(bl::launch_gemv_fused(a, X, dtype == BL_BF16, x_q, s, (flags & BITLINEAR_WEIGHTS_RESIDENT) != 0,
                                            stall, d.num_sms, stream));
-  if (stall) return BL_ERR_INVALID_ARG;  // the test hook exists on the one-kernel path only
+  a.test_stall = stall;  // the GEMM gives up
   if (bl::gemm_f8_serves(M, N, K)) {
     if (cudaError_t e = bl::launch_quant_act_x8(X, dtype == BL_BF16, M, K, x_q, s, workspace, d.num_sms, stream))
       return from_cuda(e);

@@ -92,6 +92,7 @@ struct SkCfg {
   int M, N, K, BN, nx, na, acc_stride, acol, ntn, ntp, nkb, C;  // ntp: feature-tile pairs; C: clusters
   int64_t units;  // token tiles * ntp * nkb
   int relu2;
+  int stall;  // test hook: the converters expand nothing
 };
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 2, %0;" ::"n"(32 * kEpiWarps) : "memory"); }
@@ -304,6 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_sk_kernel(const __grid_c
       }
     }
     __syncwarp();
+  } else if (warp < kEpi0 && c.stall) {
+    // test hook: no expansion, so the MMA thread's bounded wait expires
   } else if (warp < kEpi0) {
     // ---------------- weight expansion: thread = weight row r of the tile; set h
     // expands the stages q with q % 2 == h (A slot q % NA, activation slot q % NX)
@@ -643,7 +646,7 @@ cudaError_t launch_gemm_f16_sk(const ForwardArgs& a, void* ws, int num_sms, cuda
   if (C < 1) return cudaErrorInvalidConfiguration;
   if ((int64_t)C > units) C = (int)units;
   SkCfg c{a.Wp, a.gamma, a.s, a.y, a.acc, a.err, l.part, l.cnt, (int)a.M, (int)a.N, (int)a.K, BN, NX, NA,
-          acc_stride, acol, ntn, ntp, nkb, C, units, a.relu2 ? 1 : 0};
+          acc_stride, acol, ntn, ntp, nkb, C, units, a.relu2 ? 1 : 0, a.test_stall ? 1 : 0};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(kPair * C));
   cfg.blockDim = dim3(kThreads);

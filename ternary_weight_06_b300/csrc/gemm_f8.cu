@@ -88,6 +88,7 @@ struct F8Cfg {
   int64_t units;  // output tiles * nkb
   int relu2;
   int nsx;  // partial sums per token in sx
+  int stall;  // test hook: the weight producer issues nothing
 };
 
 __device__ __forceinline__ void mma_f8_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
@@ -200,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f8_kernel(const __grid_const
       const int64_t t0 = begin / c.nkb;
       int kb = (int)(begin - t0 * c.nkb), tn = (int)(t0 % c.ntn);
       int64_t mt = t0 / c.ntn;
-      for (int64_t i = begin; i < end && ok; ++i) {
+      for (int64_t i = begin; i < end && ok && !(wprod && c.stall); ++i) {
         for (int sub = 0; sub < (wprod ? 1 : kKB / kSub); ++sub) {
           if (!wait_warp(&empty[st], ph ^ 1u, c.err, abort_flag)) {
             ok = false;
@@ -586,7 +587,7 @@ cudaError_t launch_gemm_f8(const ForwardArgs& a, void* ws, int num_sms, cudaStre
   cudaError_t e = cudaFuncSetAttribute(gemm_f8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   F8Cfg c{a.gamma, a.s, a.y, a.acc, a.err, l.x8, l.sx, l.part, l.cnt, (int)a.M, (int)a.N, (int)a.K, BN, NW, NX, NI, ntn, nkb,
-          G, NA, acol, units, a.relu2 ? 1 : 0, x8_sum_parts(a.K)};
+          G, NA, acol, units, a.relu2 ? 1 : 0, x8_sum_parts(a.K), a.test_stall ? 1 : 0};
   gemm_f8_kernel<<<G, kThreads, smem, stream>>>(tw, c);
   return cudaGetLastError();
 }

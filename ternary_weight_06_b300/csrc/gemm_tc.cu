@@ -59,6 +59,7 @@ struct GemmCfg {
   int M, N, K, BN;
   int relu2;    // epilogue applies the squared ReLU
   int nstages;  // ring depth (the GEMM on pre-expanded activations)
+  int stall;    // test hook: the TMA producer issues nothing
 };
 
 // ---------------------------------------------------------------- operand expansion
@@ -145,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- TMA producer (the whole warp, one lane issues)
     {
       int issued = 0;
-      for (int kb = 0; kb < nkb; ++kb) {
+      for (int kb = 0; kb < nkb && !c.stall; ++kb) {
         const int slot = kb % kRawStages;
         if (!wait_warp(&raw_empty[slot], ((uint32_t)(kb / kRawStages) & 1u) ^ 1u, c.err, abort_flag)) break;
         uint8_t* wdst = raw_base + slot * (kWRawBytes + x_raw_bytes);
@@ -237,9 +238,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // ---- epilogue
     {
+      // the issuer commits acc_full even after giving up: a thread whose own
+      // waits failed, or that sees the abort flag, writes nothing
       const bool done = wait_flag(acc_full, 0u, c.err, abort_flag);
       tc_fence_after();
-      if (done) epilogue_store(c, tmem, tscale, warp, lane, n0, m0);
+      if (done && ok && *abort_flag == 0u) epilogue_store(c, tmem, tscale, warp, lane, n0, m0);
       tc_fence_before();
     }
   }
@@ -332,7 +335,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       int os = 0, issued = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      for (int t = blockIdx.x; t < ntiles && ok && !c.stall; t += gridDim.x) {
         const int n0 = (t % ntn) * kBM, m0 = (t / ntn) * BN;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!wait_warp(&op_empty[os], ph ^ 1u, c.err, abort_flag)) {
@@ -444,8 +447,17 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const int m = m0 + j;
         ts[j] = m < c.M ? __fdiv_rn(gamma, __ldg(c.s + m)) : 0.0f;
       }
-      asm volatile("bar.sync 2, %0;" ::"n"(32 * kPEpiWarps) : "memory");
-      if (!wait_flag(&acc_full[b], (uint32_t)(lt >> 1) & 1u, c.err, abort_flag)) break;
+      // one barrier of the epilogue warps makes the scales visible and settles, for
+      // every warp alike, whether the accumulator came (a warp whose wait gave
+      // up must not leave the others at a later barrier)
+      const bool got = wait_flag(&acc_full[b], (uint32_t)(lt >> 1) & 1u, c.err, abort_flag);
+      uint32_t any_failed;
+      asm volatile(
+          "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 2, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+          : "=r"(any_failed)
+          : "r"((uint32_t)!got), "n"(32 * kPEpiWarps)
+          : "memory");
+      if (any_failed) break;
       tc_fence_after();
       const int n = n0 + q * 32 + lane;
       // the two warps of a lane quarter take alternate 16-token chunks
@@ -526,7 +538,8 @@ cudaError_t launch_gemm_tc_x16(const ForwardArgs& a, const void* x16, int num_sm
   cudaError_t e =
       cudaFuncSetAttribute(gemm_tc_x16_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  GemmCfg c{a.gamma, a.s, a.y, a.acc, a.err, (int)a.M, (int)a.N, (int)a.K, BN, a.relu2 ? 1 : 0, NS};
+  GemmCfg c{a.gamma, a.s, a.y, a.acc, a.err, (int)a.M, (int)a.N, (int)a.K, BN, a.relu2 ? 1 : 0, NS,
+            a.test_stall ? 1 : 0};
   const int grid = (int)(tiles < num_sms ? tiles : num_sms);
   gemm_tc_x16_persistent_kernel<<<grid, kPThreads, smem, stream>>>(tw, tx, c);
   return cudaGetLastError();
@@ -539,7 +552,8 @@ cudaError_t launch_gemm_tc(const ForwardArgs& a, int num_sms, cudaStream_t strea
   CUtensorMap tw, tx;
   if (!encode_u8_2d(&tw, a.Wp, (uint64_t)a.K / 4, (uint64_t)a.N, kBK / 4, kBM, 0)) return cudaErrorInvalidValue;
   if (!encode_u8_2d(&tx, a.xq, (uint64_t)a.K, (uint64_t)a.M, kBK, (uint32_t)BN, 0)) return cudaErrorInvalidValue;
-  GemmCfg c{a.gamma, a.s, a.y, a.acc, a.err, (int)a.M, (int)a.N, (int)a.K, BN, a.relu2 ? 1 : 0, 0};
+  GemmCfg c{a.gamma, a.s, a.y, a.acc, a.err, (int)a.M, (int)a.N, (int)a.K, BN, a.relu2 ? 1 : 0, 0,
+            a.test_stall ? 1 : 0};
   const size_t smem = 1024 + (size_t)kOpStages * (kAOpBytes + BN * kARowBytes) +
                       (size_t)kRawStages * (kWRawBytes + BN * kBK) + (2 * kRawStages + 2 * kOpStages + 1) * 8 + 16 +
                       (size_t)BN * 4;

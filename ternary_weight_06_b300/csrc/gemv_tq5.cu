@@ -47,6 +47,7 @@ struct Tq5Cfg {
   int kw, words_per_warp;  // K slices per row and the words of each
   int tok0, ntok;
   int relu2;
+  int stall;  // test hook: the producer issues nothing
 };
 
 __device__ __forceinline__ bool t5_wait(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t code,
@@ -118,7 +119,7 @@ __global__ void __launch_bounds__(kT5Threads, 1) gemv_tq5_kernel(const Tq5Cfg c)
     // ---------------- producer: the CTA's rows, stage by stage
     if (lane == 0) {
       int issued = 0;
-      for (int st = 0; st < nstages; ++st) {
+      for (int st = 0; st < (c.stall ? 0 : nstages); ++st) {
         const int slot = st % NS;
         if (st >= NS &&
             !t5_wait(&empty[slot], (uint32_t)((st / NS) - 1) & 1u, c.err, kErrGemvEmptyWait, abort_flag))
@@ -299,6 +300,7 @@ cudaError_t launch_gemv_tq5(const ForwardArgs& a, int64_t pitch, int num_sms, cu
   c.pitch = (int)pitch;
   c.words = (int)(pitch / 4);
   c.relu2 = a.relu2 ? 1 : 0;
+  c.stall = a.test_stall ? 1 : 0;
 
   int grid = (int)(a.N < num_sms ? a.N : num_sms);
   c.rows_per_cta = (int)((a.N + grid - 1) / grid);

@@ -52,7 +52,7 @@ cudaError_t launch_pack_tq5(const float* W, int64_t N, int64_t K, int64_t pitch,
 // copies, one team of warps per row; else one CTA per row.  err: the device
 // error word (the staged kernel's waits are bounded).
 cudaError_t launch_quant_act(const void* X, bool bf16, int64_t M, int64_t K, int8_t* xq, float* s, int num_sms,
-                             uint32_t* err, cudaStream_t stream);
+                             uint32_t* err, cudaStream_t stream, bool test_stall = false);
 
 // Sub-layer RMS normalisation, then the quantisation: r = fp32 sqrt(fp32(ms + eps))
 // with ms the exact mean of X^2 rounded once, x_n = fp32(fp32(X * gain) / r), and
@@ -86,6 +86,7 @@ struct ForwardArgs {
   int32_t* acc;
   uint32_t* err;  // device error word
   bool relu2 = false;  // epilogue applies the squared ReLU
+  bool test_stall = false;  // test hook: the kernel's copy producer issues nothing, so its bounded waits expire
 };
 
 // The forward from base-3 packed weights (five per byte, rows of `pitch`

@@ -442,6 +442,7 @@ struct RowQuantArgs {
   uint32_t row_bytes;
   int stages;  // ring depth per team
   int team;    // warps per row
+  int stall;   // test hook: no row copies are issued, so the bounded waits expire
 };
 
 constexpr int kRowWarpsMax = 16;
@@ -499,12 +500,14 @@ __global__ void __launch_bounds__(kRowWarpsMax * 32) quant_rows_staged_kernel(co
 
   const int64_t gt = (int64_t)blockIdx.x * nteams + team, GT = (int64_t)gridDim.x * nteams;
   const int64_t nrows = gt < a.M ? (a.M - 1 - gt) / GT + 1 : 0;
+  int64_t issued = 0;  // rows 0 .. issued - 1 have been copied for (leader only)
   auto issue = [&](int64_t i, int st) {
     const int64_t m = gt + i * GT;
     mbar_arrive_expect_tx(&bars[st], a.row_bytes);
     bulk_g2s(ring + (size_t)st * a.row_bytes, a.X + m * (int64_t)a.row_bytes, a.row_bytes, &bars[st]);
+    issued = i + 1;
   };
-  if (leader)
+  if (leader && !a.stall)
     for (int i = 0; i < S && i < nrows; ++i) issue(i, i);
 
   int st = 0, prev_st = 0;
@@ -520,13 +523,13 @@ __global__ void __launch_bounds__(kRowWarpsMax * 32) quant_rows_staged_kernel(co
       issue(i - 1 + S, prev_st);
     }
     if (!ok) {
-      // give up: rows i .. i + S - 1 have been issued (the refill above ran);
-      // let every copy still in flight into this team's ring land (each wait
-      // bounded) before the CTA's shared memory is released
+      // give up: let every copy still in flight into this team's ring (rows
+      // i .. issued - 1, the refill above included) land, each wait bounded,
+      // before the CTA's shared memory is released
       if (leader) {
         int sj = st;
         uint32_t pj = phase;
-        for (int64_t j = i; j < i + S && j < nrows; ++j) {
+        for (int64_t j = i; j < issued; ++j) {
           mbar_wait_bounded(&bars[sj], pj, a.err, kErrQuantWait);
           if (++sj == S) {
             sj = 0;
@@ -661,11 +664,12 @@ RowPlan plan_rows_staged(int64_t M, int64_t K, int num_sms) {
 
 template <bool BF16>
 cudaError_t launch_rows_staged(const void* X, int64_t M, int64_t K, int8_t* xq, float* s, int num_sms, uint32_t* err,
-                               cudaStream_t stream, bool* launched) {
+                               cudaStream_t stream, bool* launched, bool test_stall) {
   *launched = false;
   const RowPlan p = plan_rows_staged<BF16>(M, K, num_sms);
   if (!p.ok) return cudaSuccess;
-  const RowQuantArgs a{static_cast<const char*>(X), M, K, xq, s, err, (uint32_t)(K * (BF16 ? 2 : 4)), p.stages, p.team};
+  const RowQuantArgs a{static_cast<const char*>(X), M, K, xq, s, err, (uint32_t)(K * (BF16 ? 2 : 4)), p.stages, p.team,
+                       test_stall ? 1 : 0};
   *launched = true;
   quant_rows_staged_kernel<BF16><<<p.grid, p.warps * 32, p.smem, stream>>>(a);
   return cudaGetLastError();
@@ -740,11 +744,11 @@ cudaError_t launch_rmsnorm_quant_act_x8(const void* X, bool bf16, int64_t M, int
 }
 
 cudaError_t launch_quant_act(const void* X, bool bf16, int64_t M, int64_t K, int8_t* xq, float* s, int num_sms,
-                             uint32_t* err, cudaStream_t stream) {
+                             uint32_t* err, cudaStream_t stream, bool test_stall) {
   if (reinterpret_cast<uintptr_t>(X) % 16 == 0 && reinterpret_cast<uintptr_t>(xq) % 16 == 0) {
     bool launched = false;
-    const cudaError_t e = bf16 ? launch_rows_staged<true>(X, M, K, xq, s, num_sms, err, stream, &launched)
-                               : launch_rows_staged<false>(X, M, K, xq, s, num_sms, err, stream, &launched);
+    const cudaError_t e = bf16 ? launch_rows_staged<true>(X, M, K, xq, s, num_sms, err, stream, &launched, test_stall)
+                               : launch_rows_staged<false>(X, M, K, xq, s, num_sms, err, stream, &launched, test_stall);
     if (e != cudaSuccess || launched) return e;
   }
   const int esize = bf16 ? 2 : 4;
