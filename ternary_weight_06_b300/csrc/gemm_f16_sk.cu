@@ -255,6 +255,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_sk_kernel(const __grid_c
     // ---------------- MMA issuer (the whole warp, one lane issues): four MMAs
     // of 16 k per 64-k stage into accumulator b
     const uint32_t idesc = f16_idesc(kBM, BN);
+    const uint32_t a_col0 = tmem + (uint32_t)c.acol;
+    const uint64_t bd0 = sw128_desc(smem_u32(xring));  // stage s: + s * x_bytes / 16 in the address field
+    const int xstep = x_bytes >> 4;
     int lt = 0;
     RingPos xr{0, 0u}, ar{0, 0u};
     bool ok = true;
@@ -267,29 +270,44 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_sk_kernel(const __grid_c
       tc_fence_after();
       const uint32_t d = tmem + (uint32_t)(b * c.acc_stride);
       uint32_t accum = 0u;  // the segment's first MMA overwrites the accumulator
+      // one 64-k stage: the single issuing warp's instruction stream, not the
+      // tensor core, bounds the rate, so addresses advance by addition and the
+      // usual eight-stage unit is unrolled
+      auto stage = [&]() -> bool {
+        // a_full implies x_full: the expanding warps waited for the stage's activations
+        if (!wait_warp(&a_full[ar.idx], ar.ph, c.err, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t a_col = a_col0 + (uint32_t)(ar.idx * kACols);
+        const uint64_t bd = bd0 + (uint64_t)(xr.idx * xstep);
+        if (elect_one()) {
+          // 16 k per MMA: 8 columns of A, 32 bytes (+2 in the address field) of B
+          mma_f16_tmem_a(d, a_col + 0, bd + 0, idesc, accum);
+          mma_f16_tmem_a(d, a_col + 8, bd + 2, idesc, 1u);
+          mma_f16_tmem_a(d, a_col + 16, bd + 4, idesc, 1u);
+          mma_f16_tmem_a(d, a_col + 24, bd + 6, idesc, 1u);
+          mma_commit_mc(&done[xr.idx], (uint16_t)((1u << kPair) - 1u));  // the stage, in both CTAs
+        }
+        __syncwarp();
+        accum = 1u;
+        xr.step(1, NX);
+        ar.step(1, NA);
+        return true;
+      };
       for (int kb = kb0; kb < kb1 && ok; ++kb) {
         const int nch = unit_chunks(kb, c.K);
-        for (int g = 0; g < nch; ++g) {
-          // a_full implies x_full: the expanding warps waited for the stage's activations
-          if (!wait_warp(&a_full[ar.idx], ar.ph, c.err, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a_col = tmem + (uint32_t)(c.acol + ar.idx * kACols);
-          const uint64_t bd = sw128_desc(smem_u32(xring + xr.idx * x_bytes));
-          if (elect_one()) {
-            // 16 k per MMA: 8 columns of A, 32 bytes (+2 in the address field) of B
-            mma_f16_tmem_a(d, a_col + 0, bd + 0, idesc, accum);
-            mma_f16_tmem_a(d, a_col + 8, bd + 2, idesc, 1u);
-            mma_f16_tmem_a(d, a_col + 16, bd + 4, idesc, 1u);
-            mma_f16_tmem_a(d, a_col + 24, bd + 6, idesc, 1u);
-            mma_commit_mc(&done[xr.idx], (uint16_t)((1u << kPair) - 1u));  // the stage, in both CTAs
-          }
-          __syncwarp();
-          accum = 1u;
-          xr.step(1, NX);
-          ar.step(1, NA);
+        if (nch == kChunks) {
+#pragma unroll
+          for (int g = 0; g < kChunks; ++g)
+            if (!stage()) {
+              ok = false;
+              break;
+            }
+        } else {
+          for (int g = 0; g < nch; ++g)
+            if (!stage()) {
+              ok = false;
+              break;
+            }
         }
       }
       if (ok && elect_one()) mma_commit(&acc_full[b]);

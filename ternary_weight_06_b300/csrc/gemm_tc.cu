@@ -369,6 +369,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // ---------------- MMA issuer (the whole warp, one lane issues)
     {
       const uint32_t idesc = f16_idesc(kBM, BN);
+      const uint32_t smem0 = smem_u32(smem);
       int os = 0, lt = 0;
       uint32_t par = 0;
       bool ok = true;
@@ -377,18 +378,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (!wait_warp(&acc_empty[b], ((uint32_t)(lt >> 1) & 1u) ^ 1u, c.err, abort_flag)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(b * 256);
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!wait_warp(&op_full[os], par, c.err, abort_flag) || !wait_warp(&tma_full[os], par, c.err, abort_flag)) {
-            ok = false;
-            break;
-          }
+        // one 64-k stage; the single issuing warp's instruction stream bounds the
+        // rate, so the stages are unrolled by four and op_full stands for the
+        // stage's copies too (the converters waited for them before arriving)
+        auto stage = [&](int kb) -> bool {
+          if (!wait_warp(&op_full[os], par, c.err, abort_flag)) return false;
           tc_fence_after();
-          const uint32_t a_base = smem_u32(smem + os * stage_bytes);
-          const uint32_t b_base = a_base + kAOpBytes;
+          const uint32_t a_base = smem0 + (uint32_t)(os * stage_bytes);
+          const uint64_t da = sw128_desc(a_base), db = sw128_desc(a_base + kAOpBytes);
           if (elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk)
-              mma_f16(d, sw128_desc(a_base + kk * 32), sw128_desc(b_base + kk * 32), idesc, (kb | kk) ? 1u : 0u);
+            for (int kk = 0; kk < kBK / 16; ++kk)  // 32 bytes (+2 in the address field) per MMA
+              mma_f16(d, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), idesc, (kb | kk) ? 1u : 0u);
             mma_commit(&op_empty[os]);
           }
           __syncwarp();
@@ -396,7 +397,20 @@ __global__ void __launch_bounds__(kPThreads, 1)
             os = 0;
             par ^= 1u;
           }
+          return true;
+        };
+        int kb = 0;
+#pragma unroll 1
+        for (; kb + 4 <= nkb && ok; kb += 4) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (!stage(kb + u)) {
+              ok = false;
+              break;
+            }
         }
+        for (; kb < nkb && ok; ++kb)
+          if (!stage(kb)) ok = false;
         if (ok && elect_one()) mma_commit(&acc_full[b]);
         __syncwarp();
       }
