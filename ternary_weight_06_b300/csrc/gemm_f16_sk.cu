@@ -293,15 +293,43 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_sk_kernel(const __grid_c
         ar.step(1, NA);
         return true;
       };
+      // two stages' operands, checked together: both are usually ready already, so
+      // one round trip of polls serves both; otherwise each is waited for in turn
+      auto ready2 = [&]() -> bool {
+        RingPos a2 = ar;
+        a2.step(1, NA);
+        const bool both = mbar_try_wait(smem_u32(&a_full[ar.idx]), ar.ph) & mbar_try_wait(smem_u32(&a_full[a2.idx]), a2.ph);
+        return __all_sync(0xffffffffu, both) != 0;
+      };
+      auto issue = [&]() {
+        tc_fence_after();
+        const uint32_t a_col = a_col0 + (uint32_t)(ar.idx * kACols);
+        const uint64_t bd = bd0 + (uint64_t)(xr.idx * xstep);
+        if (elect_one()) {
+          mma_f16_tmem_a(d, a_col + 0, bd + 0, idesc, accum);
+          mma_f16_tmem_a(d, a_col + 8, bd + 2, idesc, 1u);
+          mma_f16_tmem_a(d, a_col + 16, bd + 4, idesc, 1u);
+          mma_f16_tmem_a(d, a_col + 24, bd + 6, idesc, 1u);
+          mma_commit_mc(&done[xr.idx], (uint16_t)((1u << kPair) - 1u));
+        }
+        __syncwarp();
+        accum = 1u;
+        xr.step(1, NX);
+        ar.step(1, NA);
+      };
       for (int kb = kb0; kb < kb1 && ok; ++kb) {
         const int nch = unit_chunks(kb, c.K);
         if (nch == kChunks) {
 #pragma unroll
-          for (int g = 0; g < kChunks; ++g)
-            if (!stage()) {
+          for (int g = 0; g < kChunks; g += 2) {
+            if (ready2()) {
+              issue();
+              issue();
+            } else if (!stage() || !stage()) {
               ok = false;
               break;
             }
+          }
         } else {
           for (int g = 0; g < nch; ++g)
             if (!stage()) {
