@@ -267,7 +267,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f8_kernel(const __grid_const
         for (int kb = kb0; kb < kb1 && ok; ++kb) {
           for (int sub = q; sub < kKB / kSub; sub += NI) {
             const int as = ap.idx, xs = xp.idx;
-            if (!wait_warp(&x_full[xs], xp.ph, c.err, abort_flag) || !wait_warp(&a_full[as], ap.ph, c.err, abort_flag)) {
+            // both operands polled in one round trip (usually both ready), else waited for in turn
+            const bool ready = __all_sync(0xffffffffu, mbar_try_wait(smem_u32(&x_full[xs]), xp.ph) &
+                                                           mbar_try_wait(smem_u32(&a_full[as]), ap.ph)) != 0;
+            if (!ready &&
+                (!wait_warp(&x_full[xs], xp.ph, c.err, abort_flag) || !wait_warp(&a_full[as], ap.ph, c.err, abort_flag))) {
               ok = false;
               break;
             }
