@@ -108,40 +108,6 @@ __device__ __forceinline__ bool epi_bar_or(bool v) {
   return r != 0;
 }
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// All threads of both CTAs of the cluster.
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// TMA tile load into the same shared-memory offset of every CTA in `mask`,
-// completing bytes on the barrier at the same offset in each.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
-      : "memory");
-}
-
-// Commit of this thread's MMAs, arriving on the barrier at the same offset in
-// every CTA in `mask`.
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(mask)
-      : "memory");
-}
-
-// Position in a ring of n slots: the slot and the parity of its current
-// phase, advanced by `by` slots at a time (no division on the hot loops).
 // Cluster whose range holds flattened unit i: begin(c) = floor(c U / C) <= i.
 __device__ __forceinline__ int cluster_of(int64_t i, int64_t U, int C) { return (int)(((i + 1) * C + U - 1) / U) - 1; }
 
