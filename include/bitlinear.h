@@ -306,11 +306,14 @@ bl_status bitlinear_forward_lut(const uint8_t* W_packed, const float* gamma, con
  * bitlinear_quant_forward -- bitlinear_quant_act followed by
  * bitlinear_forward, as one call: per-token absmax int8 quantisation of X
  * (anthology note-168, "What it does": activations at 8 bits) and the
- * ternary x int8 product with the gamma/s rescale.  For M <= 4 (and K <=
- * 32768) both run in ONE kernel (each CTA quantises the few token rows it
- * needs; the first CTA writes x_q and s out), which removes a launch and a
- * round trip per layer in decode; otherwise it is the two kernels in
- * sequence.  Results are bit-identical to the two separate calls.
+ * ternary x int8 product with the gamma/s rescale.  For M <= 4 and K <= 16384
+ * both run in ONE kernel (each CTA quantises the few token rows it needs; the
+ * first CTA writes x_q and s out), which removes a launch and a round trip per
+ * layer in decode.  For M <= 4 and longer rows (to K = 32768) the per-token
+ * quantisation runs first and the GEMV is launched as its programmatic
+ * dependent, so that the weight stream starts while the row is quantised.
+ * Otherwise it is the two kernels in sequence.  Results are bit-identical to
+ * the two separate calls.
  *
  *   W_packed, gamma     in   as for bitlinear_forward
  *   X, dtype            in   as for bitlinear_quant_act

@@ -32,6 +32,18 @@ inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintp
 
 inline bl_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BL_OK : BL_ERR_CUDA; }
 
+// The few-token route (M <= 4, K <= 32768): one fused quantise + GEMV kernel
+// for rows up to 16384 activations (and always under the stall test hook);
+// longer rows are quantised by the per-token kernel, and the GEMV follows as
+// its programmatic dependent, its weight stream starting meanwhile.
+cudaError_t launch_few_tokens(const bl::ForwardArgs& a, const void* X, bool bf16, int8_t* x_q, float* s,
+                              bool resident, bool stall, const DeviceInfo& d, cudaStream_t stream) {
+  if (a.K <= bl::kGemvFusedMaxK || stall)
+    return bl::launch_gemv_fused(a, X, bf16, x_q, s, resident, stall, d.num_sms, stream);
+  if (cudaError_t e = bl::launch_quant_act(X, bf16, a.M, a.K, x_q, s, d.num_sms, d.err, stream)) return e;
+  return bl::launch_gemv(a, d.num_sms, stream, true);
+}
+
 }  // namespace
 
 extern "C" {
@@ -168,8 +180,8 @@ bl_status bitlinear_quant_forward(const uint8_t* W_packed, const float* gamma, c
   bl::ForwardArgs a{W_packed, gamma, x_q, s, M, N, K, y, acc, d.err, (flags & BITLINEAR_RELU2) != 0};
   const bool stall = (flags & BITLINEAR_TEST_STALL) != 0;
   if (M <= bl::kGemvMaxTokens && K <= bl::kGemvMaxK)
-    return from_cuda(bl::launch_gemv_fused(a, X, dtype == BL_BF16, x_q, s, (flags & BITLINEAR_WEIGHTS_RESIDENT) != 0,
-                                           stall, d.num_sms, stream));
+    return from_cuda(launch_few_tokens(a, X, dtype == BL_BF16, x_q, s, (flags & BITLINEAR_WEIGHTS_RESIDENT) != 0,
+                                       stall, d, stream));
   a.test_stall = stall;  // the staged quantisation (from 256 tokens) and the GEMM each give up
   if (cudaError_t e = bl::launch_quant_act(X, dtype == BL_BF16, M, K, x_q, s, d.num_sms, d.err, stream, stall))
     return from_cuda(e);
@@ -241,8 +253,8 @@ bl_status bitlinear_quant_forward_ws(const uint8_t* W_packed, const float* gamma
   bl::ForwardArgs a{W_packed, gamma, x_q, s, M, N, K, y, acc, d.err, (flags & BITLINEAR_RELU2) != 0};
   const bool stall = (flags & BITLINEAR_TEST_STALL) != 0;
   if (M <= bl::kGemvMaxTokens && K <= bl::kGemvMaxK)
-    return from_cuda(bl::launch_gemv_fused(a, X, dtype == BL_BF16, x_q, s, (flags & BITLINEAR_WEIGHTS_RESIDENT) != 0,
-                                           stall, d.num_sms, stream));
+    return from_cuda(launch_few_tokens(a, X, dtype == BL_BF16, x_q, s, (flags & BITLINEAR_WEIGHTS_RESIDENT) != 0,
+                                       stall, d, stream));
   a.test_stall = stall;  // the GEMM gives up
   if (bl::gemm_f8_serves(M, N, K)) {
     if (cudaError_t e = bl::launch_quant_act_x8(X, dtype == BL_BF16, M, K, x_q, s, workspace, d.num_sms, stream))
@@ -276,7 +288,7 @@ bl_status bitlinear_quant_forward_requant_ws(const uint8_t* W_packed, const floa
   const bool bf16 = dtype == BL_BF16;
   cudaError_t e;
   if (M <= bl::kGemvMaxTokens && K <= bl::kGemvMaxK) {
-    e = bl::launch_gemv_fused(a, X, bf16, x_q, s, false, false, d.num_sms, stream);
+    e = launch_few_tokens(a, X, bf16, x_q, s, false, false, d, stream);
   } else if (bl::gemm_f8_serves(M, N, K)) {
     e = bl::launch_quant_act_x8(X, bf16, M, K, x_q, s, workspace, d.num_sms, stream);
     if (e == cudaSuccess) e = bl::launch_gemm_f8(a, workspace, d.num_sms, stream);

@@ -586,8 +586,8 @@ cudaError_t run(const ForwardArgs& a, const void* X, bool x_bf16, int8_t* xq_out
 
 }  // namespace
 
-cudaError_t launch_gemv(const ForwardArgs& a, int num_sms, cudaStream_t stream) {
-  return run(a, nullptr, false, nullptr, nullptr, false, false, false, num_sms, stream);
+cudaError_t launch_gemv(const ForwardArgs& a, int num_sms, cudaStream_t stream, bool pdl) {
+  return run(a, nullptr, false, nullptr, nullptr, false, pdl, false, num_sms, stream);
 }
 
 cudaError_t launch_gemv_fused(const ForwardArgs& a, const void* X, bool x_bf16, int8_t* xq_out, float* s_out,

@@ -99,7 +99,14 @@ cudaError_t launch_gemv_tq5(const ForwardArgs& a, int64_t pitch, int num_sms, cu
 cudaError_t launch_gemv_lut(const ForwardArgs& a, int num_sms, cudaStream_t stream);
 
 // Streaming GEMV for a few tokens (tokens are taken in groups of <= 4; K <= 32768).
-cudaError_t launch_gemv(const ForwardArgs& a, int num_sms, cudaStream_t stream);
+// pdl: launched as a programmatic dependent of the preceding kernel (the weight
+// stream starts before that kernel ends; activations are read after it).
+cudaError_t launch_gemv(const ForwardArgs& a, int num_sms, cudaStream_t stream, bool pdl = false);
+
+// Rows of at most this many activations are quantised inside the fused GEMV
+// (every CTA reads the row for the maximum); longer rows are quantised by the
+// per-token kernel first, and the GEMV follows as its programmatic dependent.
+constexpr int64_t kGemvFusedMaxK = 16384;
 
 // The same GEMV with the per-token activation quantisation fused in: reads X
 // (bf16 or fp32) instead of x_q / s; the first CTA writes x_q and s out.

@@ -56,6 +56,7 @@ __global__ void __launch_bounds__(1024) quant_act_kernel(const void* __restrict_
                                                          uint4* __restrict__ xop, const X8Out o8) {
   constexpr int kEsize = BF16 ? 2 : 4;
   const int64_t m = blockIdx.x;
+  pdl_launch_dependents();  // a dependent GEMV may start streaming its weights now
   if (OUT != 0 && blockIdx.x == 0)
     for (int i = threadIdx.x; i < o8.ncnt; i += blockDim.x) o8.cnt[i] = 0u;
   if (OUT == 2) {
