@@ -11,7 +11,7 @@ packing kernels are timed in the same run and reported under "pack".
 
 The default workload is the 70B-class layer pair at M = 1, 16 and 176 tokens
 (the largest configuration that fits one GPU), so one line covers both halves
-of the metric: the few-token layers are judged in GB/s against HBM, the
+of the metric: the few-token layers are rated in GB/s against HBM, the
 176-token layers in TOPS against the tensor pipe ("roofline.per_layer").
 
 Timing: W warm-up steps, then the K steps, captured as one CUDA graph of the
