@@ -664,13 +664,19 @@ cudaError_t launch_gemm_f16_sk(const ForwardArgs& a, void* ws, int num_sms, cuda
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  // a programmatic dependent of the preceding kernel (the quantisation or the
+  // prepass): barrier set-up, tensor-memory allocation and the weight
+  // expansion start before it ends; the activation producers and the
+  // epilogue wait for it (griddepcontrol.wait) before reading what it wrote
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kPair;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, gemm_f16_sk_kernel, tx, c);
 }
 

@@ -592,8 +592,20 @@ cudaError_t launch_gemm_f8(const ForwardArgs& a, void* ws, int num_sms, cudaStre
   if (e != cudaSuccess) return e;
   F8Cfg c{a.gamma, a.s, a.y, a.acc, a.err, l.x8, l.sx, l.part, l.cnt, (int)a.M, (int)a.N, (int)a.K, BN, NW, NX, NI, ntn, nkb,
           G, NA, acol, units, a.relu2 ? 1 : 0, x8_sum_parts(a.K), a.test_stall ? 1 : 0};
-  gemm_f8_kernel<<<G, kThreads, smem, stream>>>(tw, c);
-  return cudaGetLastError();
+  // a programmatic dependent of the preceding kernel (the quantisation or the
+  // prepass): the weight stream and its expansion start before it ends; the
+  // activation producer and the epilogue wait for it before reading its output
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)G);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_f8_kernel, tw, c);
 }
 
 }  // namespace bl

@@ -555,8 +555,20 @@ cudaError_t launch_gemm_tc_x16(const ForwardArgs& a, const void* x16, int num_sm
   GemmCfg c{a.gamma, a.s, a.y, a.acc, a.err, (int)a.M, (int)a.N, (int)a.K, BN, a.relu2 ? 1 : 0, NS,
             a.test_stall ? 1 : 0};
   const int grid = (int)(tiles < num_sms ? tiles : num_sms);
-  gemm_tc_x16_persistent_kernel<<<grid, kPThreads, smem, stream>>>(tw, tx, c);
-  return cudaGetLastError();
+  // a programmatic dependent of the preceding kernel (the quantisation or the
+  // prepass): set-up starts before it ends; the producer and the epilogue wait
+  // for it (griddepcontrol.wait) before reading its output
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kPThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_x16_persistent_kernel, tw, tx, c);
 }
 
 cudaError_t launch_gemm_tc(const ForwardArgs& a, int num_sms, cudaStream_t stream) {
