@@ -46,28 +46,61 @@ struct X8Out {
   int32_t* sx;  // OUT == 2: every token's x8_sum_parts(K) partial sums of int8 activations (0 for padding tokens)
 };
 
+// Clusters of CTAs sharing one token row (a launch without clusters is a
+// cluster of one): rank, size, barrier, and a 32-bit load from a peer's
+// shared memory at the same offset as `local`.
+__device__ __forceinline__ uint32_t cl_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cl_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cl_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cl_load_peer(const void* local, uint32_t rank) {
+  uint32_t ra, v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(ra) : "memory");
+  return v;
+}
+
 // OUT: 0 x_q and s only; 1 also the fp16 operand of the f16 GEMM (x16,
 // M x K halves); 2 also the e4m3 operand of the fp8 GEMM: the grid then has a
 // CTA for every token of the last tile, and the CTAs of tokens past M (and
 // every CTA for k past K in the last block) write zeros.
+// A row may be shared by a cluster of up to 8 CTAs (launched with cluster
+// dimensions): each takes a contiguous slice of the row, and the slices'
+// maxima (and, for OUT == 2, activation sums) are exchanged through
+// distributed shared memory; max and integer sums do not depend on the split.
 template <bool BF16, int OUT>
 __global__ void __launch_bounds__(1024) quant_act_kernel(const void* __restrict__ X, int64_t K, bool vec,
                                                          int8_t* __restrict__ xq, float* __restrict__ s,
                                                          uint4* __restrict__ xop, const X8Out o8) {
   constexpr int kEsize = BF16 ? 2 : 4;
-  const int64_t m = blockIdx.x;
+  const uint32_t S = cl_size(), rk = S > 1 ? cl_rank() : 0u;  // CTAs per row, this CTA's slice
+  const int64_t m = S > 1 ? blockIdx.x / S : blockIdx.x;
   pdl_launch_dependents();  // a dependent GEMV may start streaming its weights now
   if (OUT != 0 && blockIdx.x == 0)
     for (int i = threadIdx.x; i < o8.ncnt; i += blockDim.x) o8.cnt[i] = 0u;
+  // slice [lo, hi) of n items (n * 8 < 2^32: K <= 2^24); no division for an unsplit row
+  auto slice_lo = [&](int64_t n) -> int64_t { return S > 1 ? (uint32_t)n * rk / S : 0; };
+  auto slice_hi = [&](int64_t n) -> int64_t { return S > 1 ? (uint32_t)n * (rk + 1u) / S : n; };
   if (OUT == 2) {
     const int64_t kpad = o8.nkb * kX8Block;
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-    for (int64_t k16 = (m < o8.M ? K : 0) + 16 * (int64_t)threadIdx.x; k16 < kpad; k16 += 16 * (int64_t)blockDim.x) {
+    for (int64_t k16 = (m < o8.M ? K : 0) + 16 * ((int64_t)threadIdx.x + (int64_t)rk * blockDim.x); k16 < kpad;
+         k16 += 16 * (int64_t)blockDim.x * S) {
       *reinterpret_cast<uint4*>(o8.x8 + x8_group_offset(m, k16, 0, o8.BN, o8.nkb)) = z;
       *reinterpret_cast<uint4*>(o8.x8 + x8_group_offset(m, k16, 1, o8.BN, o8.nkb)) = z;
     }
-    if (m >= o8.M) {  // a padding token of the last tile: zeros only (whole CTA, before any barrier)
-      for (int pc = threadIdx.x; pc < x8_sum_parts(K); pc += blockDim.x) o8.sx[m * x8_sum_parts(K) + pc] = 0;
+    if (m >= o8.M) {  // a padding token of the last tile: zeros only (the whole cluster, before any barrier)
+      if (rk == 0)
+        for (int pc = threadIdx.x; pc < x8_sum_parts(K); pc += blockDim.x) o8.sx[m * x8_sum_parts(K) + pc] = 0;
       return;
     }
   }
@@ -79,7 +112,7 @@ __global__ void __launch_bounds__(1024) quant_act_kernel(const void* __restrict_
   if (vec) {
     const uint4* r4 = reinterpret_cast<const uint4*>(row);
     const int64_t nch = K * kEsize / 16;
-    for (int64_t c = tid; c < nch; c += nt) {
+    for (int64_t c = slice_lo(nch) + tid, c_end = slice_hi(nch); c < c_end; c += nt) {
       const uint4 v = __ldg(r4 + c);
       if (BF16) {
         amax = max(amax, max(max(abs_bits_bf16x2(v.x), abs_bits_bf16x2(v.y)),
@@ -89,26 +122,35 @@ __global__ void __launch_bounds__(1024) quant_act_kernel(const void* __restrict_
       }
     }
   } else {
-    for (int64_t k = tid; k < K; k += nt) {
+    for (int64_t k = slice_lo(K) + tid, k_end = slice_hi(K); k < k_end; k += nt) {
       uint32_t b = BF16 ? ((uint32_t)reinterpret_cast<const uint16_t*>(row)[k] << 16)
                         : reinterpret_cast<const uint32_t*>(row)[k];
       amax = max(amax, b & 0x7fffffffu);
     }
   }
   __shared__ uint32_t red[32];
+  __shared__ uint32_t cl_max;  // this CTA's slice maximum, read by the other CTAs of the row
   amax = __reduce_max_sync(0xffffffffu, amax);
   if ((tid & 31) == 0) red[tid >> 5] = amax;
   __syncthreads();
   if (tid < 32) {
     uint32_t v = tid < (nt >> 5) ? red[tid] : 0u;
     v = __reduce_max_sync(0xffffffffu, v);
-    if (tid == 0) red[0] = v;
+    if (tid == 0) red[0] = cl_max = v;
+  }
+  if (S > 1) {
+    cl_barrier();  // every slice maximum is written
+    if (tid == 0) {
+      uint32_t v = 0u;
+      for (uint32_t q = 0; q < S; ++q) v = max(v, cl_load_peer(&cl_max, q));
+      red[0] = v;
+    }
   }
   __syncthreads();
   float a = __uint_as_float(red[0]);
   if (a < kActClampEps) a = kActClampEps;
   const float sm = __fdiv_rn(127.0f, a);
-  if (tid == 0) s[m] = sm;
+  if (tid == 0 && rk == 0) s[m] = sm;
 
   if (OUT != 0) {
     // groups of 16 activations: x_q (natural order) and the GEMM's operand:
@@ -116,7 +158,7 @@ __global__ void __launch_bounds__(1024) quant_act_kernel(const void* __restrict_
     // K % 16 == 0
     const uint4* r4 = reinterpret_cast<const uint4*>(row);
     int xsum = 0;
-    for (int64_t g = tid; g < K / 16; g += nt) {
+    for (int64_t g = slice_lo(K / 16) + tid, g_end = slice_hi(K / 16); g < g_end; g += nt) {
       uint32_t nat[4];
       if (BF16) {
         const uint4 a = __ldg(r4 + 2 * g), b = __ldg(r4 + 2 * g + 1);
@@ -150,13 +192,23 @@ __global__ void __launch_bounds__(1024) quant_act_kernel(const void* __restrict_
       }
     }
     if (OUT == 2) {  // the whole row's sum in the first of the token's partial sums, zeros in the rest
-      for (int pc = 1 + tid; pc < x8_sum_parts(K); pc += nt) o8.sx[m * x8_sum_parts(K) + pc] = 0;
-      block_sum_store(xsum, o8.sx + m * x8_sum_parts(K));
+      __shared__ int32_t cl_sum;  // this CTA's slice sum, read by rank 0
+      if (rk == 0)
+        for (int pc = 1 + tid; pc < x8_sum_parts(K); pc += nt) o8.sx[m * x8_sum_parts(K) + pc] = 0;
+      block_sum_store(xsum, S > 1 ? &cl_sum : o8.sx + m * x8_sum_parts(K));
+      if (S > 1) {
+        cl_barrier();  // every slice sum is written
+        if (rk == 0 && tid == 0) {
+          int32_t v = 0;
+          for (uint32_t q = 0; q < S; ++q) v += (int32_t)cl_load_peer(&cl_sum, q);
+          o8.sx[m * x8_sum_parts(K)] = v;
+        }
+      }
     }
   } else if (vec) {
     const uint4* r4 = reinterpret_cast<const uint4*>(row);
     const int64_t nch = K * kEsize / 16;
-    for (int64_t c = tid; c < nch; c += nt) {
+    for (int64_t c = slice_lo(nch) + tid, c_end = slice_hi(nch); c < c_end; c += nt) {
       const uint4 v = __ldg(r4 + c);
       if (BF16) {
         uint2 o;
@@ -172,12 +224,13 @@ __global__ void __launch_bounds__(1024) quant_act_kernel(const void* __restrict_
       }
     }
   } else {
-    for (int64_t k = tid; k < K; k += nt) {
+    for (int64_t k = slice_lo(K) + tid, k_end = slice_hi(K); k < k_end; k += nt) {
       const float x = BF16 ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(row)[k] << 16)
                            : reinterpret_cast<const float*>(row)[k];
       out[k] = (int8_t)q8(x, sm);
     }
   }
+  if (S > 1) cl_barrier();  // no CTA leaves while another may still read its shared memory
 }
 
 // Sub-layer RMS normalisation, then the quantisation of the normalised row
@@ -744,6 +797,53 @@ cudaError_t launch_rmsnorm_quant_act_x8(const void* X, bool bf16, int64_t M, int
   return cudaGetLastError();
 }
 
+namespace {
+
+// CTAs per token row for the fp8 operand writer: rows of at least 16384
+// activations are split into slices of about 256 groups of 16 (at most 8, a
+// portable cluster), while rows x CTAs stays within two waves of SMs.  Shorter
+// rows, and the x_q-only quantisation, measured no faster split (the cluster
+// launch costs about what the split saves there).
+int row_split(int64_t rows, int64_t K, int num_sms) {
+  if (K < 16384) return 1;
+  int64_t S = (K / 16) / 256;
+  if (S > 8) S = 8;
+  while (S > 1 && rows * S > 2 * (int64_t)num_sms) --S;
+  return S < 1 ? 1 : (int)S;
+}
+
+// quant_act_kernel over `rows` rows, each shared by a cluster of S CTAs.
+template <bool BF16, int OUT>
+cudaError_t launch_rows(int64_t rows, int S, int threads, cudaStream_t stream, const void* X, int64_t K, bool vec,
+                        int8_t* xq, float* s, uint4* xop, const X8Out& o8) {
+  if (S <= 1) {
+    quant_act_kernel<BF16, OUT><<<(unsigned)rows, threads, 0, stream>>>(X, K, vec, xq, s, xop, o8);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(rows * S));
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, quant_act_kernel<BF16, OUT>, X, K, vec, xq, s, xop, o8);
+}
+
+int threads_for(int64_t work) {
+  int threads = (int)((work + 31) / 32 * 32);
+  if (threads > 1024) threads = 1024;
+  if (threads < 64) threads = 64;
+  return threads;
+}
+
+}  // namespace
+
 cudaError_t launch_quant_act(const void* X, bool bf16, int64_t M, int64_t K, int8_t* xq, float* s, int num_sms,
                              uint32_t* err, cudaStream_t stream, bool test_stall) {
   if (reinterpret_cast<uintptr_t>(X) % 16 == 0 && reinterpret_cast<uintptr_t>(xq) % 16 == 0) {
@@ -755,13 +855,11 @@ cudaError_t launch_quant_act(const void* X, bool bf16, int64_t M, int64_t K, int
   const int esize = bf16 ? 2 : 4;
   const bool vec = (K * esize) % 16 == 0;
   const int64_t work = vec ? K * esize / 16 : K;
-  int threads = (int)((work + 31) / 32 * 32);
-  if (threads > 1024) threads = 1024;
-  if (threads < 32) threads = 32;
+  const int S = 1;  // one CTA per row (see row_split)
+  const int threads = threads_for((work + S - 1) / S);
   const X8Out none{};
-  if (bf16) quant_act_kernel<true, 0><<<(unsigned)M, threads, 0, stream>>>(X, K, vec, xq, s, nullptr, none);
-  else quant_act_kernel<false, 0><<<(unsigned)M, threads, 0, stream>>>(X, K, vec, xq, s, nullptr, none);
-  return cudaGetLastError();
+  return bf16 ? launch_rows<true, 0>(M, S, threads, stream, X, K, vec, xq, s, nullptr, none)
+              : launch_rows<false, 0>(M, S, threads, stream, X, K, vec, xq, s, nullptr, none);
 }
 
 cudaError_t launch_quant_act_x16(const void* X, bool bf16, int64_t M, int64_t K, int8_t* xq, float* s, void* x16,
@@ -781,16 +879,14 @@ cudaError_t launch_quant_act_x16(const void* X, bool bf16, int64_t M, int64_t K,
 
 cudaError_t launch_quant_act_x8(const void* X, bool bf16, int64_t M, int64_t K, int8_t* xq, float* s, void* ws,
                                 int num_sms, cudaStream_t stream) {
-  int threads = (int)((K / 16 + 31) / 32 * 32);
-  if (threads > 1024) threads = 1024;
-  if (threads < 64) threads = 64;
   const int BN = gemm_f8_token_tile(M);
   const X8Out o8{f8_operand(ws), f8_counters(ws, M, K, num_sms), num_sms, M, gemm_f8_kblocks(K), BN,
                  f8_sums(ws, M, K, num_sms)};
-  const unsigned grid = (unsigned)((M + BN - 1) / BN * BN);  // every token of the last tile
-  if (bf16) quant_act_kernel<true, 2><<<grid, threads, 0, stream>>>(X, K, true, xq, s, nullptr, o8);
-  else quant_act_kernel<false, 2><<<grid, threads, 0, stream>>>(X, K, true, xq, s, nullptr, o8);
-  return cudaGetLastError();
+  const int64_t rows = (M + BN - 1) / BN * BN;  // every token of the last tile
+  const int S = row_split(rows, K, num_sms);
+  const int threads = threads_for((K / 16 + S - 1) / S);
+  return bf16 ? launch_rows<true, 2>(rows, S, threads, stream, X, K, true, xq, s, nullptr, o8)
+              : launch_rows<false, 2>(rows, S, threads, stream, X, K, true, xq, s, nullptr, o8);
 }
 
 }  // namespace bl
