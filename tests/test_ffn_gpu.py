@@ -79,28 +79,31 @@ def test_rmsnorm_quant_act_mixed_exponents_exact_mean(bl):
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-def test_rmsnorm_quant_act_unaligned(bl, dtype):
-    """gain and X views that are not 16-byte aligned take the element-wise path"""
+@pytest.mark.parametrize("M", [3, 600])
+def test_rmsnorm_quant_act_unaligned(bl, dtype, M):
+    """gain and X views that are not 16-byte aligned take the element-wise path
+    (with many tokens too)"""
     K = 1024
-    g = torch.Generator().manual_seed(5)
-    Xb = (torch.randn((3 * K + 1,), generator=g) * 2.0).to(dtype)
+    g = torch.Generator().manual_seed(5 + M)
+    Xb = (torch.randn((M * K + 1,), generator=g) * 2.0).to(dtype)
     gb = torch.rand((K + 1,), generator=g) + 0.5
-    X = Xb[1:].view(3, K)  # starts one element in
+    X = Xb[1:].view(M, K)  # starts one element in
     gain = gb[1:]
     xq_ref, s_ref = oracle.rmsnorm_quant_act(X.to(torch.float32).numpy(), gain=gain.numpy())
-    xq, s = bl.bitlinear_rmsnorm_quant_act(Xb.cuda()[1:].view(3, K), gain=gb.cuda()[1:])
+    xq, s = bl.bitlinear_rmsnorm_quant_act(Xb.cuda()[1:].view(M, K), gain=gb.cuda()[1:])
     torch.cuda.synchronize()
     assert np.array_equal(xq.cpu().numpy(), xq_ref)
     assert np.array_equal(s.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("M", [256, 1000])
+@pytest.mark.parametrize("M", [256, 1000, 2051])
 @pytest.mark.parametrize("K", [16, 2560, 6912])
 @pytest.mark.parametrize("with_gain", [False, True])
 def test_rmsnorm_quant_act_many_tokens(bl, dtype, M, K, with_gain):
     """many tokens, special rows (zero, squares overflowing and underflowing
-    fp32, large) spread over different CTAs"""
+    fp32, large) spread over different CTAs; from 2048 tokens with rows of at
+    most 8 KB one warp per row (M = 2051 leaves the last CTA three rows)"""
     g = torch.Generator().manual_seed(M + K + with_gain)
     X = torch.randn((M, K), generator=g) * 3.0
     for r, f in ((0, 0.0), (M // 3, 1e30), (M // 2, 1e-40), (M - 1, 1e4)):
@@ -175,13 +178,15 @@ def test_ffn_chain(bl, M):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 300, 1024), (4, 999, 2560), (16, 1000, 2560), (64, 700, 8192 + 64),
-                                   (97, 2000, 640), (176, 3000, 8192), (300, 19000, 128)])
+                                   (97, 2000, 640), (176, 3000, 8192), (300, 19000, 128), (1030, 500, 6912),
+                                   (2051, 300, 640)])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("with_gain,relu2", [(False, False), (True, True)])
 def test_rmsnorm_quant_forward_ws_every_path(bl, M, N, K, dtype, with_gain, relu2):
     """the FFN's second BitLinear in one call, on each route (GEMV after the
     normalising kernel; the normalising kernel writing the fp8 GEMM's split
-    operand, or the fp16 operand of the stream-K or persistent GEMM): x_q and s
+    operand, or the fp16 operand of the stream-K or persistent GEMM, from 2048
+    tokens with short rows one warp per row): x_q and s
     bit-exact against the oracle's RMS-norm quantisation, acc and y bit-exact
     against the oracle's forward on them; special rows included"""
     rng = np.random.default_rng(M * 7 + N + K)
