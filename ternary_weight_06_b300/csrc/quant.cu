@@ -474,17 +474,33 @@ __global__ void __launch_bounds__(1024) rmsnorm_quant_act_kernel(const void* __r
   }
 }
 
+// fp32(x * s) rounded half to even by one fp32 add of 1.5 * 2^23: while
+// |x * s| < 2^22 the sum is 1.5 * 2^23 + rint(x * s) exactly (its ulp is 1,
+// and 1.5 * 2^23 is even, so ties go to the even integer), and the low byte
+// of its bits is the integer's two's-complement low byte.  For finite inputs
+// |x * s| <= 127 * (1 + 2^-24)^2, so this is the code of q8 (whose clamp never
+// acts) without the quarter-rate float-to-int conversion.
+__device__ __forceinline__ uint32_t q8_bits(float x, float s) {
+  return __float_as_uint(__fadd_rn(__fmul_rn(x, s), 12582912.0f));
+}
+
+// low bytes of a, b, c, d -> bytes 0..3 of one word
+__device__ __forceinline__ uint32_t pack_low_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  return __byte_perm(__byte_perm(a, b, 0x0040u), __byte_perm(c, d, 0x0040u), 0x5410u);
+}
+
 // Many tokens: the same normalisation and quantisation with one warp per row
 // (kRmsRowWarps rows per CTA).  With one CTA per row, every row waits on three
 // block barriers and on the one-warp finish while its other warps idle, and an
 // SM holds only a few rows; a warp per row needs no block barrier (the finish
 // is warp-wide already) and keeps many rows in flight per SM.  Each warp has
 // its own buckets; the passes, their arithmetic and therefore x_q, s and the
-// operand are those of rmsnorm_quant_act_kernel bit for bit.  Needs the
-// 16-byte path (rows, gain and x_q aligned; OUT == 1: K % 16 == 0).
+// operand are those of rmsnorm_quant_act_kernel bit for bit (its codes via
+// q8_bits: |x_n| <= max|x_n| = a and s = 127 / a bound |x_n * s| as there).
+// Needs the 16-byte path (rows, gain and x_q aligned; OUT == 1: K % 16 == 0).
 constexpr int kRmsRowWarps = 4;
 // It serves from 2048 tokens with rows of at most 8 KB (2048 x 2560 bf16:
-// 25.5 against 33.7 us; 8192 x 2560: 83.5 against 122 us).  With fewer rows
+// 24.8 against 33.7 us; 8192 x 2560: 81.5 against 122 us).  With fewer rows
 // per SM, or longer rows, one CTA per row is faster (512 x 2560 bf16: 18.7
 // against 10.8 us; 600 x 28672: 206 against 86 us; 2048 x 6912 fp32: equal).
 // Its three passes cost about 60 instructions per element (the IEEE
@@ -583,10 +599,10 @@ __global__ void __launch_bounds__(32 * kRmsRowWarps) rmsnorm_quant_rows_kernel(
         load_gain(c, g);
         uint32_t q[kPer];
 #pragma unroll
-        for (int i = 0; i < kPer; ++i) q[i] = q8(__fdiv_rn(__fmul_rn(x[i], g[i]), r), sg);
+        for (int i = 0; i < kPer; ++i) q[i] = q8_bits(__fdiv_rn(__fmul_rn(x[i], g[i]), r), sg);
 #pragma unroll
         for (int v = 0; v < kPer / 4; ++v)
-          nat[c2 * (kPer / 4) + v] = q[4 * v] | (q[4 * v + 1] << 8) | (q[4 * v + 2] << 16) | (q[4 * v + 3] << 24);
+          nat[c2 * (kPer / 4) + v] = pack_low_bytes(q[4 * v], q[4 * v + 1], q[4 * v + 2], q[4 * v + 3]);
       }
       const uint4 q4 = make_uint4(nat[0], nat[1], nat[2], nat[3]);
       reinterpret_cast<uint4*>(out)[gq] = q4;
@@ -603,15 +619,12 @@ __global__ void __launch_bounds__(32 * kRmsRowWarps) rmsnorm_quant_rows_kernel(
       load_gain(c, g);
       uint32_t q[kPer];
 #pragma unroll
-      for (int i = 0; i < kPer; ++i) q[i] = q8(__fdiv_rn(__fmul_rn(x[i], g[i]), r), sg);
-      if (BF16) {
-        uint2 o;
-        o.x = q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24);
-        o.y = q[4] | (q[5] << 8) | (q[6] << 16) | (q[7] << 24);
-        reinterpret_cast<uint2*>(out)[c] = o;
-      } else {
-        reinterpret_cast<uint32_t*>(out)[c] = q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24);
-      }
+      for (int i = 0; i < kPer; ++i) q[i] = q8_bits(__fdiv_rn(__fmul_rn(x[i], g[i]), r), sg);
+      if (BF16)
+        reinterpret_cast<uint2*>(out)[c] = make_uint2(pack_low_bytes(q[0], q[1], q[2], q[3]),
+                                                      pack_low_bytes(q[4], q[5], q[6], q[7]));
+      else
+        reinterpret_cast<uint32_t*>(out)[c] = pack_low_bytes(q[0], q[1], q[2], q[3]);
     }
   }
 }
@@ -648,21 +661,6 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
-}
-
-// fp32(x * s) rounded half to even by one fp32 add of 1.5 * 2^23: while
-// |x * s| < 2^22 the sum is 1.5 * 2^23 + rint(x * s) exactly (its ulp is 1,
-// and 1.5 * 2^23 is even, so ties go to the even integer), and the low byte
-// of its bits is the integer's two's-complement low byte.  For finite inputs
-// |x * s| <= 127 * (1 + 2^-24)^2, so this is the code of q8 (whose clamp never
-// acts) without the quarter-rate float-to-int conversion.
-__device__ __forceinline__ uint32_t q8_bits(float x, float s) {
-  return __float_as_uint(__fadd_rn(__fmul_rn(x, s), 12582912.0f));
-}
-
-// low bytes of a, b, c, d -> bytes 0..3 of one word
-__device__ __forceinline__ uint32_t pack_low_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  return __byte_perm(__byte_perm(a, b, 0x0040u), __byte_perm(c, d, 0x0040u), 0x5410u);
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
