@@ -218,7 +218,7 @@ bl_status bitlinear_quant_act(const void* X, bl_dtype dtype, int64_t M, int64_t 
  * Results are unspecified where X holds a non-finite value or X * gain
  * overflows fp32.  A row whose mean square overflows fp32 gives r = inf and
  * x_q = 0.  One CTA per token; rows and gains that are 16-byte aligned take a
- * vectorised path with the same arithmetic; from 2048 tokens with rows of at
+ * vectorised path with the same arithmetic; from 1536 tokens with rows of at
  * most 8 KB, one warp per token (same results bit for bit).
  */
 bl_status bitlinear_rmsnorm_quant_act(const void* X, bl_dtype dtype, int64_t M, int64_t K, const float* gain,

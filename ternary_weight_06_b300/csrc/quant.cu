@@ -499,14 +499,16 @@ __device__ __forceinline__ uint32_t pack_low_bytes(uint32_t a, uint32_t b, uint3
 // q8_bits: |x_n| <= max|x_n| = a and s = 127 / a bound |x_n * s| as there).
 // Needs the 16-byte path (rows, gain and x_q aligned; OUT == 1: K % 16 == 0).
 constexpr int kRmsRowWarps = 4;
-// It serves from 2048 tokens with rows of at most 8 KB, where it measured
-// faster (warp per row / CTA per row: 2048 x 2560 bf16 24.8 / 33.7 us,
-// 8192 x 2560 81.5 / 122 us).  With fewer rows per SM, or longer rows, one
-// CTA per row is faster (512 x 2560 bf16 18.7 / 10.8 us, 600 x 28672
-// 206 / 86 us; 2048 x 6912 fp32 equal): the three passes take an estimated
-// 60 instructions per element (the IEEE division and the exact square sum),
-// so a lone warp per row is issue-bound.
-constexpr int64_t kRmsRowWarpsMinM = 2048;
+// It serves from 1536 tokens with rows of at most 8 KB, where it measured
+// faster (warp per row / CTA per row: 1536 x 2560 bf16 21.4 / 26.8 us,
+// 2048 x 2560 24.8 / 33.7 us, 8192 x 2560 81.5 / 122 us, 2048 x 4096
+// 37.2 / 46.8 us, 2048 x 2048 fp32 24.3 / 33.9 us).  With fewer rows per SM,
+// or longer rows, one CTA per row is faster (1024 x 2560 bf16 19.5 / 18.5 us,
+// 512 x 2560 18.7 / 10.8 us, 600 x 28672 206 / 86 us; 2048 x 6912 fp32
+// equal): the three passes take an estimated 60 instructions per element
+// (the IEEE division and the exact square sum), so a lone warp per row is
+// issue-bound.
+constexpr int64_t kRmsRowWarpsMinM = 1536;
 constexpr int64_t kRmsRowWarpsMaxRowBytes = 8192;
 __host__ __device__ constexpr bool rms_row_warps_serve(int64_t M, int64_t row_bytes) {
   return M >= kRmsRowWarpsMinM && row_bytes <= kRmsRowWarpsMaxRowBytes;

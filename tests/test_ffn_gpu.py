@@ -97,13 +97,14 @@ def test_rmsnorm_quant_act_unaligned(bl, dtype, M):
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("M", [256, 1000, 2051])
+@pytest.mark.parametrize("M", [256, 1000, 1537, 2051])
 @pytest.mark.parametrize("K", [16, 2560, 6912])
 @pytest.mark.parametrize("with_gain", [False, True])
 def test_rmsnorm_quant_act_many_tokens(bl, dtype, M, K, with_gain):
     """many tokens, special rows (zero, squares overflowing and underflowing
-    fp32, large) spread over different CTAs; from 2048 tokens with rows of at
-    most 8 KB one warp per row (M = 2051 leaves the last CTA three rows)"""
+    fp32, large) spread over different CTAs; from 1536 tokens with rows of at
+    most 8 KB one warp per row (M = 1537 and 2051 leave the last CTA one and
+    three rows)"""
     g = torch.Generator().manual_seed(M + K + with_gain)
     X = torch.randn((M, K), generator=g) * 3.0
     for r, f in ((0, 0.0), (M // 3, 1e30), (M // 2, 1e-40), (M - 1, 1e4)):
@@ -185,7 +186,7 @@ def test_ffn_chain(bl, M):
 def test_rmsnorm_quant_forward_ws_every_path(bl, M, N, K, dtype, with_gain, relu2):
     """the FFN's second BitLinear in one call, on each route (GEMV after the
     normalising kernel; the normalising kernel writing the fp8 GEMM's split
-    operand, or the fp16 operand of the stream-K or persistent GEMM, from 2048
+    operand, or the fp16 operand of the stream-K or persistent GEMM, from 1536
     tokens with short rows one warp per row): x_q and s
     bit-exact against the oracle's RMS-norm quantisation, acc and y bit-exact
     against the oracle's forward on them; special rows included"""
